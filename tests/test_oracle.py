@@ -1,0 +1,322 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here runs the CUDA library. Each test is chosen so that a plausible
+mistake in the oracle (a dropped term, a wrong sign or index, a transposed
+operand, a different accumulation order or precision, a wrong rounding
+rule) makes at least one of them fail.
+"""
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import allreduce as orc
+from oracle import atomic_model, protocol
+from oracle import fpformats as fp
+from tp_allreduce_persistent_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ieee_sum_cases.json")
+
+
+def _bits_array(hexes, dtype):
+    return np.array([int(h, 16) for h in hexes], dtype=fp.BITS_DTYPE[dtype])
+
+
+# ---------------------------------------------------------------- golden cases
+def test_golden_ieee_cases():
+    cases = json.load(open(GOLDEN))["cases"]
+    assert len(cases) >= 8
+    for c in cases:
+        dt = c["dtype"]
+        x = np.stack([_bits_array(r, dt) for r in c["inputs"]])
+        want = _bits_array(c["expected"], dt)
+        got = orc.allreduce(x, dt)
+        for row in got:
+            assert [hex(v) for v in row] == [hex(v) for v in want], c["name"]
+        got2 = orc.allreduce_two_shot(x, dt)
+        assert np.array_equal(got2, got), c["name"]
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+@pytest.mark.parametrize("n", range(2, 9))
+def test_rank_id_inputs_sum_to_triangle(dtype, n):
+    x = inputs.bits_of(inputs.rank_ids(n, 37, dtype))
+    y = fp.decode(orc.allreduce(x, dtype), dtype)
+    assert np.all(y == n * (n - 1) / 2)
+
+
+@pytest.mark.parametrize("dtype,lo,hi", [("fp32", -64, 64), ("fp16", -64, 64), ("bf16", -32, 32)])
+def test_integer_inputs_sum_exactly(dtype, lo, hi):
+    x = inputs.bits_of(inputs.integers(8, 4096, dtype, seed=11, lo=lo, hi=hi))
+    ints = fp.decode(x, dtype).astype(np.int64)
+    exact = ints.sum(axis=0)
+    y = fp.decode(orc.allreduce(x, dtype), dtype)
+    assert np.array_equal(y.astype(np.int64), np.broadcast_to(exact, y.shape))
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_rank_permutation_invariant_when_exact(dtype):
+    x = inputs.bits_of(inputs.integers(6, 999, dtype, seed=3, lo=-30, hi=30))
+    base = orc.allreduce(x, dtype)
+    rng = np.random.default_rng(0)
+    for _ in range(5):
+        perm = rng.permutation(6)
+        assert np.array_equal(orc.allreduce(x[perm], dtype), base)
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_all_outputs_identical_across_ranks(dtype):
+    x = inputs.bits_of(inputs.normal(5, 513, dtype, seed=4))
+    y = orc.allreduce(x, dtype)
+    assert all(np.array_equal(y[0], y[r]) for r in range(5))
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_zero_peers_return_own_input(dtype):
+    x = inputs.bits_of(inputs.normal(4, 300, dtype, seed=5))
+    x[1:] = 0
+    y = orc.allreduce(x, dtype)
+    neg_zero = {"fp32": 0x80000000, "fp16": 0x8000, "bf16": 0x8000}[dtype]
+    want = np.where(x[0] == neg_zero, 0, x[0])  # -0 + +0 = +0
+    assert np.array_equal(y[2], want.astype(y.dtype))
+
+
+# ----------------------------------------------------- brute force vs exact sum
+def _exact_sum_check(x, dtype):
+    """|oracle - exact rational sum| within the float32 recursive-summation
+    bound plus one final rounding to the dtype."""
+    n, count = x.shape
+    vals = fp.decode(x, dtype)
+    y = fp.decode(orc.allreduce(x, dtype)[0], dtype)
+    u = Fraction(1, 2 ** 24)
+    gamma = (n - 1) * u / (1 - (n - 1) * u)
+    tiny = Fraction(n - 1, 2 ** 150)  # underflow: half the float32 subnormal step per add
+    for i in range(count):
+        terms = [Fraction(float(vals[r, i])) for r in range(n)]
+        exact = sum(terms)
+        mag = sum(abs(t) for t in terms)
+        bound = gamma * mag + tiny
+        if dtype != fp.FP32:
+            bound += Fraction(float(fp.ulp(float(abs(exact) + bound), dtype))) / 2
+        assert abs(Fraction(float(y[i])) - exact) <= bound, (i, [float(t) for t in terms], float(y[i]))
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_brute_force_against_exact_rational_sum(dtype):
+    rng = np.random.default_rng(42)
+    for trial in range(40):
+        n = int(rng.integers(2, 9))
+        count = int(rng.integers(1, 68))
+        scale = float(10.0 ** rng.integers(-3, 4))
+        x = inputs.bits_of(inputs.normal(n, count, dtype, seed=100 + trial, scale=scale))
+        _exact_sum_check(x, dtype)
+
+
+def test_exact_check_is_sharp_enough_to_catch_mistakes():
+    # the bound used above must reject an oracle that drops a term, flips a
+    # sign or reads a neighbouring element
+    x = inputs.bits_of(inputs.normal(4, 64, "fp32", seed=9))
+    vals = fp.decode(x, "fp32").astype(np.float64)
+    exact = vals.sum(axis=0)
+    mag = np.abs(vals).sum(axis=0)
+    bound = 3 * 2.0 ** -24 * mag * 1.01
+    wrong = [vals[:3].sum(0), vals[0] - vals[1] + vals[2] + vals[3],
+             vals[0] + vals[1] + vals[2] + np.roll(vals[3], 1)]
+    for w in wrong:
+        assert np.any(np.abs(w - exact) > bound)
+
+
+# ---------------------------------------------------------------- two-shot
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+@pytest.mark.parametrize("n,count", [(2, 1), (3, 7), (8, 1), (8, 9), (8, 1000), (5, 64), (7, 130)])
+def test_two_shot_equals_one_shot(dtype, n, count):
+    x = inputs.bits_of(inputs.normal(n, count, dtype, seed=count + n))
+    assert np.array_equal(orc.allreduce_two_shot(x, dtype), orc.allreduce(x, dtype))
+
+
+@pytest.mark.parametrize("n,count", [(2, 0), (2, 1), (8, 7), (8, 64), (3, 10), (8, 1025)])
+def test_shard_bounds_partition(n, count):
+    seen = []
+    per = -(-count // n) if count else 0
+    for s in range(n):
+        lo, hi = orc.shard_bounds(count, n, s)
+        assert 0 <= lo <= hi <= count
+        assert hi - lo <= per
+        seen.extend(range(lo, hi))
+    assert seen == list(range(count))
+
+
+# ---------------------------------------------------------------- chains
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+@pytest.mark.parametrize("n", [4, 8])
+def test_chain_closed_form_half(dtype, n):
+    # rank-id inputs, scale 1/2: every rank holds T = n(n-1)/2 after step 0,
+    # then each step sums n copies of half the previous result, so
+    # y_e = T * (n/2)^e exactly, until it passes the dtype's overflow
+    # threshold max + ulp/2, from which on it is +inf.
+    iters = 160
+    x = inputs.bits_of(inputs.rank_ids(n, 5, dtype))
+    y = fp.decode(orc.allreduce_iters(x, iters, dtype, chain_scale=0.5), dtype)
+    t = Fraction(n * (n - 1), 2)
+    limit = Fraction(fp.max_finite(dtype)) + Fraction(float(fp.ulp(fp.max_finite(dtype), dtype))) / 2
+    for e in range(iters):
+        exact = t * Fraction(n, 2) ** e
+        want = float(exact) if exact < limit else np.inf
+        assert np.all(y[e] == want), (e, y[e][0, 0], want)
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+@pytest.mark.parametrize("n", [4, 8])
+def test_chain_scale_one_over_n_is_stationary(dtype, n):
+    x = inputs.bits_of(inputs.integers(n, 33, dtype, seed=n, lo=-8, hi=8))
+    y = orc.allreduce_iters(x, 20, dtype, chain_scale=1.0 / n)
+    assert all(np.array_equal(y[0], y[e]) for e in range(20))
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_chain_next_halves_exactly(dtype):
+    y = inputs.bits_of(inputs.normal(1, 2000, dtype, seed=8))[0]
+    v = fp.decode(y, dtype).astype(np.float64)
+    h = fp.decode(orc.chain_next(y, 0.5, dtype), dtype).astype(np.float64)
+    normal = np.abs(v) >= 2.0 ** (fp.EMIN[dtype] + 1)
+    assert np.array_equal(h[normal], v[normal] / 2)
+
+
+def test_fresh_input_sequence_is_per_iteration():
+    x = inputs.bits_of(inputs.uniform(2, 32, "fp32", seed=0, iters=6))
+    y = orc.allreduce_iters(x, 6, "fp32")
+    for e in range(6):
+        assert np.array_equal(y[e], orc.allreduce(x[e], "fp32"))
+
+
+# ------------------------------------------------------------ format helpers
+def _structured_f32():
+    hi = np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF, 0x4000, 0xC000], dtype=np.uint32)
+    a = (hi[:, None] | lows[None, :]).ravel()
+    rng = np.random.default_rng(1)
+    b = rng.integers(0, 2 ** 32, size=2_000_000, dtype=np.uint64).astype(np.uint32)
+    return np.concatenate([a, b]).view(np.float32)
+
+
+def test_bf16_rne_matches_torch_cast():
+    f = _structured_f32()
+    ours = fp.encode_rne(f, "bf16")
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(fp.is_nan_bits(ours[nan], "bf16"))
+
+
+def test_fp16_rne_matches_torch_cast():
+    f = _structured_f32()
+    with np.errstate(over="ignore"):
+        ours = fp.encode_rne(f, "fp16")
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(fp.is_nan_bits(ours[nan], "fp16"))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_decode_encode_roundtrip_all_patterns(dtype):
+    b = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = fp.decode(b, dtype)
+    back = fp.encode_rne(v, dtype)
+    nan = np.isnan(v)
+    assert np.array_equal(back[~nan], b[~nan])
+    ref = torch.from_numpy(b.view(np.int16).copy()).view(inputs.TORCH_DTYPE[dtype]).float().numpy()
+    assert np.array_equal(v[~nan], ref[~nan])
+
+
+def test_ulp_closed_forms():
+    assert fp.ulp(1.0, "fp32") == 2.0 ** -23
+    assert fp.ulp(1.0, "fp16") == 2.0 ** -10
+    assert fp.ulp(1.0, "bf16") == 2.0 ** -7
+    assert fp.ulp(1.5, "bf16") == 2.0 ** -7
+    assert fp.ulp(2.0, "bf16") == 2.0 ** -6
+    assert fp.ulp(65504.0, "fp16") == 32.0
+    assert fp.ulp(0.0, "fp16") == 2.0 ** -24
+    assert fp.ulp(0.0, "fp32") == 2.0 ** -149
+    assert fp.ulp(0.0, "bf16") == 2.0 ** -133
+    assert fp.ulp(-3.0, "fp32") == 2.0 ** -22
+    assert fp.max_finite("fp16") == 65504.0
+    assert fp.max_finite("bf16") == float(np.float32(3.3895314e38))
+
+
+# ------------------------------------------------------ atomic-path tolerance
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_atomic_tolerance_admits_every_arrival_order(dtype):
+    rng = np.random.default_rng(7)
+    x = inputs.bits_of(inputs.normal(8, 2000, dtype, seed=12))
+    want = orc.allreduce(x, dtype)
+    worst = 0.0
+    for _ in range(12):
+        order = rng.permutation(8)
+        got = atomic_model.atomic_sum(x, order, dtype)
+        ok, _, rel = orc.compare_atomic(np.stack([got] * 8), want, x, dtype)
+        assert ok
+        worst = max(worst, rel)
+    assert worst > 0.0 or dtype == "fp32"  # 16-bit atomics do round differently
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_atomic_tolerance_rejects_a_lost_contribution(dtype):
+    x = inputs.bits_of(inputs.normal(8, 500, dtype, seed=13))
+    want = orc.allreduce(x, dtype)
+    lost = orc.allreduce(x[:7], dtype)[:1]
+    ok, _, _ = orc.compare_atomic(np.concatenate([lost] * 8), want, x, dtype)
+    assert not ok
+
+
+def test_atomic_tolerance_closed_form():
+    x = np.stack([fp.encode_rne(np.array([1.0], np.float32), "bf16")] * 2)
+    assert orc.atomic_tolerance(x, "bf16")[0] == 2.0 ** -6  # (N-1) ulp(2) in bf16
+
+
+def test_atomic_model_of_identical_values_matches_oracle():
+    # n copies of one value: every order gives the same partial sums k*v
+    x = np.stack([fp.encode_rne(np.array([0.3, -1.7, 5.0], np.float32), "fp32")] * 4)
+    for order in ([0, 1, 2, 3], [3, 2, 1, 0]):
+        assert np.array_equal(atomic_model.atomic_sum(x, order, "fp32"), orc.allreduce(x, "fp32")[0])
+
+
+# -------------------------------------------------------- protocol constants
+def test_ll_line_halves_bandwidth_and_doubles_staging():
+    assert protocol.ll_payload_fraction() == 0.5
+    assert protocol.ll_staging_bytes(16384) == 32768
+    assert protocol.ll_staging_bytes(12) == 32
+
+
+def test_ll128_flag_overhead_matches_page_percentages():
+    # "about 1.5% in FP16, about 3% in FP32"
+    assert abs(protocol.ll128_overhead("fp16") * 100 - 1.5) < 0.1
+    assert abs(protocol.ll128_overhead("fp32") * 100 - 3.0) < 0.15
+    assert protocol.ll128_payload_elems("fp16") == 63
+    assert protocol.ll128_payload_elems("bf16") == 63
+    assert protocol.ll128_payload_elems("fp32") == 31
+    assert protocol.LL128_LINE_BYTES == protocol.LL128_GROUP_THREADS * 16
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_ll128_staging_is_about_d_over_n(dtype):
+    n = 8
+    for nbytes in (1 << 20, 1 << 22):
+        count = nbytes // fp.ELEM_BYTES[dtype]
+        s = protocol.ll128_round_staging_bytes(count, n, dtype)
+        ratio = s / (nbytes / n)
+        assert 1.0 < ratio < 1.0 + 1.5 * protocol.ll128_overhead(dtype)
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_sentinel_is_a_negative_nan(dtype):
+    b = np.array([protocol.sentinel_bits(dtype)], dtype=fp.BITS_DTYPE[dtype])
+    v = fp.decode(b, dtype)
+    assert np.isnan(v[0]) and np.signbit(v[0])
+    assert protocol.sentinel_refilled(np.full(10, protocol.sentinel_bits(dtype), fp.BITS_DTYPE[dtype]), dtype)
+    assert not protocol.sentinel_refilled(np.zeros(10, fp.BITS_DTYPE[dtype]), dtype)
