@@ -1,0 +1,193 @@
+/*
+ * llar: low-latency sum AllReduce over N virtual ranks on one GPU.
+ *
+ * C ABI. Every argument is a plain pointer, size or integer; no framework
+ * types cross this boundary. A `stream` argument is a cudaStream_t passed
+ * as `void*` (NULL = the legacy default stream).
+ *
+ * The operation, from the pages this library restates:
+ *  - AllReduce: afterwards every rank holds the complete aggregated result
+ *    ("zcube network architecture for LLM inference", collectives table,
+ *    All-Reduce row); in tensor parallelism the aggregation is the sum of
+ *    the ranks' partial outputs (same page, "Why does Tensor Parallel
+ *    affect every token").
+ *  - One-shot, or two-shot = ReduceScatter then AllGather ("Every
+ *    Microsecond Matters: Achieving Near Speed-of-Light Latency in GPU
+ *    Collectives", summary page, technique 4).
+ *  - Signalling without a global memory barrier (same page, techniques
+ *    1-4: LL flag-in-data, sentinel, bidirectional double buffering,
+ *    two-shot LL128 atomics).
+ *
+ * Virtual ranks: rank r is a group of CTAs of one persistent kernel, with
+ * its own input, output and staging buffers in device memory; ranks signal
+ * each other through L2 with relaxed/acquire/release loads, stores and
+ * reductions at GPU scope.
+ *
+ * Numerics: every fixed-order protocol (LL, SENTINEL, FIXED_*) adds the
+ * ranks in order 0..N-1 in float32 and rounds once (roundTiesToEven) to the
+ * element type, so its result is bit-identical to that definition.
+ * LL128_ATOMIC adds with floating-point atomics in the element type in
+ * arrival order; its result is not deterministic (technique 4 says so).
+ *
+ * Errors: calls return an llar_status_t. Invalid arguments are rejected
+ * before any device work. Every device-side wait is bounded by a timeout
+ * (llar_set_timeout_ns); a wait that runs out records LLAR_ERR_TIMEOUT
+ * with the rank, CTA and epoch in a status word, the kernel returns, and
+ * every later call reports LLAR_ERR_TIMEOUT until llar_reset().
+ *
+ * Concurrency: one process-global context. Calls on it must be ordered
+ * (one stream, or streams ordered by events): two of its kernels running
+ * at once would share staging and race.
+ */
+#ifndef LLAR_H
+#define LLAR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { LLAR_F32 = 0, LLAR_F16 = 1, LLAR_BF16 = 2 } llar_dtype_t;
+
+typedef enum {
+  LLAR_PROTO_AUTO = 0,          /* pick by size, see llar_select_protocol */
+  LLAR_PROTO_LL = 1,            /* one-shot, 8 B data + 8 B flag per 16 B line (technique 1) */
+  LLAR_PROTO_SENTINEL = 2,      /* one-shot, -NaN prefilled staging, chunked and
+                                   double-buffered with implicit credits (techniques 2, 3) */
+  LLAR_PROTO_LL128_ATOMIC = 3,  /* two-shot, atomic ReduceScatter into 128 B lines with a
+                                   count flag, LL AllGather (technique 4); nondeterministic */
+  LLAR_PROTO_FIXED_ONESHOT = 4, /* one-shot, every rank reads all inputs directly */
+  LLAR_PROTO_FIXED_TWOSHOT = 5  /* two-shot, owner of each segment reads all inputs
+                                   directly and writes every rank's output */
+} llar_proto_t;
+
+typedef enum {
+  LLAR_OK = 0,
+  LLAR_ERR_INVALID = 1,     /* bad argument (null/misaligned pointer, aliasing, bad rank count) */
+  LLAR_ERR_NOT_INIT = 2,    /* no context (llar_init not called, or destroyed) */
+  LLAR_ERR_TOO_LARGE = 3,   /* count * element size exceeds the staging sized at init */
+  LLAR_ERR_UNSUPPORTED = 4, /* dtype/protocol/mode combination not provided */
+  LLAR_ERR_OCCUPANCY = 5,   /* the N x G CTAs cannot all be resident at once */
+  LLAR_ERR_CUDA = 6,        /* a CUDA runtime call failed (no device, out of memory, ...) */
+  LLAR_ERR_TIMEOUT = 7      /* a device-side wait ran out; see llar_get_status */
+} llar_status_t;
+
+typedef enum {
+  LLAR_INJECT_NONE = 0,
+  LLAR_INJECT_SKIP_PUSH = 1, /* the chosen rank never sends: its peers' waits run out */
+  LLAR_INJECT_POISON = 2,    /* the chosen rank sends lines whose signal never completes */
+  LLAR_INJECT_DELAY = 3      /* the chosen rank sleeps ~20 us before each send; results stay exact */
+} llar_inject_t;
+
+/* Create the context: `nranks` virtual ranks (2..8), element type `dtype`
+ * (llar_dtype_t), messages up to `max_bytes` per rank. Allocates and
+ * initialises all staging (LL lines zeroed, sentinel slots filled with the
+ * all-ones -NaN pattern, LL128 lines zeroed), the epoch counter and the
+ * status word. Returns LLAR_ERR_INVALID for a second init without
+ * llar_destroy, LLAR_ERR_CUDA if no device or memory is available. */
+int llar_init(int nranks, int dtype, size_t max_bytes);
+
+/* Free everything llar_init allocated. Synchronises the device first. */
+int llar_destroy(void);
+
+/* One AllReduce. in[r] / out[r] (host arrays of N device pointers, copied
+ * at call time) are rank r's input and output, each `count` elements,
+ * 16-byte aligned, owned by the caller. out[r] must not alias any in[q].
+ * On return the work is queued on `stream`; out[r] holds the sum of all
+ * in[q] once the stream reaches it. count == 0 is a no-op. */
+int llar_allreduce(const void* const* in, void* const* out, size_t count,
+                   int protocol, void* stream);
+
+/* `iters` AllReduces back to back inside ONE persistent launch, with no
+ * barrier between iterations (technique 3). Iteration e writes
+ * out[r] + e*out_stride_elems. Its input is in[r] + e*in_stride_elems, or,
+ * when chain_scale != 0 (a chain of dependent AllReduces, as across the
+ * layers of one decode step), in[r] for e == 0 and afterwards
+ * roundTiesToEven(chain_scale * output of e-1), kept in library memory.
+ * The output of iteration e is identical to llar_allreduce on that input. */
+int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
+                         int protocol, int iters, size_t in_stride_elems,
+                         size_t out_stride_elems, float chain_scale, void* stream);
+
+/* One AllReduce on HOST buffers: in_host and out_host are [N][count]
+ * contiguous arrays in host memory (pinned memory makes the copies
+ * asynchronous). Copies in, runs, copies out, all on `stream`, through
+ * device buffers the library allocates on first use; returns once the
+ * work is queued (synchronise the stream before reading out_host). */
+int llar_allreduce_host(const void* in_host, void* out_host, size_t count,
+                        int protocol, void* stream);
+
+/* The status word written by the device: LLAR_OK, or LLAR_ERR_TIMEOUT with
+ * the virtual rank, CTA and epoch of the first wait that ran out. Any
+ * pointer may be NULL. Reads the word without synchronising. */
+int llar_get_status(int* rank, int* cta, unsigned long long* epoch);
+
+/* Refill sentinel staging, zero LL and LL128 staging and the abort flag,
+ * clear the status word; epochs keep counting. Synchronises the device. */
+int llar_reset(void* stream);
+
+/* Bound on every device-side wait, in nanoseconds (default 1e9). */
+void llar_set_timeout_ns(unsigned long long ns);
+
+/* Force CTAs per rank and threads per CTA for later launches (0 = choose
+ * automatically). threads must be a multiple of 32, at most 512. */
+int llar_set_launch(int ctas_per_rank, int threads);
+
+/* Sentinel chunk size in bytes per rank (multiple of 16, at most 64 KiB;
+ * default 8 KiB): each call moves ceil(bytes / chunk) chunks through the
+ * two staging slots of every peer (technique 3). */
+int llar_set_sentinel_chunk(size_t bytes);
+
+/* Host-controlled fault injection on virtual rank `rank` (llar_inject_t);
+ * LLAR_INJECT_NONE switches it off. No GPU fault is ever raised: the
+ * affected waits end through their timeout. */
+int llar_debug_inject(int rank, int mode);
+
+/* Speed-of-light latency of one AllReduce on this GPU, measured as the
+ * pages define it ("Every Microsecond Matters", summary page, the
+ * speed-of-light paragraph: 2 x L2 round trip + one remote write).
+ * l2_rt_us: median dependent-load latency of a pointer chase over a 16 MB
+ * buffer resident in L2, one chasing thread per SM; write_us: half the
+ * median round trip of a store-to-observe ping-pong between CTA pairs on
+ * different SMs; sol_us = 2 * l2_rt_us + write_us. Needs llar_init. */
+int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us);
+
+/* The raw measurements behind llar_sol_probe. Arrays hold at least 256
+ * (chase) and 128 (pairs) entries. chase_ns[i]: ns per dependent load of
+ * the chasing thread on SM chase_smid[i]; rt_ns[k]: ns per round trip of
+ * pair k between SMs smid_a[k] and smid_b[k] (0 if its wait ran out). */
+int llar_sol_probe_detail(double* chase_ns, int* chase_smid, int* nchase, double* rt_ns,
+                          int* smid_a, int* smid_b, int* npairs);
+
+/* Location of a protocol's staging (for state checks): base device
+ * pointer, bytes between consecutive ranks' regions, and bytes used per
+ * rank. For LLAR_PROTO_LL128_ATOMIC this is the line staging only. */
+int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes,
+                 size_t* rank_bytes);
+
+/* Host-only layout query (no device needed): bytes per signalling line,
+ * data elements per line, and staging bytes per rank that `protocol`
+ * needs for `count` elements of `dtype` over `nranks` ranks. */
+int llar_layout(int protocol, int dtype, int nranks, size_t count,
+                size_t* line_bytes, size_t* payload_elems_per_line,
+                size_t* staging_bytes_per_rank);
+
+/* The protocol LLAR_PROTO_AUTO picks for this size (host-only). */
+int llar_select_protocol(int nranks, int dtype, size_t count);
+
+/* Epoch the next launch starts from; strictly increasing, never reset. */
+unsigned long long llar_epoch(void);
+
+/* Launch shape of the most recent launch: protocol used, CTAs per rank,
+ * threads per CTA, iterations. Any pointer may be NULL. */
+int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters);
+
+/* Static description of a status code. */
+const char* llar_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAR_H */

@@ -1,0 +1,152 @@
+"""Parity of every protocol with the CPU oracle, through the C ABI.
+
+Fixed-order protocols (LL, SENTINEL, FIXED_ONESHOT, FIXED_TWOSHOT) must
+match bit for bit; LL128_ATOMIC, whose atomic accumulation order is free,
+must stay within (N-1) ulp of the output dtype at sum_r |x_r| and be exact
+on integer-valued inputs. Every rank's output must equal every other's.
+Sizes span several CTAs, several words per thread and ragged tails.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import allreduce as orc
+from tp_allreduce_persistent_b300 import inputs, llar
+
+from gpu_util import allreduce, allreduce_iters, context
+
+pytestmark = pytest.mark.gpu
+
+FIXED_ORDER = ["ll", "sentinel", "fixed_oneshot", "fixed_twoshot"]
+DTYPES = ["fp32", "fp16", "bf16"]
+COUNTS = [1, 3, 8, 31, 64, 129, 1000, 4099, 16389]
+
+
+def _ranks_identical(y):
+    assert all(np.array_equal(y[0], y[r]) for r in range(1, y.shape[0]))
+
+
+@pytest.mark.parametrize("proto", FIXED_ORDER)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_fixed_order_bit_exact(proto, dtype, n):
+    with context(n, dtype, 1 << 20):
+        for i, count in enumerate(COUNTS):
+            x = inputs.normal(n, count, dtype, seed=1000 + 17 * n + i)
+            got = allreduce(x, dtype, proto)
+            want = orc.allreduce(inputs.bits_of(x), dtype)
+            assert np.array_equal(got, want), (proto, dtype, n, count)
+            _ranks_identical(got)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_ll128_within_tolerance(dtype, n):
+    with context(n, dtype, 1 << 20):
+        for i, count in enumerate(COUNTS):
+            x = inputs.normal(n, count, dtype, seed=2000 + 17 * n + i)
+            got = allreduce(x, dtype, "ll128")
+            xb = inputs.bits_of(x)
+            ok, err, rel = orc.compare_atomic(got, orc.allreduce(xb, dtype), xb, dtype)
+            assert ok, (dtype, n, count, err, rel)
+            _ranks_identical(got)
+
+
+@pytest.mark.parametrize("dtype,lo,hi", [("fp32", -64, 64), ("fp16", -64, 64), ("bf16", -32, 32)])
+def test_ll128_exact_on_integers(dtype, lo, hi):
+    with context(8, dtype, 1 << 20):
+        for count in (63, 1000, 32768):
+            x = inputs.integers(8, count, dtype, seed=count, lo=lo, hi=hi)
+            got = allreduce(x, dtype, "ll128")
+            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
+
+
+@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128"])
+def test_rank_id_inputs(proto):
+    for n in (2, 8):
+        with context(n, "bf16", 1 << 16):
+            x = inputs.rank_ids(n, 777, "bf16")
+            got = allreduce(x, "bf16", proto)
+            assert np.all(got == inputs.bits_of(torch.full((1,), n * (n - 1) / 2).to(torch.bfloat16))[0])
+
+
+@pytest.mark.parametrize("proto,shapes", [
+    ("ll", [(1, 32), (3, 64), (7, 96), (18, 512)]),
+    ("sentinel", [(1, 32), (2, 64), (5, 128), (16, 256)]),
+    ("ll128", [(1, 32), (3, 64), (9, 256), (18, 512)]),
+    ("fixed_oneshot", [(1, 32), (4, 64), (37, 256)]),
+    ("fixed_twoshot", [(1, 32), (4, 96), (74, 256)]),
+])
+def test_launch_shapes(proto, shapes):
+    # several words per thread, idle CTAs, uneven splits
+    dtype, n = "fp16", 4
+    with context(n, dtype, 1 << 20):
+        for g, t in shapes:
+            llar.llar_set_launch(g, t)
+            for count in (5, 2053, 70001):
+                x = inputs.normal(n, count, dtype, seed=g * 1000 + t + count)
+                got = allreduce(x, dtype, proto)
+                xb = inputs.bits_of(x)
+                want = orc.allreduce(xb, dtype)
+                if proto == "ll128":
+                    assert orc.compare_atomic(got, want, xb, dtype)[0]
+                else:
+                    assert np.array_equal(got, want), (g, t, count)
+
+
+@pytest.mark.parametrize("chunk", [16, 256, 4096, 65536])
+def test_sentinel_chunk_sizes(chunk):
+    dtype, n = "bf16", 8
+    with context(n, dtype, 1 << 20):
+        llar.llar_set_sentinel_chunk(chunk)
+        for count in (9, 3000, 65536 + 3):
+            x = inputs.normal(n, count, dtype, seed=chunk + count)
+            got = allreduce(x, dtype, "sentinel")
+            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
+
+
+@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_iters_fresh_inputs(proto, dtype):
+    n, iters = 4, 9
+    with context(n, dtype, 1 << 20):
+        for count in (13, 4096, 9001):
+            x = inputs.uniform(n, count, dtype, seed=count, iters=iters)
+            got = allreduce_iters(x, dtype, proto, iters)
+            xb = inputs.bits_of(x)
+            want = orc.allreduce_iters(xb, iters, dtype)
+            if proto == "ll128":
+                for e in range(iters):
+                    assert orc.compare_atomic(got[e], want[e], xb[e], dtype)[0], e
+            else:
+                assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("proto", FIXED_ORDER)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("scale", [0.5, 0.25])
+def test_chain_bit_exact(proto, dtype, scale):
+    n, iters = 4, 24
+    with context(n, dtype, 1 << 20):
+        for count in (7, 8192, 20001):
+            x = inputs.normal(n, count, dtype, seed=count, scale=0.02)
+            got = allreduce_iters(x, dtype, proto, iters, chain_scale=scale)
+            want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=scale)
+            assert np.array_equal(got, want), (proto, dtype, count)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_chain_ll128_stepwise(dtype):
+    # each step checked against the oracle applied to the GPU's own previous
+    # output (atomic results may differ in the last place, then propagate)
+    n, iters, scale = 8, 12, 0.125
+    with context(n, dtype, 1 << 20):
+        count = 65536
+        x = inputs.normal(n, count, dtype, seed=5, scale=0.02)
+        got = allreduce_iters(x, dtype, "ll128", iters, chain_scale=scale)
+        cur = inputs.bits_of(x)
+        for e in range(iters):
+            ok, err, rel = orc.compare_atomic(got[e], orc.allreduce(cur, dtype), cur, dtype)
+            assert ok, (e, err, rel)
+            cur = orc.chain_next(got[e], scale, dtype)

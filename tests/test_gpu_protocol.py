@@ -1,0 +1,200 @@
+"""Protocol state, errors, fault handling and the probes, through the C ABI.
+
+* Sentinel staging holds the all-ones (-NaN) pattern again after every call
+  ("Every Microsecond Matters", summary page, technique 2: the buffer must be
+  reset after each use).
+* LL128 line staging is all zero after every call (the owner clears each
+  line after reading it, so the next count starts from zero).
+* Epochs only grow.
+* Invalid arguments are refused before any launch.
+* A virtual rank that never sends makes its peers' waits run out: the
+  status word says TIMEOUT, nothing hangs, and after llar_reset the same
+  context computes exact results again. No GPU fault is raised.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import allreduce as orc
+from oracle import protocol as oproto
+from tp_allreduce_persistent_b300 import inputs, llar
+
+from gpu_util import allreduce, allreduce_iters, context, device_inputs, filled_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+class _Raw:
+    def __init__(self, ptr, nbytes):
+        self.__cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1",
+                                         "data": (ptr, False), "version": 3}
+
+
+def staging_bytes(protocol, n):
+    ptr, stride, used = llar.llar_staging(protocol)
+    torch.cuda.synchronize()
+    return [torch.as_tensor(_Raw(ptr + r * stride, used), device="cuda").cpu().numpy()
+            for r in range(n)]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_sentinel_staging_refilled_after_each_call(dtype):
+    n = 8
+    with context(n, dtype, 1 << 20):
+        llar.llar_set_sentinel_chunk(8192)
+        for count in (4096, 32768, 32771):
+            x = inputs.normal(n, count, dtype, seed=count, exclude_sentinel=True)
+            got = allreduce(x, dtype, "sentinel")
+            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
+            for buf in staging_bytes("sentinel", n):
+                assert np.all(buf == 0xFF)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_ll128_lines_clear_after_each_call(dtype):
+    n = 8
+    with context(n, dtype, 1 << 20):
+        for count in (100, 65536, 70001):
+            x = inputs.normal(n, count, dtype, seed=count)
+            allreduce(x, dtype, "ll128")
+            for buf in staging_bytes("ll128", n):
+                assert oproto.ll128_lines_clear(buf)
+
+
+def test_epochs_strictly_increase():
+    with context(4, "bf16", 1 << 16):
+        x = inputs.normal(4, 100, "bf16", seed=1)
+        e0 = llar.llar_epoch()
+        allreduce(x, "bf16", "ll")
+        e1 = llar.llar_epoch()
+        allreduce_iters(inputs.normal(4, 100, "bf16", seed=2, iters=5), "bf16", "ll", 5)
+        e2 = llar.llar_epoch()
+        assert e0 >= 1 and e1 == e0 + 1 and e2 == e1 + 5
+
+
+def test_layout_matches_page_constants():
+    # 8 bytes of flag per 8 bytes of data; 128-byte lines with one flag element
+    for dtype in ("fp32", "fp16", "bf16"):
+        lb, pl, st = llar.llar_layout("ll", dtype, 8, 8192)
+        e = inputs.ELEM_BYTES[dtype]
+        assert lb == 16 and pl * e == 8
+        assert st == 2 * 8 * oproto.ll_staging_bytes(8192 * e)
+        lb, pl, st = llar.llar_layout("ll128", dtype, 8, 1 << 18)
+        assert lb == oproto.LL128_LINE_BYTES and pl == oproto.ll128_payload_elems(dtype)
+        assert st == 2 * oproto.ll128_round_staging_bytes(1 << 18, 8, dtype)
+
+
+def test_invalid_arguments_rejected():
+    with context(4, "fp16", 1 << 16):
+        x = inputs.normal(4, 256, "fp16", seed=3)
+        ins = device_inputs(x)
+        outs = filled_outputs(4, 256, "fp16")
+        cases = [
+            (lambda: llar.llar_allreduce(ins, outs, 256, 9), llar.ERR_INVALID),
+            (lambda: llar.llar_allreduce(ins, [o.data_ptr() + 2 for o in outs], 200, "ll"), llar.ERR_INVALID),
+            (lambda: llar.llar_allreduce(ins, [ins[0]] + outs[1:], 256, "ll"), llar.ERR_INVALID),
+            (lambda: llar.llar_allreduce(ins, [outs[0]] * 4, 256, "ll"), llar.ERR_INVALID),
+            (lambda: llar.llar_allreduce(ins, outs, (1 << 16) // 2 + 8, "ll"), llar.ERR_TOO_LARGE),
+            (lambda: llar.llar_init(4, "fp16", 1 << 16), llar.ERR_INVALID),
+        ]
+        for fn, code in cases:
+            with pytest.raises(llar.LlarError) as ei:
+                fn()
+            assert ei.value.code == code
+    with pytest.raises(llar.LlarError) as ei:
+        llar.llar_allreduce(ins, outs, 256, "ll")
+    assert ei.value.code == llar.ERR_NOT_INIT
+
+
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128"])
+def test_dead_rank_times_out_then_recovers(proto):
+    n, dtype, count = 4, "bf16", 4096
+    with context(n, dtype, 1 << 20, timeout_ns=20_000_000):
+        x = inputs.normal(n, count, dtype, seed=4)
+        llar.llar_debug_inject(2, "skip")
+        ins = device_inputs(x)
+        outs = filled_outputs(n, count, dtype)
+        llar.llar_allreduce(ins, outs, count, proto)
+        torch.cuda.synchronize()
+        code, rank, cta, epoch = llar.llar_get_status()
+        assert code == llar.ERR_TIMEOUT and 0 <= rank < n and epoch >= 1
+        if proto != "ll128":  # in LL128 the silent rank also waits, as owner of its segment
+            assert rank != 2
+        with pytest.raises(llar.LlarError) as ei:  # sticky until reset
+            llar.llar_allreduce(ins, outs, count, proto)
+        assert ei.value.code == llar.ERR_TIMEOUT
+        llar.llar_debug_inject(-1, "none")
+        llar.llar_reset()
+        got = allreduce(x, dtype, proto)
+        want = orc.allreduce(inputs.bits_of(x), dtype)
+        if proto == "ll128":
+            assert orc.compare_atomic(got, want, inputs.bits_of(x), dtype)[0]
+        else:
+            assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128"])
+def test_poisoned_rank_times_out(proto):
+    n, dtype, count = 8, "fp16", 2048
+    with context(n, dtype, 1 << 20, timeout_ns=20_000_000):
+        llar.llar_debug_inject(5, "poison")
+        x = inputs.normal(n, count, dtype, seed=6)
+        ins = device_inputs(x)
+        outs = filled_outputs(n, count, dtype)
+        llar.llar_allreduce(ins, outs, count, proto)
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.ERR_TIMEOUT
+        llar.llar_debug_inject(-1, "none")
+        llar.llar_reset()
+        assert llar.llar_get_status()[0] == llar.OK
+
+
+@pytest.mark.parametrize("proto", ["fixed_oneshot", "fixed_twoshot"])
+def test_fixed_chain_dead_rank_times_out(proto):
+    n, dtype, count = 4, "fp32", 4096
+    with context(n, dtype, 1 << 20, timeout_ns=20_000_000):
+        llar.llar_debug_inject(1, "skip")
+        x = inputs.normal(n, count, dtype, seed=7)
+        ins = device_inputs(x)
+        outs = filled_outputs(n, count, dtype)
+        llar.llar_allreduce_iters(ins, outs, count, proto, 4, 0, 0, 0.5)
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.ERR_TIMEOUT
+        llar.llar_debug_inject(-1, "none")
+        llar.llar_reset()
+
+
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"])
+def test_delayed_rank_still_exact(proto):
+    n, dtype, count, iters = 4, "bf16", 8192, 6
+    with context(n, dtype, 1 << 20):
+        llar.llar_debug_inject(3, "delay")
+        x = inputs.normal(n, count, dtype, seed=8, scale=0.02)
+        got = allreduce_iters(x, dtype, proto, iters, chain_scale=0.5)
+        want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=0.5)
+        if proto == "ll128":
+            assert orc.compare_atomic(got[0], want[0], inputs.bits_of(x), dtype)[0]
+        else:
+            assert np.array_equal(got, want)
+
+
+def test_host_buffer_entry_point():
+    n, dtype, count = 8, "bf16", 8192
+    with context(n, dtype, 1 << 20):
+        x = inputs.normal(n, count, dtype, seed=9).pin_memory()
+        out = torch.empty_like(x).pin_memory()
+        for proto in ("ll", "sentinel", "fixed_twoshot"):
+            llar.llar_allreduce_host(x, out, count, proto)
+            torch.cuda.synchronize()
+            assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
+
+
+def test_sol_probe_is_consistent():
+    with context(2, "fp32", 1 << 12):
+        l2, wr, sol = llar.llar_sol_probe()
+        assert 0.05 < l2 < 5.0 and 0.05 < wr < 10.0
+        assert abs(sol - (2 * l2 + wr)) < 1e-9
+        d = llar.llar_sol_probe_detail()
+        assert len(d["chase_ns"]) >= 100 and all(v > 0 for v in d["rt_ns"])
+        assert all(a != b for a, b in zip(d["smid_a"], d["smid_b"]))

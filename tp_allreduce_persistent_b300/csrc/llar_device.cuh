@@ -1,0 +1,286 @@
+// Device-side building blocks: GPU-scope loads/stores/reductions in inline
+// PTX, element formats, bounded waits and error reporting.
+//
+// Memory-model notes (PTX ISA memory consistency model):
+//  * Signalling loads and stores are .relaxed.gpu: they are morally strong,
+//    go to L2 (not the non-coherent L1), and never form a data race.
+//  * A producer that must make earlier writes (a reset of a sentinel slot,
+//    zeroing of an LL128 line, data reductions before a count flag) visible
+//    before a later signal issues fence.acq_rel.gpu between them: fence
+//    followed by a strong write is a release pattern.
+//  * A consumer's completed poll (a relaxed load whose value was tested)
+//    gates its later stores through a control dependency; stores are not
+//    issued before the branch on the loaded value resolves. Where a consumer
+//    reads *other* locations after seeing a flag (LL128 count flag, fixed
+//    path ready flags) the flag load is ld.acquire.gpu.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "llar_internal.h"
+
+namespace llar {
+
+typedef unsigned long long u64;
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ u64 globaltimer_ns() {
+  u64 t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void fence_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// 16-byte scalar (.b128) relaxed store/load: one single access of 16 bytes,
+// used for LL lines {8 bytes data, 8 bytes flag}.
+__device__ __forceinline__ void st_relaxed_b128(void* p, u64 lo, u64 hi) {
+  asm volatile(
+      "{\n .reg .b128 t;\n mov.b128 t, {%1, %2};\n st.relaxed.gpu.global.b128 [%0], t;\n}"
+      :: "l"(p), "l"(lo), "l"(hi) : "memory");
+}
+__device__ __forceinline__ void ld_relaxed_b128(const void* p, u64& lo, u64& hi) {
+  asm volatile(
+      "{\n .reg .b128 t;\n ld.relaxed.gpu.global.b128 t, [%2];\n mov.b128 {%0, %1}, t;\n}"
+      : "=l"(lo), "=l"(hi) : "l"(p) : "memory");
+}
+
+// 16-byte vector relaxed store/load (four 32-bit single-copy-atomic parts).
+__device__ __forceinline__ void st_relaxed_v4(void* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const void* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ u64 ld_acquire_u64(const void* p) {
+  u64 v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed_u32(const void* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(void* p, u64 v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+// read-only streaming load (inputs that no one writes during the launch)
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// L2-coherent load (data another CTA wrote during this launch)
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// --------------------------------------------------------- element formats
+// DT: 0 = fp32, 1 = fp16, 2 = bf16 (llar_dtype_t values).
+template <int DT> struct Fmt;
+
+template <> struct Fmt<0> {
+  static constexpr int kBytes = 4;
+  static constexpr unsigned kSentinel = 0xFFFFFFFFu;
+  __device__ static __forceinline__ float to_f(unsigned b) { return __uint_as_float(b); }
+  __device__ static __forceinline__ unsigned from_f(float f) { return __float_as_uint(f); }
+  __device__ static __forceinline__ unsigned load(const char* base, size_t i) {
+    return *reinterpret_cast<const unsigned*>(base + i * 4);
+  }
+  __device__ static __forceinline__ void store(char* base, size_t i, unsigned b) {
+    *reinterpret_cast<unsigned*>(base + i * 4) = b;
+  }
+};
+template <> struct Fmt<1> {
+  static constexpr int kBytes = 2;
+  static constexpr unsigned kSentinel = 0xFFFFu;
+  __device__ static __forceinline__ float to_f(unsigned b) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+  }
+  __device__ static __forceinline__ unsigned from_f(float f) {
+    return __half_as_ushort(__float2half_rn(f));
+  }
+  __device__ static __forceinline__ unsigned load(const char* base, size_t i) {
+    return *reinterpret_cast<const unsigned short*>(base + i * 2);
+  }
+  __device__ static __forceinline__ void store(char* base, size_t i, unsigned b) {
+    *reinterpret_cast<unsigned short*>(base + i * 2) = static_cast<unsigned short>(b);
+  }
+};
+template <> struct Fmt<2> {
+  static constexpr int kBytes = 2;
+  static constexpr unsigned kSentinel = 0xFFFFu;
+  __device__ static __forceinline__ float to_f(unsigned b) { return __uint_as_float(b << 16); }
+  __device__ static __forceinline__ unsigned from_f(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  }
+  __device__ static __forceinline__ unsigned load(const char* base, size_t i) {
+    return *reinterpret_cast<const unsigned short*>(base + i * 2);
+  }
+  __device__ static __forceinline__ void store(char* base, size_t i, unsigned b) {
+    *reinterpret_cast<unsigned short*>(base + i * 2) = static_cast<unsigned short>(b);
+  }
+};
+
+// Elements of a 32-bit word: element k of word w (little endian).
+template <int DT>
+__device__ __forceinline__ unsigned word_elem(unsigned w, int k) {
+  if (Fmt<DT>::kBytes == 4) return w;
+  return (w >> (16 * k)) & 0xFFFFu;
+}
+template <int DT>
+__device__ __forceinline__ unsigned word_set(unsigned w, int k, unsigned e) {
+  if (Fmt<DT>::kBytes == 4) return e;
+  const unsigned sh = 16 * k;
+  return (w & ~(0xFFFFu << sh)) | (e << sh);
+}
+
+// acc[i] += value of element i of a packed group of 32-bit words
+template <int DT, int NW>
+__device__ __forceinline__ void accumulate(float* acc, const unsigned* w) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      acc[i * PER + k] = __fadd_rn(acc[i * PER + k], Fmt<DT>::to_f(word_elem<DT>(w[i], k)));
+}
+template <int DT, int NW>
+__device__ __forceinline__ void init_acc(float* acc, const unsigned* w) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[i * PER + k] = Fmt<DT>::to_f(word_elem<DT>(w[i], k));
+}
+// round every accumulator once (roundTiesToEven) and pack into words
+template <int DT, int NW>
+__device__ __forceinline__ void pack_acc(const float* acc, unsigned* w) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    unsigned x = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) x = word_set<DT>(x, k, Fmt<DT>::from_f(acc[i * PER + k]));
+    w[i] = x;
+  }
+}
+// next input of a chain: roundTiesToEven(scale * y), product in float32
+template <int DT, int NW>
+__device__ __forceinline__ void chain_words(const unsigned* y, unsigned* nx, float scale) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    unsigned x = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      x = word_set<DT>(x, k, Fmt<DT>::from_f(__fmul_rn(scale, Fmt<DT>::to_f(word_elem<DT>(y[i], k)))));
+    nx[i] = x;
+  }
+}
+
+// True if any element of the 16-byte vector is the sentinel pattern.
+template <int DT>
+__device__ __forceinline__ bool has_sentinel(uint4 v) {
+  if (Fmt<DT>::kBytes == 4)
+    return v.x == 0xFFFFFFFFu || v.y == 0xFFFFFFFFu || v.z == 0xFFFFFFFFu || v.w == 0xFFFFFFFFu;
+  auto h = [](unsigned w) {
+    return ((w & 0xFFFFu) == 0xFFFFu) || ((w >> 16) == 0xFFFFu);
+  };
+  return h(v.x) || h(v.y) || h(v.z) || h(v.w);
+}
+
+// Load n32 32-bit words of a vector that may run past `count` elements:
+// words (and elements) at or beyond the end read as zero.
+template <int DT, int NW>
+__device__ __forceinline__ void load_words_tail(const char* base, size_t first_elem, size_t count,
+                                                unsigned* w) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    unsigned x = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const size_t g = first_elem + i * PER + k;
+      if (g < count) x = word_set<DT>(x, k, Fmt<DT>::load(base, g));
+    }
+    w[i] = x;
+  }
+}
+template <int DT, int NW>
+__device__ __forceinline__ void store_words_tail(char* base, size_t first_elem, size_t count,
+                                                 const unsigned* w) {
+  constexpr int PER = 4 / Fmt<DT>::kBytes;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const size_t g = first_elem + i * PER + k;
+      if (g < count) Fmt<DT>::store(base, g, word_elem<DT>(w[i], k));
+    }
+}
+
+// ------------------------------------------------------------ bounded waits
+// Counts polls; every 32nd poll it reads %globaltimer (the deadline is set
+// on the first reading, so short waits never read the clock) and the
+// launch-wide abort word. expired() == true means: give up.
+struct Waiter {
+  u64 deadline = 0;
+  unsigned spins = 0;
+  __device__ __forceinline__ bool expired(const Params& p) {
+    if ((++spins & 31u) != 0) return false;
+    const u64 now = globaltimer_ns();
+    if (deadline == 0) deadline = now + p.timeout_ns;
+    if (now > deadline) return true;
+    return ld_relaxed_u32(p.abort_flag) != 0;
+  }
+};
+
+// First failing wait wins the device word and fills the host-visible status.
+__device__ __noinline__ void report_timeout(const Params& p, int rank, int cta, u64 epoch) {
+  if (atomicCAS(p.abort_flag, 0u, 7u) == 0u) {
+    volatile DevStatus* st = p.status;
+    st->rank = rank;
+    st->cta = cta;
+    st->epoch = epoch;
+    __threadfence_system();
+    st->code = 7u;
+    __threadfence_system();
+  }
+}
+
+__device__ __forceinline__ bool aborted(const Params& p) {
+  return ld_relaxed_u32(p.abort_flag) != 0;
+}
+
+// Injected sleep of the DELAY fault mode (about 20 us, bounded).
+__device__ __forceinline__ void injected_delay() {
+  for (int i = 0; i < 20; ++i) __nanosleep(1000);
+}
+
+}  // namespace llar

@@ -1,0 +1,94 @@
+// Internal types shared by the host runtime (llar_runtime.cu) and the
+// kernels (llar_kernels.cu). Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace llar {
+
+constexpr int kMaxRanks = 8;
+constexpr int kMaxThreads = 512;   // threads per CTA, upper bound of every kernel
+constexpr int kLL128Line = 128;    // bytes per LL128 line
+constexpr int kLL128Lanes = 8;     // 16-byte lanes (threads) per line
+constexpr int kLLLine = 16;        // bytes per LL line: 8 data + 8 flag
+constexpr int kAgLineBytes = 256;  // one LL128 line re-sent as 16 LL lines
+
+// fault-injection modes (values of llar_inject_t)
+constexpr int LLAR_INJECT_SKIP_ = 1;
+constexpr int LLAR_INJECT_POISON_ = 2;
+constexpr int LLAR_INJECT_DELAY_ = 3;
+
+// Written by the first device wait that runs out; lives in mapped host
+// memory so the host can read it without a device synchronisation.
+struct DevStatus {
+  unsigned int code;  // 0 = ok, else an llar_status_t
+  int rank;
+  int cta;
+  int pad;
+  unsigned long long epoch;
+};
+
+// Everything a launch needs. Passed by value as the kernel parameter.
+struct Params {
+  const char* in[kMaxRanks];  // rank inputs (iteration 0 / base)
+  char* out[kMaxRanks];       // rank outputs (iteration 0 / base)
+  size_t count;               // elements per rank
+  int nranks;
+  int G;                      // CTAs per rank
+  int iters;
+  int chain;                  // 1: next input = RNE(chain_scale * output)
+  float chain_scale;
+  size_t in_stride;           // elements between iterations' inputs
+  size_t out_stride;          // elements between iterations' outputs
+  unsigned long long epoch0;  // epoch of iteration 0 (>= 1, strictly increasing)
+
+  // staging regions (device memory), rank r's region at base + r * stride
+  char* ll;            size_t ll_stride;        // [2][N][W][16]
+  size_t ll_slot_words;                         // W for this launch's layout (max words)
+  char* sen;           size_t sen_stride;       // [2][N][CV][16]
+  int sen_chunk_vecs;                           // CV: 16-byte vectors per chunk
+  char* l128;          size_t l128_stride;      // [2][L][128]
+  char* l128ag;        size_t l128ag_stride;    // [2][N][L][256]
+  size_t l128_lines;                            // L: lines per slot
+  char* chainbuf;      size_t chain_stride;     // [2][max_bytes] per rank
+  size_t chain_slot_bytes;
+  unsigned long long* flags;                    // [N][Gmax][2] ready/done epochs
+  int flags_gmax;
+
+  unsigned long long timeout_ns;
+  int inject_rank;
+  int inject_mode;
+  unsigned int* abort_flag;  // device memory
+  DevStatus* status;         // mapped host memory (device pointer)
+};
+
+// Launchers, defined in llar_kernels.cu. Return a cudaError_t.
+cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s);
+cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_t s);
+cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s);
+cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s);
+cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s);
+
+// Largest number of CTAs of the kernel for (proto, dtype, chain) that can
+// be resident at once with `threads` threads each (0 on error).
+int max_resident_ctas(int proto, int dtype, int chain, int threads);
+
+// Speed-of-light probes: per-SM pointer-chase latency (ns per dependent
+// L2 load) and per-pair ping-pong round trips (ns per store-observe-reply).
+constexpr int kSolMaxBlocks = 256;
+struct SolResult {
+  int nchase;
+  double chase_ns[kSolMaxBlocks];
+  int chase_smid[kSolMaxBlocks];
+  int npairs;
+  double rt_ns[kSolMaxBlocks / 2];
+  int smid_a[kSolMaxBlocks / 2];
+  int smid_b[kSolMaxBlocks / 2];
+};
+// The probes use their own abort word, never the context's.
+cudaError_t run_sol(SolResult* res, unsigned long long timeout_ns);
+
+}  // namespace llar

@@ -1,0 +1,870 @@
+// Persistent AllReduce kernels over N virtual ranks, and the speed-of-light
+// probes. One launch = N x G CTAs; CTAs [r*G, (r+1)*G) are virtual rank r.
+// CTA c of rank r pairs with CTA c of every peer: all of them cover the same
+// element range, and every element position is always handled by the same
+// thread index, so a thread's program order carries the credit rule of the
+// double-buffered protocols ("Every Microsecond Matters: Achieving Near
+// Speed-of-Light Latency in GPU Collectives", summary page, technique 3:
+// receiving a chunk from a peer is the permission to send it the next one).
+// No kernel contains a grid-wide barrier; the only waits are per-line polls
+// (techniques 1, 2, 4) and, on the fixed-order chained paths, per-CTA-pair
+// epoch flags.
+#include <vector>
+
+#include "llar_device.cuh"
+
+namespace llar {
+
+// ----------------------------------------------------------- shared helpers
+template <int DT>
+__device__ __forceinline__ const char* rank_input(const Params& p, int q, int e) {
+  if (p.chain)
+    return e == 0 ? p.in[q] : p.chainbuf + (size_t)q * p.chain_stride + (size_t)(e & 1) * p.chain_slot_bytes;
+  return p.in[q] + (size_t)e * p.in_stride * Fmt<DT>::kBytes;
+}
+template <int DT>
+__device__ __forceinline__ char* rank_output(const Params& p, int q, int e) {
+  return p.out[q] + (size_t)e * p.out_stride * Fmt<DT>::kBytes;
+}
+__device__ __forceinline__ char* chain_next_buf(const Params& p, int q, int e) {
+  return p.chainbuf + (size_t)q * p.chain_stride + (size_t)((e + 1) & 1) * p.chain_slot_bytes;
+}
+
+// 8-byte word w (elements [w*PER8, (w+1)*PER8)) of a rank buffer; a word
+// that runs past `count` is read element by element, the rest as zeros.
+template <int DT>
+__device__ __forceinline__ u64 load_word8(const char* base, size_t w, size_t count) {
+  constexpr int PER8 = 8 / Fmt<DT>::kBytes;
+  if ((w + 1) * PER8 <= count) return *reinterpret_cast<const u64*>(base + w * 8);
+  unsigned x[2];
+  load_words_tail<DT, 2>(base, w * PER8, count, x);
+  return (u64)x[0] | ((u64)x[1] << 32);
+}
+template <int DT>
+__device__ __forceinline__ void store_word8(char* base, size_t w, size_t count, u64 v) {
+  constexpr int PER8 = 8 / Fmt<DT>::kBytes;
+  if ((w + 1) * PER8 <= count) {
+    *reinterpret_cast<u64*>(base + w * 8) = v;
+    return;
+  }
+  unsigned x[2] = {(unsigned)v, (unsigned)(v >> 32)};
+  store_words_tail<DT, 2>(base, w * PER8, count, x);
+}
+template <int DT>
+__device__ __forceinline__ uint4 load_vec16(const char* base, size_t v, size_t count, bool stream) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  if ((v + 1) * PER16 <= count) return stream ? ld_stream_v4(base + v * 16) : ld_cg_v4(base + v * 16);
+  unsigned x[4];
+  load_words_tail<DT, 4>(base, v * PER16, count, x);
+  return make_uint4(x[0], x[1], x[2], x[3]);
+}
+template <int DT>
+__device__ __forceinline__ void store_vec16(char* base, size_t v, size_t count, uint4 val) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  if ((v + 1) * PER16 <= count) {
+    st_v4(base + v * 16, val);
+    return;
+  }
+  unsigned x[4] = {val.x, val.y, val.z, val.w};
+  store_words_tail<DT, 4>(base, v * PER16, count, x);
+}
+
+__device__ __forceinline__ uint4 u4(const unsigned* w) { return make_uint4(w[0], w[1], w[2], w[3]); }
+
+// ============================================================ LL one-shot
+// Technique 1: each 8 bytes of data leave with an 8-byte flag (the launch
+// epoch of this AllReduce) as one 16-byte store into every peer's slot
+// [epoch & 1][source rank][word]; the receiver polls that 16-byte line
+// until the flag equals the epoch, so no separate signal and no barrier is
+// needed. Epochs only grow, so slots never need a reset.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int PER8 = 8 / EB;
+  const int N = p.nranks;
+  const int r = blockIdx.x / p.G;
+  const int c = blockIdx.x - r * p.G;
+  const size_t W = (p.count + PER8 - 1) / PER8;
+  const size_t per = (W + p.G - 1) / p.G;
+  const size_t w0 = min(W, (size_t)c * per);
+  const size_t w1 = min(W, w0 + per);
+  const bool injected = (p.inject_rank == r);
+  const size_t src_stride = p.ll_slot_words * kLLLine;
+  const size_t slot_stride = (size_t)N * src_stride;
+  char* const mine = p.ll + (size_t)r * p.ll_stride;
+  const unsigned peers = ((1u << N) - 1u) & ~(1u << r);
+
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = p.epoch0 + (u64)e;
+    const size_t slot_off = (size_t)(E & 1) * slot_stride;
+    const char* src = rank_input<DT>(p, r, e);
+    char* dst = rank_output<DT>(p, r, e);
+    if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+
+    // push my words to every peer
+    if (!(injected && p.inject_mode == LLAR_INJECT_SKIP_)) {
+      const u64 flag = (injected && p.inject_mode == LLAR_INJECT_POISON_) ? E + 2 : E;
+      for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
+        const u64 x = load_word8<DT>(src, w, p.count);
+        char* line = p.ll + slot_off + (size_t)r * src_stride + w * kLLLine;
+#pragma unroll
+        for (int q = 0; q < kMaxRanks; ++q)
+          if (q < N && q != r) st_relaxed_b128(line + (size_t)q * p.ll_stride, x, flag);
+      }
+    }
+
+    // poll, reduce in rank order, store
+    for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
+      const u64 own = load_word8<DT>(src, w, p.count);
+      const char* line = mine + slot_off + w * kLLLine;
+      u64 d[kMaxRanks];
+      unsigned pending = peers;
+      Waiter wt;
+      while (true) {
+        u64 lo[kMaxRanks], hi[kMaxRanks];
+#pragma unroll
+        for (int q = 0; q < kMaxRanks; ++q)
+          if ((pending >> q) & 1u) ld_relaxed_b128(line + (size_t)q * src_stride, lo[q], hi[q]);
+#pragma unroll
+        for (int q = 0; q < kMaxRanks; ++q)
+          if (((pending >> q) & 1u) && hi[q] == E) {
+            d[q] = lo[q];
+            pending &= ~(1u << q);
+          }
+        if (pending == 0u) break;
+        if (wt.expired(p)) {
+          report_timeout(p, r, c, E);
+          return;
+        }
+      }
+      float acc[PER8];
+      {
+        const u64 v0 = (r == 0) ? own : d[0];
+        const unsigned w2[2] = {(unsigned)v0, (unsigned)(v0 >> 32)};
+        init_acc<DT, 2>(acc, w2);
+      }
+#pragma unroll
+      for (int q = 1; q < kMaxRanks; ++q)
+        if (q < N) {
+          const u64 v = (q == r) ? own : d[q];
+          const unsigned w2[2] = {(unsigned)v, (unsigned)(v >> 32)};
+          accumulate<DT, 2>(acc, w2);
+        }
+      unsigned y[2];
+      pack_acc<DT, 2>(acc, y);
+      store_word8<DT>(dst, w, p.count, (u64)y[0] | ((u64)y[1] << 32));
+      if (p.chain) {
+        unsigned nx[2];
+        chain_words<DT, 2>(y, nx, p.chain_scale);
+        store_word8<DT>(chain_next_buf(p, r, e), w, p.count, (u64)nx[0] | ((u64)nx[1] << 32));
+      }
+    }
+  }
+}
+
+// ====================================================== sentinel one-shot
+// Technique 2 with technique 3's chunking: staging slot
+// [seq & 1][source][vector] is prefilled with the all-ones (-NaN) pattern;
+// the sender stores raw 16-byte vectors, the receiver polls until no
+// element of the vector is the sentinel, reduces, and writes the sentinel
+// back (the reset). Chunk seq+1 is pushed only after chunk seq was received
+// from every peer, so a peer's slot (seq+1) & 1 was consumed and reset in
+// its chunk seq-1. The reset is ordered before the next push by a fence.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int PER16 = 16 / EB;
+  const int N = p.nranks;
+  const int r = blockIdx.x / p.G;
+  const int c = blockIdx.x - r * p.G;
+  const size_t NV = (p.count + PER16 - 1) / PER16;
+  const size_t CV = (size_t)p.sen_chunk_vecs;
+  const size_t nchunks = (NV + CV - 1) / CV;
+  const size_t per = (CV + p.G - 1) / p.G;
+  const size_t j0 = min(CV, (size_t)c * per);
+  const size_t j1 = min(CV, j0 + per);
+  const size_t src_stride = CV * 16;
+  const size_t slot_stride = (size_t)N * src_stride;
+  char* const mine = p.sen + (size_t)r * p.sen_stride;
+  const bool injected = (p.inject_rank == r);
+  const unsigned peers = ((1u << N) - 1u) & ~(1u << r);
+  const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  unsigned long long seq = 0;
+
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = p.epoch0 + (u64)e;
+    const char* src = rank_input<DT>(p, r, e);
+    char* dst = rank_output<DT>(p, r, e);
+    const bool own_stream = !p.chain;  // user input: read-only for the launch
+    for (size_t k = 0; k < nchunks; ++k, ++seq) {
+      const size_t slot_off = (size_t)(seq & 1) * slot_stride;
+      if (seq > 0) fence_gpu();  // previous chunk's resets before this chunk's pushes
+      if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+      if (!(injected && p.inject_mode == LLAR_INJECT_SKIP_)) {
+        const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
+        for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+          const size_t v = k * CV + j;
+          if (v >= NV) break;
+          const uint4 x = poison ? ones : load_vec16<DT>(src, v, p.count, own_stream);
+          char* line = p.sen + slot_off + (size_t)r * src_stride + j * 16;
+#pragma unroll
+          for (int q = 0; q < kMaxRanks; ++q)
+            if (q < N && q != r) st_relaxed_v4(line + (size_t)q * p.sen_stride, x);
+        }
+      }
+      for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+        const size_t v = k * CV + j;
+        if (v >= NV) break;
+        const uint4 own = load_vec16<DT>(src, v, p.count, own_stream);
+        char* line = mine + slot_off + j * 16;
+        uint4 d[kMaxRanks];
+        unsigned pending = peers;
+        Waiter wt;
+        while (true) {
+          uint4 t[kMaxRanks];
+#pragma unroll
+          for (int q = 0; q < kMaxRanks; ++q)
+            if ((pending >> q) & 1u) t[q] = ld_relaxed_v4(line + (size_t)q * src_stride);
+#pragma unroll
+          for (int q = 0; q < kMaxRanks; ++q)
+            if (((pending >> q) & 1u) && !has_sentinel<DT>(t[q])) {
+              d[q] = t[q];
+              pending &= ~(1u << q);
+            }
+          if (pending == 0u) break;
+          if (wt.expired(p)) {
+            report_timeout(p, r, c, E);
+            return;
+          }
+        }
+        // reset my slot for the next use of this parity
+#pragma unroll
+        for (int q = 0; q < kMaxRanks; ++q)
+          if (q < N && q != r) st_relaxed_v4(line + (size_t)q * src_stride, ones);
+        float acc[PER16];
+        {
+          const uint4 v0 = (r == 0) ? own : d[0];
+          const unsigned w4[4] = {v0.x, v0.y, v0.z, v0.w};
+          init_acc<DT, 4>(acc, w4);
+        }
+#pragma unroll
+        for (int q = 1; q < kMaxRanks; ++q)
+          if (q < N) {
+            const uint4 vq = (q == r) ? own : d[q];
+            const unsigned w4[4] = {vq.x, vq.y, vq.z, vq.w};
+            accumulate<DT, 4>(acc, w4);
+          }
+        unsigned y[4];
+        pack_acc<DT, 4>(acc, y);
+        store_vec16<DT>(dst, v, p.count, u4(y));
+        if (p.chain) {
+          unsigned nx[4];
+          chain_words<DT, 4>(y, nx, p.chain_scale);
+          store_vec16<DT>(chain_next_buf(p, r, e), v, p.count, u4(nx));
+        }
+      }
+    }
+  }
+}
+
+// ======================================================= LL128 two-shot
+// Technique 4. Rank s owns segment s (ceil(count/N) elements). A segment
+// is carried in 128-byte lines of 8 lanes x 16 bytes; element 0 of lane 0
+// is the line's count flag, the other 128/e - 1 elements are data. Every
+// rank adds its data of segment s into owner s's line with vector
+// reductions in the element type; after a fence, lane 0 adds 1 to the
+// flag. When the owner's flag reads N, every contribution is in. The owner
+// re-sends its reduced lines to every peer as LL lines (AllGather) and
+// zeroes its lines for their next use (epoch + 2).
+template <int DT>
+__device__ __forceinline__ void red_add_v4(void* a, const unsigned* w) {
+  if (DT == 0)
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(a), "f"(__uint_as_float(w[0])), "f"(__uint_as_float(w[1])),
+                    "f"(__uint_as_float(w[2])), "f"(__uint_as_float(w[3])) : "memory");
+  else if (DT == 1)
+    asm volatile("red.relaxed.gpu.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};"
+                 :: "l"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+  else
+    asm volatile("red.relaxed.gpu.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};"
+                 :: "l"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]) : "memory");
+}
+template <int DT>
+__device__ __forceinline__ void red_add_flag(void* a, unsigned one_bits) {
+  if (DT == 0) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;"
+                 :: "l"(a), "f"(__uint_as_float(one_bits)) : "memory");
+  } else {
+    const unsigned short h = (unsigned short)one_bits;
+    if (DT == 1)
+      asm volatile("red.relaxed.gpu.global.add.noftz.f16 [%0], %1;" :: "l"(a), "h"(h) : "memory");
+    else
+      asm volatile("red.relaxed.gpu.global.add.noftz.bf16 [%0], %1;" :: "l"(a), "h"(h) : "memory");
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int V = 16 / EB;    // elements per lane
+  constexpr int EL = 128 / EB;  // elements per line
+  constexpr int P = EL - 1;     // data elements per line
+  const int N = p.nranks;
+  const int r = blockIdx.x / p.G;
+  const int c = blockIdx.x - r * p.G;
+  const size_t count = p.count;
+  const size_t seg = (count + N - 1) / N;
+  const size_t L = (seg + P - 1) / P;
+  const size_t Lc = (L + p.G - 1) / p.G;
+  const size_t l0 = min(L, (size_t)c * Lc);
+  const size_t nl = min(L, l0 + Lc) - l0;
+  const size_t items = (size_t)N * nl * kLL128Lanes;
+  const size_t T = blockDim.x;
+  const unsigned one_bits = Fmt<DT>::from_f(1.0f);
+  const unsigned n_bits = Fmt<DT>::from_f((float)N);
+  const unsigned flag_mask = (EB == 4) ? 0xFFFFFFFFu : 0xFFFFu;
+  const bool injected = (p.inject_rank == r);
+  const bool skip = injected && p.inject_mode == LLAR_INJECT_SKIP_;
+  const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
+  const size_t line_slot = p.l128_lines * (size_t)kLL128Line;
+  const size_t ag_src = p.l128_lines * (size_t)kAgLineBytes;
+  const size_t ag_slot = (size_t)N * ag_src;
+  char* const my_lines = p.l128 + (size_t)r * p.l128_stride;
+  char* const my_ag = p.l128ag + (size_t)r * p.l128ag_stride;
+  bool failed = false;
+
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = p.epoch0 + (u64)e;
+    const int slot = (int)(E & 1);
+    const char* src = rank_input<DT>(p, r, e);
+    char* dst = rank_output<DT>(p, r, e);
+    if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+
+    // ---- ReduceScatter: add my data into every owner's lines
+    if (!skip) {
+      for (size_t i = threadIdx.x; i < items; i += T) {
+        const int s = (int)(i / (nl * kLL128Lanes));
+        const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+        const size_t l = l0 + rem / kLL128Lanes;
+        const int j = (int)(rem % kLL128Lanes);
+        unsigned w[4];
+        bool any = false;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          const int pos = j * V + k;
+          const size_t sl = l * P + (size_t)pos - 1;
+          const size_t g = (size_t)s * seg + sl;
+          unsigned b = 0;
+          if (pos >= 1 && sl < seg && g < count) {
+            b = Fmt<DT>::load(src, g);
+            any = true;
+          }
+          const int word = (k * EB) / 4, sub = (EB == 4) ? 0 : (k & 1);
+          if (EB == 4) w[word] = b;
+          else w[word] = sub ? (w[word] | (b << 16)) : b;
+        }
+        if (any)
+          red_add_v4<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line + j * 16, w);
+      }
+    }
+    __syncwarp();
+    fence_gpu();  // every data reduction of this warp before its flags
+    if (!skip) {
+      for (size_t i = threadIdx.x; i < items; i += T) {
+        if ((i % kLL128Lanes) != 0) continue;
+        const int s = (int)(i / (nl * kLL128Lanes));
+        const size_t l = l0 + (i - (size_t)s * nl * kLL128Lanes) / kLL128Lanes;
+        red_add_flag<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line,
+                         poison ? 0u : one_bits);
+      }
+    }
+
+    // ---- owner: wait for count N, read, AllGather as LL lines, zero
+    for (size_t base = 0; base < items; base += T) {
+      const size_t i = base + threadIdx.x;
+      int s = -1;
+      size_t l = 0;
+      int j = 0;
+      if (i < items) {
+        s = (int)(i / (nl * kLL128Lanes));
+        const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+        l = l0 + rem / kLL128Lanes;
+        j = (int)(rem % kLL128Lanes);
+      }
+      const bool own = (s == r);
+      char* line = my_lines + slot * line_slot + l * kLL128Line;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (own) {
+        if (!failed) {
+          Waiter wt;
+          while ((ld_acquire_u32(line) & flag_mask) != n_bits) {
+            if (wt.expired(p)) {
+              report_timeout(p, r, c, E);
+              failed = true;
+              break;
+            }
+          }
+        }
+        v = ld_relaxed_v4(line + j * 16);
+      }
+      __syncwarp();  // all 8 lanes have read the flag and their data before any zeroing
+      if (own) {
+        const unsigned w[4] = {v.x, v.y, v.z, v.w};
+        unsigned nx[4];
+        if (p.chain) chain_words<DT, 4>(w, nx, p.chain_scale);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          const int pos = j * V + k;
+          const size_t sl = l * P + (size_t)pos - 1;
+          const size_t g = (size_t)r * seg + sl;
+          if (pos >= 1 && sl < seg && g < count) {
+            Fmt<DT>::store(dst, g, word_elem<DT>(w[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+            if (p.chain)
+              Fmt<DT>::store(chain_next_buf(p, r, e), g, word_elem<DT>(nx[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+          }
+        }
+        if (!skip) {
+          const u64 lo = (u64)v.x | ((u64)v.y << 32);
+          const u64 hi = (u64)v.z | ((u64)v.w << 32);
+          const u64 flag = poison ? E + 2 : E;
+          char* ag = p.l128ag + slot * ag_slot + (size_t)r * ag_src + l * kAgLineBytes + j * 32;
+#pragma unroll
+          for (int q = 0; q < kMaxRanks; ++q)
+            if (q < N && q != r) {
+              st_relaxed_b128(ag + (size_t)q * p.l128ag_stride, lo, flag);
+              st_relaxed_b128(ag + (size_t)q * p.l128ag_stride + 16, hi, flag);
+            }
+        }
+        st_relaxed_v4(line + j * 16, make_uint4(0, 0, 0, 0));
+      }
+    }
+
+    // ---- AllGather receive: poll the owners' LL lines, write my output
+    for (size_t i = threadIdx.x; i < items; i += T) {
+      const int s = (int)(i / (nl * kLL128Lanes));
+      if (s == r) continue;
+      const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+      const size_t l = l0 + rem / kLL128Lanes;
+      const int j = (int)(rem % kLL128Lanes);
+      const char* ag = my_ag + slot * ag_slot + (size_t)s * ag_src + l * kAgLineBytes + j * 32;
+      u64 lo = 0, hi = 0;
+      if (!failed) {
+        Waiter wt;
+        bool got0 = false, got1 = false;
+        while (true) {
+          u64 a0, f0, a1, f1;
+          if (!got0) ld_relaxed_b128(ag, a0, f0);
+          if (!got1) ld_relaxed_b128(ag + 16, a1, f1);
+          if (!got0 && f0 == E) { lo = a0; got0 = true; }
+          if (!got1 && f1 == E) { hi = a1; got1 = true; }
+          if (got0 && got1) break;
+          if (wt.expired(p)) {
+            report_timeout(p, r, c, E);
+            failed = true;
+            break;
+          }
+        }
+      }
+      const unsigned w[4] = {(unsigned)lo, (unsigned)(lo >> 32), (unsigned)hi, (unsigned)(hi >> 32)};
+      unsigned nx[4];
+      if (p.chain) chain_words<DT, 4>(w, nx, p.chain_scale);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int pos = j * V + k;
+        const size_t sl = l * P + (size_t)pos - 1;
+        const size_t g = (size_t)s * seg + sl;
+        if (pos >= 1 && sl < seg && g < count) {
+          Fmt<DT>::store(dst, g, word_elem<DT>(w[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+          if (p.chain)
+            Fmt<DT>::store(chain_next_buf(p, r, e), g, word_elem<DT>(nx[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+        }
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, failed)) return;
+  }
+}
+
+// ==================================================== fixed-order paths
+// Deterministic direct-read variants: the reader loads every rank's input
+// itself, adds in rank order 0..N-1 in float32 and rounds once. Inputs of a
+// launch are complete when it starts (stream order), so without a chain no
+// flag is needed. In a chain, the next input of rank q is written by rank q
+// into its double-buffered chain slot, and CTA c publishes epoch flags for
+// its range: ready[q][c] (input of epoch E is in place, and q's reads of
+// epoch E-1 are done) and, for the two-shot, done[s][c] (owner s wrote
+// segment s, range c, of every output for epoch E).
+__device__ __forceinline__ unsigned long long* flag_ptr(const Params& p, int rank, int cta, int kind) {
+  return p.flags + ((size_t)rank * p.flags_gmax + cta) * 2 + kind;
+}
+
+// Thread 0 waits until flag[q][c][kind] >= want for every q != skip_rank;
+// the result is shared with the CTA through a barrier. Returns false on timeout.
+__device__ __forceinline__ bool wait_flags(const Params& p, int skip_rank, int c, int kind, u64 want,
+                                           int my_rank, u64 E, int* s_fail) {
+  if (threadIdx.x == 0) {
+    int fail = 0;
+    for (int q = 0; q < p.nranks && !fail; ++q) {
+      if (q == skip_rank) continue;
+      Waiter wt;
+      while (ld_acquire_u64(flag_ptr(p, q, c, kind)) < want) {
+        if (wt.expired(p)) {
+          report_timeout(p, my_rank, c, E);
+          fail = 1;
+          break;
+        }
+      }
+    }
+    *s_fail = fail;
+  }
+  __syncthreads();
+  return *s_fail == 0;
+}
+__device__ __forceinline__ void publish_flag(const Params& p, int rank, int c, int kind, u64 value) {
+  __syncthreads();
+  if (p.inject_rank == rank && p.inject_mode == LLAR_INJECT_SKIP_) return;  // a rank that never signals
+  if (p.inject_rank == rank && p.inject_mode == LLAR_INJECT_DELAY_ && threadIdx.x == 0) injected_delay();
+  if (threadIdx.x == 0) {
+    fence_gpu();
+    st_relaxed_u64(flag_ptr(p, rank, c, kind), value);
+  }
+}
+
+// Sum of vector v over all ranks' inputs of iteration e, rank order,
+// float32, one rounding. `full` vectors are loaded whole; the last vector of
+// a ragged message element by element.
+template <int DT>
+__device__ __forceinline__ uint4 sum_ranks_vec(const Params& p, int e, size_t v, bool stream) {
+  const int N = p.nranks;
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  uint4 x[kMaxRanks];
+#pragma unroll
+  for (int q = 0; q < kMaxRanks; ++q)
+    if (q < N) x[q] = load_vec16<DT>(rank_input<DT>(p, q, e), v, p.count, stream);
+  float acc[PER16];
+  {
+    const unsigned w4[4] = {x[0].x, x[0].y, x[0].z, x[0].w};
+    init_acc<DT, 4>(acc, w4);
+  }
+#pragma unroll
+  for (int q = 1; q < kMaxRanks; ++q)
+    if (q < N) {
+      const unsigned w4[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+      accumulate<DT, 4>(acc, w4);
+    }
+  unsigned y[4];
+  pack_acc<DT, 4>(acc, y);
+  return u4(y);
+}
+
+// Reduce vectors [v0, v1) of iteration e and store the result to rank
+// `only`'s output (one-shot) or, with only < 0, to every rank's output
+// (two-shot AllGather by direct writes). Full vectors go through an
+// unrolled loop that keeps 2N 16-byte loads in flight per thread.
+template <int DT>
+__device__ __forceinline__ void reduce_range(const Params& p, int e, size_t v0, size_t v1, bool stream,
+                                             int only) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  const int N = p.nranks;
+  const size_t T = blockDim.x;
+  const size_t nfull = p.count / PER16;
+  const size_t h1 = v1 < nfull ? v1 : nfull;
+  size_t v = v0 + threadIdx.x;
+  for (; v + T < h1; v += 2 * T) {
+    const uint4 ya = sum_ranks_vec<DT>(p, e, v, stream);
+    const uint4 yb = sum_ranks_vec<DT>(p, e, v + T, stream);
+    if (only >= 0) {
+      char* o = rank_output<DT>(p, only, e);
+      st_v4(o + v * 16, ya);
+      st_v4(o + (v + T) * 16, yb);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kMaxRanks; ++q)
+        if (q < N) {
+          char* o = rank_output<DT>(p, q, e);
+          st_v4(o + v * 16, ya);
+          st_v4(o + (v + T) * 16, yb);
+        }
+    }
+  }
+  for (; v < v1; v += T) {
+    const uint4 y = sum_ranks_vec<DT>(p, e, v, stream);
+#pragma unroll
+    for (int q = 0; q < kMaxRanks; ++q)
+      if (q < N && (only < 0 || q == only)) store_vec16<DT>(rank_output<DT>(p, q, e), v, p.count, y);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void chain_range(const Params& p, int r, int e, size_t v0, size_t v1) {
+  const char* y_src = rank_output<DT>(p, r, e);
+  char* nxt = chain_next_buf(p, r, e);
+  for (size_t v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const uint4 y = load_vec16<DT>(y_src, v, p.count, false);
+    const unsigned w4[4] = {y.x, y.y, y.z, y.w};
+    unsigned nx[4];
+    chain_words<DT, 4>(w4, nx, p.chain_scale);
+    store_vec16<DT>(nxt, v, p.count, u4(nx));
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  __shared__ int s_fail;
+  const int r = blockIdx.x / p.G;
+  const int c = blockIdx.x - r * p.G;
+  const size_t NV = (p.count + PER16 - 1) / PER16;
+  const size_t per = (NV + p.G - 1) / p.G;
+  const size_t v0 = min(NV, (size_t)c * per);
+  const size_t v1 = min(NV, v0 + per);
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = p.epoch0 + (u64)e;
+    if (p.chain && e > 0 && !wait_flags(p, r, c, 0, E, r, E, &s_fail)) return;
+    reduce_range<DT>(p, e, v0, v1, !p.chain || e == 0, r);
+    if (p.chain) {
+      // my own output was written by this CTA: the barrier in publish_flag
+      // is not needed for it, each thread re-reads what it stored
+      chain_range<DT>(p, r, e, v0, v1);
+      publish_flag(p, r, c, 0, E + 1);
+    }
+  }
+}
+
+// Two-shot: rank s owns vectors [s*ceil(NV/N), ...) of the message; CTA c
+// of every rank covers sub-range c of every segment.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  __shared__ int s_fail;
+  const int N = p.nranks;
+  const int r = blockIdx.x / p.G;
+  const int c = blockIdx.x - r * p.G;
+  const size_t NV = (p.count + PER16 - 1) / PER16;
+  const size_t segv = (NV + N - 1) / N;
+  const size_t per = (segv + p.G - 1) / p.G;
+  auto sub = [&](int s, size_t& v0, size_t& v1) {
+    const size_t sbeg = min(NV, (size_t)s * segv);
+    const size_t send = min(NV, sbeg + segv);
+    v0 = min(send, sbeg + (size_t)c * per);
+    v1 = min(send, v0 + per);
+  };
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = p.epoch0 + (u64)e;
+    // phase 1, owner of segment r: reduce sub-range c, write it to every rank
+    if (p.chain && e > 0 && !wait_flags(p, r, c, 0, E, r, E, &s_fail)) return;
+    size_t v0, v1;
+    sub(r, v0, v1);
+    reduce_range<DT>(p, e, v0, v1, !p.chain || e == 0, -1);
+    if (!p.chain) continue;
+    publish_flag(p, r, c, 1, E);
+    if (e + 1 == p.iters) continue;  // no next input after the last step
+    // phase 2, rank r: once every owner wrote sub-range c of its segment
+    // into my output, compute my next input there
+    if (!wait_flags(p, r, c, 1, E, r, E, &s_fail)) return;
+    for (int s = 0; s < N; ++s) {
+      sub(s, v0, v1);
+      chain_range<DT>(p, r, e, v0, v1);
+    }
+    publish_flag(p, r, c, 0, E + 1);
+  }
+}
+
+// ============================================================ launchers
+template <typename K>
+static cudaError_t coop_launch(K kernel, const Params& p, int threads, cudaStream_t s) {
+  void* args[] = {const_cast<Params*>(&p)};
+  return cudaLaunchCooperativeKernel((const void*)kernel, dim3(p.nranks * p.G), dim3(threads), args, 0, s);
+}
+
+#define LLAR_DISPATCH(KERNEL, COOP)                                             \
+  switch (dtype) {                                                              \
+    case 0: return (COOP) ? coop_launch(KERNEL<0>, p, threads, s)                \
+                          : (KERNEL<0><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
+    case 1: return (COOP) ? coop_launch(KERNEL<1>, p, threads, s)                \
+                          : (KERNEL<1><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
+    case 2: return (COOP) ? coop_launch(KERNEL<2>, p, threads, s)                \
+                          : (KERNEL<2><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
+    default: return cudaErrorInvalidValue;                                      \
+  }
+
+cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_ll, true)
+}
+cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_sentinel, true)
+}
+cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_ll128, true)
+}
+cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_fixed_oneshot, p.chain != 0)
+}
+cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_fixed_twoshot, p.chain != 0)
+}
+
+template <int DT>
+static const void* kernel_for(int proto) {
+  switch (proto) {
+    case 1: return (const void*)k_ll<DT>;
+    case 2: return (const void*)k_sentinel<DT>;
+    case 3: return (const void*)k_ll128<DT>;
+    case 4: return (const void*)k_fixed_oneshot<DT>;
+    case 5: return (const void*)k_fixed_twoshot<DT>;
+    default: return nullptr;
+  }
+}
+
+int max_resident_ctas(int proto, int dtype, int /*chain*/, int threads) {
+  const void* k = dtype == 0 ? kernel_for<0>(proto) : dtype == 1 ? kernel_for<1>(proto) : kernel_for<2>(proto);
+  if (!k) return 0;
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return per_sm * sms;
+}
+
+// ======================================================= speed-of-light
+// Pointer chase: buf holds, at word 32*i (one 128-byte line per entry), the
+// index of the next line of one random cycle. One thread per block walks
+// `hops` dependent GPU-scope loads (served by L2, never by L1) after an
+// equal warm-up walk. The dynamic shared memory request keeps blocks on
+// distinct SMs.
+__global__ void k_sol_chase(const unsigned* buf, unsigned nlines, int hops, unsigned long long* ns,
+                            int* smid, unsigned* sink) {
+  extern __shared__ char pad[];
+  if (threadIdx.x != 0) return;
+  unsigned cur = (unsigned)(((unsigned long long)blockIdx.x * nlines) / gridDim.x);
+  for (int i = 0; i < hops; ++i) cur = ld_relaxed_u32(buf + (size_t)cur * 32);
+  const u64 t0 = globaltimer_ns();
+  for (int i = 0; i < hops; ++i) cur = ld_relaxed_u32(buf + (size_t)cur * 32);
+  const u64 t1 = globaltimer_ns();
+  unsigned id;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+  ns[blockIdx.x] = t1 - t0;
+  smid[blockIdx.x] = (int)id;
+  sink[blockIdx.x] = cur;
+  (void)pad;
+}
+
+// Ping-pong: blocks 2k (A) and 2k+1 (B) share two flags on separate lines.
+// A stores i into B's flag and waits to see i in its own; B waits for i and
+// answers. One round trip = two store-to-observe latencies. Waits are
+// bounded by the timeout and by the abort word.
+__global__ void k_sol_pingpong(unsigned* flags, int rounds, unsigned long long* ns, int* smid,
+                               unsigned* abort_flag, unsigned long long timeout_ns) {
+  extern __shared__ char pad[];
+  if (threadIdx.x != 0) return;
+  const int pair = blockIdx.x / 2;
+  const bool a_side = (blockIdx.x & 1) == 0;
+  unsigned* to_a = flags + (size_t)pair * 64;
+  unsigned* to_b = to_a + 32;
+  unsigned id;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+  smid[blockIdx.x] = (int)id;
+  const u64 start = globaltimer_ns();
+  const u64 deadline = start + timeout_ns;
+  bool ok = true;
+  for (int i = 1; i <= rounds && ok; ++i) {
+    if (a_side) asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" :: "l"(to_b), "r"((unsigned)i) : "memory");
+    const unsigned* watch = a_side ? to_a : to_b;
+    unsigned spins = 0;
+    while (ld_relaxed_u32(watch) != (unsigned)i) {
+      if ((++spins & 1023u) == 0 && (globaltimer_ns() > deadline || ld_relaxed_u32(abort_flag) != 0)) {
+        atomicExch(abort_flag, 7u);
+        ok = false;
+        break;
+      }
+    }
+    if (!a_side && ok)
+      asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" :: "l"(to_a), "r"((unsigned)i) : "memory");
+  }
+  const u64 end = globaltimer_ns();
+  if (a_side) ns[pair] = ok ? end - start : 0ull;
+  (void)pad;
+}
+
+static int sol_pad_bytes() {
+  int dev = 0, smem = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  return smem / 2 + 1024;  // more than half an SM's shared memory: one block per SM
+}
+
+cudaError_t run_sol(SolResult* res, unsigned long long timeout_ns) {
+  cudaError_t err;
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const int pad = sol_pad_bytes();
+
+  // one random cycle over the lines of a 16 MiB buffer (Sattolo's shuffle)
+  const unsigned nlines = (16u << 20) / 128u;
+  std::vector<unsigned> next(nlines), host((size_t)nlines * 32u, 0u);
+  for (unsigned i = 0; i < nlines; ++i) next[i] = i;
+  unsigned long long rng = 0x9E3779B97F4A7C15ull;
+  for (unsigned i = nlines - 1; i > 0; --i) {
+    rng ^= rng << 13; rng ^= rng >> 7; rng ^= rng << 17;
+    const unsigned j = (unsigned)(rng % i);
+    const unsigned t = next[i]; next[i] = next[j]; next[j] = t;
+  }
+  for (unsigned i = 0; i < nlines; ++i) host[(size_t)i * 32u] = next[i];
+
+  const int blocks = sms < kSolMaxBlocks ? sms : kSolMaxBlocks;
+  const int pairs = blocks / 2;
+  const int hops = 20000, rounds = 20000;
+  unsigned *buf = nullptr, *sink = nullptr, *flags = nullptr, *abort_flag = nullptr;
+  unsigned long long* ns = nullptr;
+  int* smid = nullptr;
+  std::vector<unsigned long long> h_ns(blocks);
+  std::vector<int> h_smid(blocks);
+#define LLAR_TRY(x) do { if ((err = (x)) != cudaSuccess) goto done; } while (0)
+  LLAR_TRY(cudaMalloc(&buf, host.size() * sizeof(unsigned)));
+  LLAR_TRY(cudaMalloc(&sink, blocks * sizeof(unsigned)));
+  LLAR_TRY(cudaMalloc(&ns, blocks * sizeof(unsigned long long)));
+  LLAR_TRY(cudaMalloc(&smid, blocks * sizeof(int)));
+  LLAR_TRY(cudaMalloc(&flags, (size_t)pairs * 64 * sizeof(unsigned)));
+  LLAR_TRY(cudaMalloc(&abort_flag, sizeof(unsigned)));
+  LLAR_TRY(cudaMemset(abort_flag, 0, sizeof(unsigned)));
+  LLAR_TRY(cudaMemcpy(buf, host.data(), host.size() * sizeof(unsigned), cudaMemcpyHostToDevice));
+  LLAR_TRY(cudaFuncSetAttribute(k_sol_chase, cudaFuncAttributeMaxDynamicSharedMemorySize, pad));
+  LLAR_TRY(cudaFuncSetAttribute(k_sol_pingpong, cudaFuncAttributeMaxDynamicSharedMemorySize, pad));
+  k_sol_chase<<<blocks, 32, pad>>>(buf, nlines, hops, ns, smid, sink);
+  LLAR_TRY(cudaGetLastError());
+  LLAR_TRY(cudaDeviceSynchronize());
+  LLAR_TRY(cudaMemcpy(h_ns.data(), ns, blocks * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  LLAR_TRY(cudaMemcpy(h_smid.data(), smid, blocks * sizeof(int), cudaMemcpyDeviceToHost));
+  res->nchase = blocks;
+  for (int b = 0; b < blocks; ++b) {
+    res->chase_ns[b] = (double)h_ns[b] / hops;
+    res->chase_smid[b] = h_smid[b];
+  }
+  LLAR_TRY(cudaMemset(flags, 0, (size_t)pairs * 64 * sizeof(unsigned)));
+  LLAR_TRY(cudaMemset(ns, 0, blocks * sizeof(unsigned long long)));
+  {
+    int rounds_arg = rounds;
+    void* args[] = {&flags, &rounds_arg, &ns, &smid, &abort_flag, &timeout_ns};
+    LLAR_TRY(cudaLaunchCooperativeKernel((const void*)k_sol_pingpong, dim3(2 * pairs), dim3(32), args, pad, 0));
+  }
+  LLAR_TRY(cudaDeviceSynchronize());
+  LLAR_TRY(cudaMemcpy(h_ns.data(), ns, pairs * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  LLAR_TRY(cudaMemcpy(h_smid.data(), smid, 2 * pairs * sizeof(int), cudaMemcpyDeviceToHost));
+  res->npairs = pairs;
+  for (int k = 0; k < pairs; ++k) {
+    res->rt_ns[k] = (double)h_ns[k] / rounds;  // 0 if that pair's wait ran out
+    res->smid_a[k] = h_smid[2 * k];
+    res->smid_b[k] = h_smid[2 * k + 1];
+  }
+#undef LLAR_TRY
+done:
+  cudaFree(buf);
+  cudaFree(sink);
+  cudaFree(ns);
+  cudaFree(smid);
+  cudaFree(flags);
+  cudaFree(abort_flag);
+  return err;
+}
+
+}  // namespace llar

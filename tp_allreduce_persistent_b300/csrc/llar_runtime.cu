@@ -1,0 +1,561 @@
+// Host runtime of the C ABI declared in include/llar.h: the process-global
+// context, staging layout and initialisation, argument checks, launch-shape
+// choice, epochs, status word, and the speed-of-light probe.
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "llar.h"
+#include "llar_internal.h"
+
+namespace {
+
+using llar::Params;
+
+constexpr size_t kAlign = 256;
+constexpr size_t kDefaultLLCap = 1u << 20;      // LL messages up to 1 MiB per rank
+constexpr size_t kDefaultLL128Cap = 64u << 20;  // LL128 messages up to 64 MiB per rank
+constexpr size_t kDefaultChunk = 8u << 10;      // sentinel chunk: 8 KiB per rank
+constexpr size_t kMaxChunk = 64u << 10;         // largest sentinel chunk
+constexpr int kFlagsGmax = 1024;                // CTAs per rank the chain flags can address
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+size_t elem_bytes(int dtype) { return dtype == LLAR_F32 ? 4 : 2; }
+
+size_t env_size(const char* name, size_t dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return (size_t)std::strtoull(v, nullptr, 0);
+}
+
+struct Ctx {
+  int n = 0, dtype = 0, dev = 0, sms = 0;
+  size_t max_bytes = 0, esize = 0;
+  size_t ll_cap = 0, ll128_cap = 0, chunk_bytes = kDefaultChunk;
+  char* base = nullptr;
+  size_t total = 0;
+  // regions
+  size_t ll_off = 0, ll_stride = 0, ll_words = 0;
+  size_t sen_off = 0, sen_stride = 0;
+  size_t l128_off = 0, l128_stride = 0, l128_lines = 0;
+  size_t ag_off = 0, ag_stride = 0;
+  size_t chain_off = 0, chain_stride = 0, chain_slot = 0;
+  size_t flags_off = 0, abort_off = 0;
+  llar::DevStatus* status_host = nullptr;
+  llar::DevStatus* status_dev = nullptr;
+  unsigned long long epoch = 1;
+  // host-API staging
+  char* io = nullptr;
+  size_t io_stride = 0;
+};
+
+std::mutex g_mu;
+Ctx* g = nullptr;
+unsigned long long g_timeout_ns = 1000000000ull;
+int g_force_G = 0, g_force_T = 0;
+int g_inject_rank = -1, g_inject_mode = 0;
+int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return LLAR_OK;
+  if (e == cudaErrorCooperativeLaunchTooLarge) return LLAR_ERR_OCCUPANCY;
+  return LLAR_ERR_CUDA;
+}
+
+size_t ll128_payload(int dtype) { return 128 / elem_bytes(dtype) - 1; }
+size_t ll128_lines_for(size_t count, int n, int dtype) {
+  const size_t seg = (count + n - 1) / n;
+  const size_t pl = ll128_payload(dtype);
+  return (seg + pl - 1) / pl;
+}
+
+bool valid_dtype(int d) { return d == LLAR_F32 || d == LLAR_F16 || d == LLAR_BF16; }
+bool valid_proto(int p) { return p >= LLAR_PROTO_AUTO && p <= LLAR_PROTO_FIXED_TWOSHOT; }
+
+int select_protocol(int n, int dtype, size_t count) {
+  const char* force = std::getenv("LLAR_PROTO");
+  if (force && *force) {
+    const int f = std::atoi(force);
+    if (f >= LLAR_PROTO_LL && f <= LLAR_PROTO_FIXED_TWOSHOT) return f;
+  }
+  const size_t bytes = count * elem_bytes(dtype);
+  (void)n;
+  if (bytes <= (64u << 10)) return LLAR_PROTO_LL;
+  if (bytes <= (512u << 10)) return LLAR_PROTO_SENTINEL;
+  return LLAR_PROTO_FIXED_TWOSHOT;
+}
+
+// CTAs per rank and threads per CTA for one launch.
+void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int* T) {
+  const int n = c.n;
+  const size_t e = c.esize;
+  const int one_per_sm = std::max(1, c.sms / n);
+  size_t units = 0;  // independent work items per rank
+  int t = 128;
+  switch (proto) {
+    case LLAR_PROTO_LL: units = (count * e + 7) / 8; break;
+    case LLAR_PROTO_SENTINEL: units = std::min(c.chunk_bytes, round_up(count * e, 16)) / 16; break;
+    case LLAR_PROTO_LL128_ATOMIC: units = ll128_lines_for(count, n, c.dtype) * n * llar::kLL128Lanes; break;
+    default: units = (count * e + 15) / 16; break;
+  }
+  int g = 1;
+  if (proto == LLAR_PROTO_FIXED_TWOSHOT || proto == LLAR_PROTO_FIXED_ONESHOT) {
+    t = 256;
+    const size_t per_rank = proto == LLAR_PROTO_FIXED_TWOSHOT ? (units + n - 1) / n : units;
+    const size_t want = (per_rank + 2 * t - 1) / (2 * t);
+    const int cap = chain ? one_per_sm : std::max(1, (c.sms * 4) / n);
+    g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)cap);
+  } else {
+    const size_t want = (units + t - 1) / t;
+    if (want <= (size_t)one_per_sm) {
+      g = (int)std::max<size_t>(want, 1);
+    } else {
+      g = one_per_sm;
+      const size_t per_cta = (units + g - 1) / g;
+      t = (int)std::min<size_t>(llar::kMaxThreads, round_up(per_cta, 32));
+    }
+  }
+  if (g_force_G > 0) g = g_force_G;
+  if (g_force_T > 0) t = g_force_T;
+  g = std::min(g, kFlagsGmax);
+  *G = g;
+  *T = t;
+}
+
+int check_ptrs(const void* const* in, void* const* out, int n, size_t in_span, size_t out_span) {
+  if (!in || !out) return LLAR_ERR_INVALID;
+  for (int r = 0; r < n; ++r) {
+    if (!in[r] || !out[r]) return LLAR_ERR_INVALID;
+    if (((uintptr_t)in[r] | (uintptr_t)out[r]) & 15u) return LLAR_ERR_INVALID;
+  }
+  for (int r = 0; r < n; ++r) {
+    const uintptr_t o0 = (uintptr_t)out[r], o1 = o0 + out_span;
+    for (int q = 0; q < n; ++q) {
+      const uintptr_t i0 = (uintptr_t)in[q], i1 = i0 + in_span;
+      if (o0 < i1 && i0 < o1) return LLAR_ERR_INVALID;  // output overlaps an input
+      if (q != r) {
+        const uintptr_t p0 = (uintptr_t)out[q], p1 = p0 + out_span;
+        if (o0 < p1 && p0 < o1) return LLAR_ERR_INVALID;  // two outputs overlap
+      }
+    }
+  }
+  return LLAR_OK;
+}
+
+int run(const void* const* in, void* const* out, size_t count, int proto, int iters,
+        size_t in_stride, size_t out_stride, float chain_scale, cudaStream_t stream) {
+  if (!g) return LLAR_ERR_NOT_INIT;
+  Ctx& c = *g;
+  if (!valid_proto(proto) || iters < 1) return LLAR_ERR_INVALID;
+  const size_t e = c.esize;
+  const int chain = chain_scale != 0.0f;
+  if (chain) in_stride = 0;
+  if ((in_stride * e) % 16 || (out_stride * e) % 16) return LLAR_ERR_INVALID;
+  const size_t bytes = count * e;
+  const size_t in_span = (size_t)(iters - 1) * in_stride * e + bytes;
+  const size_t out_span = (size_t)(iters - 1) * out_stride * e + bytes;
+  if (proto == LLAR_PROTO_AUTO) proto = select_protocol(c.n, c.dtype, count);
+  if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
+  if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
+  if (proto == LLAR_PROTO_LL128_ATOMIC && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
+  int st = check_ptrs(in, out, c.n, in_span, out_span);
+  if (st != LLAR_OK) return st;
+  if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
+  if (count == 0) return LLAR_OK;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < c.n; ++r) {
+    p.in[r] = static_cast<const char*>(in[r]);
+    p.out[r] = static_cast<char*>(out[r]);
+  }
+  p.count = count;
+  p.nranks = c.n;
+  p.iters = iters;
+  p.chain = chain;
+  p.chain_scale = chain_scale;
+  p.in_stride = in_stride;
+  p.out_stride = out_stride;
+  p.epoch0 = c.epoch;
+  p.ll = c.base + c.ll_off;
+  p.ll_stride = c.ll_stride;
+  p.ll_slot_words = c.ll_words;
+  p.sen = c.base + c.sen_off;
+  p.sen_stride = c.sen_stride;
+  p.sen_chunk_vecs = (int)(c.chunk_bytes / 16);
+  p.l128 = c.base + c.l128_off;
+  p.l128_stride = c.l128_stride;
+  p.l128ag = c.base + c.ag_off;
+  p.l128ag_stride = c.ag_stride;
+  p.l128_lines = c.l128_lines;
+  p.chainbuf = c.base + c.chain_off;
+  p.chain_stride = c.chain_stride;
+  p.chain_slot_bytes = c.chain_slot;
+  p.flags = reinterpret_cast<unsigned long long*>(c.base + c.flags_off);
+  p.flags_gmax = kFlagsGmax;
+  p.timeout_ns = g_timeout_ns;
+  p.inject_rank = g_inject_rank;
+  p.inject_mode = g_inject_mode;
+  p.abort_flag = reinterpret_cast<unsigned*>(c.base + c.abort_off);
+  p.status = c.status_dev;
+
+  int G = 1, T = 128;
+  choose_shape(c, proto, count, chain, &G, &T);
+  const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
+                    proto == LLAR_PROTO_LL128_ATOMIC || chain;
+  if (coop) {
+    const int cap = llar::max_resident_ctas(proto, c.dtype, chain, T);
+    if (cap <= 0) return LLAR_ERR_CUDA;
+    if (c.n * G > cap) {
+      if (g_force_G > 0) return LLAR_ERR_OCCUPANCY;
+      G = std::max(1, cap / c.n);
+    }
+  }
+  p.G = G;
+  cudaError_t err;
+  switch (proto) {
+    case LLAR_PROTO_LL: err = llar::launch_ll(c.dtype, p, T, stream); break;
+    case LLAR_PROTO_SENTINEL: err = llar::launch_sentinel(c.dtype, p, T, stream); break;
+    case LLAR_PROTO_LL128_ATOMIC: err = llar::launch_ll128(c.dtype, p, T, stream); break;
+    case LLAR_PROTO_FIXED_ONESHOT: err = llar::launch_fixed_oneshot(c.dtype, p, T, stream); break;
+    default: err = llar::launch_fixed_twoshot(c.dtype, p, T, stream); break;
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(err);
+  }
+  c.epoch += (unsigned long long)iters;
+  g_last_proto = proto;
+  g_last_G = G;
+  g_last_T = T;
+  g_last_iters = iters;
+  return LLAR_OK;
+}
+
+int fill_staging(Ctx& c, cudaStream_t s) {
+  cudaError_t err = cudaSuccess;
+  auto ok = [&](cudaError_t x) { if (err == cudaSuccess) err = x; };
+  ok(cudaMemsetAsync(c.base + c.ll_off, 0, c.ll_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.sen_off, 0xFF, c.sen_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.l128_off, 0, c.l128_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.ag_off, 0, c.ag_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.flags_off, 0, (size_t)c.n * kFlagsGmax * 2 * 8, s));
+  ok(cudaMemsetAsync(c.base + c.abort_off, 0, kAlign, s));
+  ok(cudaStreamSynchronize(s));
+  std::memset(c.status_host, 0, sizeof(llar::DevStatus));
+  return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+int llar_init(int nranks, int dtype, size_t max_bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g) return LLAR_ERR_INVALID;
+  if (nranks < 2 || nranks > llar::kMaxRanks || !valid_dtype(dtype) || max_bytes == 0)
+    return LLAR_ERR_INVALID;
+  Ctx* c = new Ctx();
+  c->n = nranks;
+  c->dtype = dtype;
+  c->esize = elem_bytes(dtype);
+  c->max_bytes = round_up(max_bytes, 16);
+  c->ll_cap = std::min(c->max_bytes, round_up(env_size("LLAR_LL_MAX_BYTES", kDefaultLLCap), 16));
+  c->ll128_cap = std::min(c->max_bytes, round_up(env_size("LLAR_LL128_MAX_BYTES", kDefaultLL128Cap), 16));
+  c->chunk_bytes = round_up(std::min(env_size("LLAR_CHUNK_BYTES", kDefaultChunk), kMaxChunk), 16);
+  g_timeout_ns = env_size("LLAR_TIMEOUT_NS", g_timeout_ns);
+  g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", (size_t)g_force_G);
+  g_force_T = (int)env_size("LLAR_THREADS", (size_t)g_force_T);
+
+  cudaError_t err = cudaGetDevice(&c->dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return LLAR_ERR_CUDA;
+  }
+  const int n = nranks;
+  size_t off = 0;
+  auto region = [&](size_t per_rank, size_t* o, size_t* stride) {
+    *stride = round_up(std::max<size_t>(per_rank, 16), kAlign);
+    *o = off;
+    off += *stride * n;
+  };
+  c->ll_words = (c->ll_cap + 7) / 8;
+  region(2 * (size_t)n * c->ll_words * llar::kLLLine, &c->ll_off, &c->ll_stride);
+  region(2 * (size_t)n * kMaxChunk, &c->sen_off, &c->sen_stride);
+  c->l128_lines = ll128_lines_for(c->ll128_cap / c->esize, n, dtype);
+  region(2 * c->l128_lines * llar::kLL128Line, &c->l128_off, &c->l128_stride);
+  region(2 * (size_t)n * c->l128_lines * llar::kAgLineBytes, &c->ag_off, &c->ag_stride);
+  c->chain_slot = round_up(c->max_bytes, kAlign);
+  region(2 * c->chain_slot, &c->chain_off, &c->chain_stride);
+  c->flags_off = off;
+  off += round_up((size_t)n * kFlagsGmax * 2 * 8, kAlign);
+  c->abort_off = off;
+  off += kAlign;
+  c->total = off;
+  err = cudaMalloc(&c->base, c->total);
+  if (err == cudaSuccess) err = cudaHostAlloc(&c->status_host, sizeof(llar::DevStatus), cudaHostAllocMapped);
+  if (err == cudaSuccess) err = cudaHostGetDevicePointer((void**)&c->status_dev, c->status_host, 0);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    if (c->base) cudaFree(c->base);
+    if (c->status_host) cudaFreeHost(c->status_host);
+    delete c;
+    return LLAR_ERR_CUDA;
+  }
+  const int st = fill_staging(*c, 0);
+  if (st != LLAR_OK) {
+    cudaFree(c->base);
+    cudaFreeHost(c->status_host);
+    delete c;
+    return st;
+  }
+  g = c;
+  return LLAR_OK;
+}
+
+int llar_destroy(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  cudaError_t err = cudaDeviceSynchronize();
+  cudaFree(g->base);
+  if (g->io) cudaFree(g->io);
+  cudaFreeHost(g->status_host);
+  delete g;
+  g = nullptr;
+  return cuda_status(err);
+}
+
+int llar_allreduce(const void* const* in, void* const* out, size_t count, int protocol, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return run(in, out, count, protocol, 1, 0, 0, 0.0f, static_cast<cudaStream_t>(stream));
+}
+
+int llar_allreduce_iters(const void* const* in, void* const* out, size_t count, int protocol, int iters,
+                         size_t in_stride_elems, size_t out_stride_elems, float chain_scale, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return run(in, out, count, protocol, iters, in_stride_elems, out_stride_elems, chain_scale,
+             static_cast<cudaStream_t>(stream));
+}
+
+int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int protocol, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (!in_host || !out_host) return LLAR_ERR_INVALID;
+  Ctx& c = *g;
+  const size_t bytes = count * c.esize;
+  if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
+  if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
+  if (count == 0) return LLAR_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!c.io) {
+    c.io_stride = round_up(c.max_bytes, kAlign);
+    if (cudaMalloc(&c.io, 2 * c.io_stride * c.n) != cudaSuccess) {
+      cudaGetLastError();
+      c.io = nullptr;
+      return LLAR_ERR_CUDA;
+    }
+  }
+  char* din = c.io;
+  char* dout = c.io + c.io_stride * c.n;
+  cudaError_t err = cudaMemcpy2DAsync(din, c.io_stride, in_host, bytes, bytes, c.n, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_status(err);
+  const void* ins[llar::kMaxRanks];
+  void* outs[llar::kMaxRanks];
+  for (int r = 0; r < c.n; ++r) {
+    ins[r] = din + r * c.io_stride;
+    outs[r] = dout + r * c.io_stride;
+  }
+  const int st = run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
+  if (st != LLAR_OK) return st;
+  err = cudaMemcpy2DAsync(out_host, bytes, dout, c.io_stride, bytes, c.n, cudaMemcpyDeviceToHost, s);
+  return cuda_status(err);
+}
+
+int llar_get_status(int* rank, int* cta, unsigned long long* epoch) {
+  if (!g) return LLAR_ERR_NOT_INIT;
+  volatile llar::DevStatus* st = g->status_host;
+  const unsigned code = st->code;
+  if (rank) *rank = code ? st->rank : -1;
+  if (cta) *cta = code ? st->cta : -1;
+  if (epoch) *epoch = code ? st->epoch : 0ull;
+  return (int)code;
+}
+
+int llar_reset(void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return cuda_status(err);
+  return fill_staging(*g, static_cast<cudaStream_t>(stream));
+}
+
+void llar_set_timeout_ns(unsigned long long ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timeout_ns = ns ? ns : 1;
+}
+
+int llar_set_launch(int ctas_per_rank, int threads) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (ctas_per_rank < 0 || ctas_per_rank > kFlagsGmax) return LLAR_ERR_INVALID;
+  if (threads < 0 || threads > llar::kMaxThreads || threads % 32) return LLAR_ERR_INVALID;
+  g_force_G = ctas_per_rank;
+  g_force_T = threads;
+  return LLAR_OK;
+}
+
+int llar_set_sentinel_chunk(size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (bytes == 0 || bytes % 16 || bytes > kMaxChunk) return LLAR_ERR_INVALID;
+  g->chunk_bytes = bytes;
+  return LLAR_OK;
+}
+
+int llar_debug_inject(int rank, int mode) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (mode < LLAR_INJECT_NONE || mode > LLAR_INJECT_DELAY) return LLAR_ERR_INVALID;
+  if (mode != LLAR_INJECT_NONE && (rank < 0 || rank >= llar::kMaxRanks)) return LLAR_ERR_INVALID;
+  g_inject_rank = mode == LLAR_INJECT_NONE ? -1 : rank;
+  g_inject_mode = mode;
+  return LLAR_OK;
+}
+
+int llar_sol_probe_detail(double* chase_ns, int* chase_smid, int* nchase, double* rt_ns, int* smid_a,
+                          int* smid_b, int* npairs) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  std::vector<llar::SolResult> res(1);
+  cudaError_t err = llar::run_sol(res.data(), g_timeout_ns);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(err);
+  }
+  const llar::SolResult& r = res[0];
+  for (int i = 0; i < r.nchase; ++i) {
+    if (chase_ns) chase_ns[i] = r.chase_ns[i];
+    if (chase_smid) chase_smid[i] = r.chase_smid[i];
+  }
+  for (int i = 0; i < r.npairs; ++i) {
+    if (rt_ns) rt_ns[i] = r.rt_ns[i];
+    if (smid_a) smid_a[i] = r.smid_a[i];
+    if (smid_b) smid_b[i] = r.smid_b[i];
+  }
+  if (nchase) *nchase = r.nchase;
+  if (npairs) *npairs = r.npairs;
+  for (int i = 0; i < r.npairs; ++i)
+    if (r.rt_ns[i] <= 0.0) return LLAR_ERR_TIMEOUT;  // that pair's wait ran out
+  return LLAR_OK;
+}
+
+static double median(std::vector<double> v) {
+  if (v.empty()) return 0.0;
+  std::sort(v.begin(), v.end());
+  const size_t m = v.size() / 2;
+  return v.size() % 2 ? v[m] : 0.5 * (v[m - 1] + v[m]);
+}
+
+int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us) {
+  std::vector<double> chase(llar::kSolMaxBlocks), rt(llar::kSolMaxBlocks / 2);
+  int nchase = 0, npairs = 0;
+  const int st = llar_sol_probe_detail(chase.data(), nullptr, &nchase, rt.data(), nullptr, nullptr, &npairs);
+  if (st != LLAR_OK) return st;
+  chase.resize(nchase);
+  std::vector<double> ok;
+  for (int i = 0; i < npairs; ++i)
+    if (rt[i] > 0) ok.push_back(rt[i]);
+  if (ok.empty() || chase.empty()) return LLAR_ERR_TIMEOUT;
+  const double l2 = median(chase) * 1e-3;
+  const double wr = 0.5 * median(ok) * 1e-3;
+  if (l2_rt_us) *l2_rt_us = l2;
+  if (write_us) *write_us = wr;
+  if (sol_us) *sol_us = 2.0 * l2 + wr;
+  return LLAR_OK;
+}
+
+int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes, size_t* rank_bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  const Ctx& c = *g;
+  size_t off = 0, stride = 0, used = 0;
+  switch (protocol) {
+    case LLAR_PROTO_LL: off = c.ll_off; stride = c.ll_stride; used = 2 * c.n * c.ll_words * llar::kLLLine; break;
+    case LLAR_PROTO_SENTINEL: off = c.sen_off; stride = c.sen_stride; used = 2 * c.n * c.chunk_bytes; break;
+    case LLAR_PROTO_LL128_ATOMIC: off = c.l128_off; stride = c.l128_stride; used = 2 * c.l128_lines * llar::kLL128Line; break;
+    default: return LLAR_ERR_UNSUPPORTED;
+  }
+  if (dev_ptr) *dev_ptr = c.base + off;
+  if (rank_stride_bytes) *rank_stride_bytes = stride;
+  if (rank_bytes) *rank_bytes = used;
+  return LLAR_OK;
+}
+
+int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_bytes,
+                size_t* payload_elems_per_line, size_t* staging_bytes_per_rank) {
+  if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks || !valid_proto(protocol))
+    return LLAR_ERR_INVALID;
+  if (protocol == LLAR_PROTO_AUTO) protocol = select_protocol(nranks, dtype, count);
+  const size_t e = elem_bytes(dtype);
+  size_t lb = 16, pl = 16 / e, st = 0;
+  switch (protocol) {
+    case LLAR_PROTO_LL:
+      pl = 8 / e;
+      st = 2 * (size_t)nranks * ((count * e + 7) / 8) * llar::kLLLine;
+      break;
+    case LLAR_PROTO_SENTINEL: {
+      const size_t chunk = g ? g->chunk_bytes : kDefaultChunk;
+      st = 2 * (size_t)nranks * chunk;
+      break;
+    }
+    case LLAR_PROTO_LL128_ATOMIC:
+      lb = llar::kLL128Line;
+      pl = ll128_payload(dtype);
+      st = 2 * ll128_lines_for(count, nranks, dtype) * llar::kLL128Line;
+      break;
+    default: st = 0; break;
+  }
+  if (line_bytes) *line_bytes = lb;
+  if (payload_elems_per_line) *payload_elems_per_line = pl;
+  if (staging_bytes_per_rank) *staging_bytes_per_rank = st;
+  return LLAR_OK;
+}
+
+int llar_select_protocol(int nranks, int dtype, size_t count) {
+  if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
+  return select_protocol(nranks, dtype, count);
+}
+
+unsigned long long llar_epoch(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g ? g->epoch : 0ull;
+}
+
+int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (protocol) *protocol = g_last_proto;
+  if (ctas_per_rank) *ctas_per_rank = g_last_G;
+  if (threads) *threads = g_last_T;
+  if (iters) *iters = g_last_iters;
+  return LLAR_OK;
+}
+
+const char* llar_strerror(int status) {
+  switch (status) {
+    case LLAR_OK: return "ok";
+    case LLAR_ERR_INVALID: return "invalid argument";
+    case LLAR_ERR_NOT_INIT: return "llar_init has not been called";
+    case LLAR_ERR_TOO_LARGE: return "message larger than the staging sized at init";
+    case LLAR_ERR_UNSUPPORTED: return "unsupported dtype, protocol or mode";
+    case LLAR_ERR_OCCUPANCY: return "the persistent grid cannot be fully resident";
+    case LLAR_ERR_CUDA: return "CUDA runtime error";
+    case LLAR_ERR_TIMEOUT: return "a device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+"""Thin Python binding of the C-ABI library libllar.so (include/llar.h).
+
+Argument marshalling only: tensors become device pointers, names become
+enum values, torch's current stream becomes the cudaStream_t. Every step of
+the AllReduce runs in the library's CUDA kernels. There is no fallback: if
+libllar.so is missing or a call fails, an exception is raised.
+"""
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libllar.so")
+
+DTYPES = {"fp32": 0, "fp16": 1, "bf16": 2}
+PROTOCOLS = {"auto": 0, "ll": 1, "sentinel": 2, "ll128": 3,
+             "fixed_oneshot": 4, "fixed_twoshot": 5}
+PROTOCOL_NAMES = {v: k for k, v in PROTOCOLS.items()}
+INJECT = {"none": 0, "skip": 1, "poison": 2, "delay": 3}
+OK, ERR_INVALID, ERR_NOT_INIT, ERR_TOO_LARGE, ERR_UNSUPPORTED, ERR_OCCUPANCY, ERR_CUDA, ERR_TIMEOUT = range(8)
+
+_lib = None
+
+
+class LlarError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (status {code})")
+
+
+def lib():
+    """The loaded libllar.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m tp_allreduce_persistent_b300.build` (no CPU fallback exists)")
+    L = ctypes.CDLL(LIB_PATH)
+    c_int, c_size, c_vp, c_ull = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_ulonglong
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "llar_init": (c_int, [c_int, c_int, c_size]),
+        "llar_destroy": (c_int, []),
+        "llar_allreduce": (c_int, [pp, pp, c_size, c_int, c_vp]),
+        "llar_allreduce_iters": (c_int, [pp, pp, c_size, c_int, c_int, c_size, c_size, ctypes.c_float, c_vp]),
+        "llar_allreduce_host": (c_int, [c_vp, c_vp, c_size, c_int, c_vp]),
+        "llar_get_status": (c_int, [ctypes.POINTER(c_int), ctypes.POINTER(c_int), ctypes.POINTER(c_ull)]),
+        "llar_reset": (c_int, [c_vp]),
+        "llar_set_timeout_ns": (None, [c_ull]),
+        "llar_set_launch": (c_int, [c_int, c_int]),
+        "llar_set_sentinel_chunk": (c_int, [c_size]),
+        "llar_debug_inject": (c_int, [c_int, c_int]),
+        "llar_sol_probe": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3),
+        "llar_sol_probe_detail": (c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int),
+                                          ctypes.POINTER(c_int), ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(c_int), ctypes.POINTER(c_int),
+                                          ctypes.POINTER(c_int)]),
+        "llar_staging": (c_int, [c_int, ctypes.POINTER(c_vp), ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
+        "llar_layout": (c_int, [c_int, c_int, c_int, c_size, ctypes.POINTER(c_size),
+                                ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
+        "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
+        "llar_epoch": (c_ull, []),
+        "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
+        "llar_strerror": (ctypes.c_char_p, [c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(code, what):
+    if code != OK:
+        raise LlarError(code, what)
+    return code
+
+
+def _enum(table, value):
+    return table[value] if isinstance(value, str) else int(value)
+
+
+def _ptr(x):
+    return x.data_ptr() if hasattr(x, "data_ptr") else int(x)
+
+
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * len(xs))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def strerror(code):
+    return lib().llar_strerror(int(code)).decode()
+
+
+def llar_init(nranks, dtype, max_bytes):
+    _check(lib().llar_init(int(nranks), _enum(DTYPES, dtype), int(max_bytes)), "llar_init")
+
+
+def llar_destroy():
+    _check(lib().llar_destroy(), "llar_destroy")
+
+
+def llar_allreduce(ins, outs, count=None, protocol="auto", stream=None):
+    """One AllReduce: outs[r] = sum over q of ins[q] (lists of N device tensors)."""
+    if count is None:
+        count = ins[0].numel()
+    _check(lib().llar_allreduce(_ptr_array(ins), _ptr_array(outs), int(count),
+                                _enum(PROTOCOLS, protocol), ctypes.c_void_p(_stream(stream))),
+           "llar_allreduce")
+
+
+def llar_allreduce_iters(ins, outs, count, protocol, iters, in_stride=0, out_stride=0,
+                         chain_scale=0.0, stream=None):
+    """`iters` AllReduces in one persistent launch (strides in elements)."""
+    _check(lib().llar_allreduce_iters(_ptr_array(ins), _ptr_array(outs), int(count),
+                                      _enum(PROTOCOLS, protocol), int(iters), int(in_stride),
+                                      int(out_stride), float(chain_scale),
+                                      ctypes.c_void_p(_stream(stream))),
+           "llar_allreduce_iters")
+
+
+def llar_allreduce_host(in_host, out_host, count, protocol="auto", stream=None):
+    """AllReduce of host [N][count] arrays (tensors or raw host pointers)."""
+    _check(lib().llar_allreduce_host(ctypes.c_void_p(_ptr(in_host)), ctypes.c_void_p(_ptr(out_host)),
+                                     int(count), _enum(PROTOCOLS, protocol),
+                                     ctypes.c_void_p(_stream(stream))),
+           "llar_allreduce_host")
+
+
+def llar_get_status():
+    """(code, rank, cta, epoch) of the device status word."""
+    r, c, e = ctypes.c_int(), ctypes.c_int(), ctypes.c_ulonglong()
+    code = lib().llar_get_status(ctypes.byref(r), ctypes.byref(c), ctypes.byref(e))
+    return code, r.value, c.value, e.value
+
+
+def llar_reset(stream=None):
+    _check(lib().llar_reset(ctypes.c_void_p(_stream(stream))), "llar_reset")
+
+
+def llar_set_timeout_ns(ns):
+    lib().llar_set_timeout_ns(int(ns))
+
+
+def llar_set_launch(ctas_per_rank=0, threads=0):
+    _check(lib().llar_set_launch(int(ctas_per_rank), int(threads)), "llar_set_launch")
+
+
+def llar_set_sentinel_chunk(nbytes):
+    _check(lib().llar_set_sentinel_chunk(int(nbytes)), "llar_set_sentinel_chunk")
+
+
+def llar_debug_inject(rank, mode):
+    _check(lib().llar_debug_inject(int(rank), _enum(INJECT, mode)), "llar_debug_inject")
+
+
+def llar_sol_probe():
+    """(l2_round_trip_us, write_us, speed_of_light_us)."""
+    a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(lib().llar_sol_probe(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "llar_sol_probe")
+    return a.value, b.value, c.value
+
+
+def llar_sol_probe_detail():
+    """Per-SM chase latencies and per-pair ping-pong round trips (ns)."""
+    chase = (ctypes.c_double * 256)()
+    csm = (ctypes.c_int * 256)()
+    rt = (ctypes.c_double * 128)()
+    sa = (ctypes.c_int * 128)()
+    sb = (ctypes.c_int * 128)()
+    nc, npair = ctypes.c_int(), ctypes.c_int()
+    _check(lib().llar_sol_probe_detail(chase, csm, ctypes.byref(nc), rt, sa, sb, ctypes.byref(npair)),
+           "llar_sol_probe_detail")
+    return {"chase_ns": list(chase[:nc.value]), "chase_smid": list(csm[:nc.value]),
+            "rt_ns": list(rt[:npair.value]), "smid_a": list(sa[:npair.value]),
+            "smid_b": list(sb[:npair.value])}
+
+
+def llar_staging(protocol):
+    """(device pointer, rank stride bytes, bytes used per rank) of a protocol's staging."""
+    p, s, u = ctypes.c_void_p(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().llar_staging(_enum(PROTOCOLS, protocol), ctypes.byref(p), ctypes.byref(s),
+                              ctypes.byref(u)), "llar_staging")
+    return p.value, s.value, u.value
+
+
+def llar_layout(protocol, dtype, nranks, count):
+    """(line bytes, data elements per line, staging bytes per rank) — host only."""
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().llar_layout(_enum(PROTOCOLS, protocol), _enum(DTYPES, dtype), int(nranks), int(count),
+                             ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "llar_layout")
+    return a.value, b.value, c.value
+
+
+def llar_select_protocol(nranks, dtype, count):
+    return PROTOCOL_NAMES[lib().llar_select_protocol(int(nranks), _enum(DTYPES, dtype), int(count))]
+
+
+def llar_epoch():
+    return int(lib().llar_epoch())
+
+
+def llar_last_launch():
+    """(protocol name, CTAs per rank, threads per CTA, iterations) of the latest launch."""
+    v = [ctypes.c_int() for _ in range(4)]
+    lib().llar_last_launch(*[ctypes.byref(x) for x in v])
+    return PROTOCOL_NAMES.get(v[0].value, v[0].value), v[1].value, v[2].value, v[3].value
