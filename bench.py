@@ -48,7 +48,7 @@ FLUSH_BYTES = 256 << 20    # > 126 MB L2
 FALLBACK_HBM_GBS = 6400.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -56,7 +56,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth"],
+                    help="run one leg only (small profiling cases)")
+    ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
+    ap.add_argument("--bw-mib", type=int, default=BW_COUNT * 2 >> 20, help="MiB per rank, bandwidth leg")
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ helpers
@@ -168,9 +172,14 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
+        return self.parse(self.lines)
+
+    @staticmethod
+    def parse(lines):
+        """Median SM clock, max clock and the throttle reasons seen active."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -188,6 +197,90 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ our CUDA path
+def _events(n):
+    import torch
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+
+
+def latency_leg(args, llar, inputs, torch, dev, stream, flush, pg, local):
+    """ITERS back-to-back 16 KiB AllReduces per launch; returns a dict."""
+    iters = args.iters
+    x = inputs.normal(NRANKS, COUNT, DTYPE, seed=1, scale=0.02)
+    ins = [x[r].to(dev) for r in range(NRANKS)]
+    outs = [torch.empty_like(t) for t in ins]
+    proto = args.protocol
+    for _ in range(args.warmup):
+        llar.llar_allreduce_iters(ins, outs, COUNT, proto, iters, 0, 0, 0.0)
+    torch.cuda.synchronize()
+    used_proto, g, t, _ = llar.llar_last_launch()
+    ev = _events(args.steps)
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)  # evict L2 between timed launches (outside the events)
+        ev[k][0].record(stream)
+        llar.llar_allreduce_iters(ins, outs, COUNT, proto, iters, 0, 0, 0.0)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    wall = time.perf_counter() - wall0
+    code = llar.llar_get_status()[0]
+    if code != llar.OK:
+        raise RuntimeError(f"device status {code} during the latency leg")
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return {"us_per_ar": step_ms * 1e3 / iters, "step_ms": step_ms, "proto": used_proto,
+            "G": g, "T": t, "wall_s": wall, "x": x}
+
+
+def bandwidth_leg(args, llar, torch, dev, stream, pg, local):
+    """BW_REPS AllReduces of bw_mib MiB per rank per step, fixed two-shot."""
+    count = (args.bw_mib << 20) // 2
+    gen = torch.Generator(device=dev)
+    bw_ins = []
+    for r in range(NRANKS):
+        gen.manual_seed(5 + r)
+        bw_ins.append(torch.randn(count, device=dev, generator=gen).to(torch.bfloat16))
+    bw_outs = [torch.empty_like(a) for a in bw_ins]
+    for _ in range(args.warmup):
+        llar.llar_allreduce(bw_ins, bw_outs, count, "fixed_twoshot")
+    torch.cuda.synchronize()
+    shape = llar.llar_last_launch()
+    bev = _events(args.steps * BW_REPS)
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    for i in range(args.steps * BW_REPS):
+        bev[i][0].record(stream)
+        llar.llar_allreduce(bw_ins, bw_outs, count, "fixed_twoshot")
+        bev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    launch_s = statistics.mean(a.elapsed_time(b) for a, b in bev) * 1e-3
+    alg_bytes = 2 * NRANKS * count * 2
+    return {"gbs": alg_bytes / launch_s / 1e9, "launch_s": launch_s, "alg_bytes": alg_bytes,
+            "count": count, "G": shape[1], "T": shape[2]}
+
+
+def e2e_leg(args, llar, torch, stream, x, pg, local):
+    """One AllReduce per llar_allreduce_host call on pinned host buffers."""
+    proto = args.protocol
+    hx = x.contiguous().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    for _ in range(args.warmup):
+        llar.llar_allreduce_host(hx, hy, COUNT, proto)
+    torch.cuda.synchronize()
+    calls = max(3, args.steps // 5) * E2E_CALLS
+    e0, e1 = _events(1)[0]
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(calls):
+        llar.llar_allreduce_host(hx, hy, COUNT, proto)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / calls
+
+
 def run_ours(args, world, rank, local, pg):
     import torch
     from tp_allreduce_persistent_b300 import inputs, llar
@@ -195,152 +288,78 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    llar.llar_init(NRANKS, DTYPE, BW_COUNT * 2)
+    llar.llar_init(NRANKS, DTYPE, max(args.bw_mib << 20, COUNT * 2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    # ---- speed of light on this GPU (2 x L2 round trip + one write)
-    l2_us, write_us, sol_us = llar.llar_sol_probe()
-
-    # ---- latency leg: 16 KiB bf16 x 8 ranks, ITERS back to back per launch
-    x = inputs.normal(NRANKS, COUNT, DTYPE, seed=1, scale=0.02)
-    ins = [x[r].to(dev) for r in range(NRANKS)]
-    outs = [torch.empty_like(t) for t in ins]
-    proto = args.protocol
-    for _ in range(args.warmup):
-        llar.llar_allreduce_iters(ins, outs, COUNT, proto, ITERS, 0, 0, 0.0)
-    torch.cuda.synchronize()
-    used_proto, g, t, _ = llar.llar_last_launch()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)  # evict L2 between timed launches (outside the events)
-        ev[k][0].record(stream)
-        llar.llar_allreduce_iters(ins, outs, COUNT, proto, ITERS, 0, 0, 0.0)
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(pg, local)
-    wall_lat = time.perf_counter() - wall0
-    lat_ms = [a.elapsed_time(b) for a, b in ev]
-    code = llar.llar_get_status()[0]
-    if code != llar.OK:
-        raise RuntimeError(f"device status {code} during the latency leg")
-    step_ms = sum(lat_ms) / len(lat_ms)
-    us_per_ar = step_ms * 1e3 / ITERS
-
-    # ---- bandwidth leg: 64 MiB bf16 x 8 ranks, fixed-order two-shot
-    bw_ins = [torch.randn(BW_COUNT, device=dev, generator=torch.Generator(device=dev).manual_seed(5 + r))
-              .to(torch.bfloat16) for r in range(NRANKS)]
-    bw_outs = [torch.empty_like(a) for a in bw_ins]
-    for _ in range(args.warmup):
-        llar.llar_allreduce(bw_ins, bw_outs, BW_COUNT, "fixed_twoshot")
-    torch.cuda.synchronize()
-    bw_shape = llar.llar_last_launch()
-    bev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps * BW_REPS)]
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    i = 0
-    for k in range(args.steps):
-        for _ in range(BW_REPS):
-            bev[i][0].record(stream)
-            llar.llar_allreduce(bw_ins, bw_outs, BW_COUNT, "fixed_twoshot")
-            bev[i][1].record(stream)
-            i += 1
-    torch.cuda.synchronize()
-    barrier(pg, local)
-    clk = clocks.stop()
-    bw_ms = [a.elapsed_time(b) for a, b in bev]
-    bw_launch_s = statistics.mean(bw_ms) * 1e-3
-    alg_bytes = 2 * NRANKS * BW_COUNT * 2
-    gbs = alg_bytes / bw_launch_s / 1e9
-
-    # ---- end to end: host buffers through llar_allreduce_host
-    hx = x.contiguous().pin_memory()
-    hy = torch.empty_like(hx).pin_memory()
-    for _ in range(args.warmup):
-        llar.llar_allreduce_host(hx, hy, COUNT, proto)
-    torch.cuda.synchronize()
-    e2e_steps = max(3, args.steps // 5)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps * E2E_CALLS):
-        llar.llar_allreduce_host(hx, hy, COUNT, proto)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1e3 / (e2e_steps * E2E_CALLS)
-    llar.llar_destroy()
-
-    # ---- aggregate over ranks (independent replicas)
-    us_per_ar = max_over_ranks(pg, us_per_ar, dev)
-    gbs_min = -max_over_ranks(pg, -gbs, dev)
-    e2e_us = max_over_ranks(pg, e2e_us, dev)
-    total_ars = sum_over_ranks(pg, ITERS * args.steps, dev)
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    bw_workload = "8 ranks x 64 MiB bf16, fixed-order two-shot"
-    traffic = recorded_traffic("k_fixed_twoshot<bf16>", bw_workload)
-    result = {
-        "metric": METRIC,
-        "value": round(us_per_ar, 4),
-        "unit": "us",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 4),
-        "higher_is_better": False,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32-accumulate over bf16",
-        "data": "synthetic: N(0,1)*0.02 activations (latency leg), N(0,1) (bandwidth leg), seeded",
-        "config": {
-            "workload": "8 virtual ranks x 16 KiB bf16 (8192 elements) AllReduce, "
-                        f"{ITERS} back-to-back per persistent launch",
-            "nranks": NRANKS, "count": COUNT, "iters_per_launch": ITERS,
-            "protocol": used_proto, "ctas_per_rank": g, "threads_per_cta": t,
-            "l2": "flushed between timed launches (256 MiB write outside the events)",
-            "bandwidth_workload": bw_workload + "; inputs+outputs 1 GiB > L2",
-            "replicas": "independent per GPU" if world > 1 else "single GPU",
-        },
-        "bandwidth": {
-            "value": round(gbs_min, 1), "unit": "GB/s",
-            "us_per_allreduce": round(bw_launch_s * 1e6, 2),
-            "algorithmic_bytes": alg_bytes,
-            "algbw_gbs": round(BW_COUNT * 2 / bw_launch_s / 1e9, 1),
-            "busbw_gbs": round(BW_COUNT * 2 / bw_launch_s / 1e9 * 2 * (NRANKS - 1) / NRANKS, 1),
-            "ctas_per_rank": bw_shape[1], "threads_per_cta": bw_shape[2],
-        },
-        "roofline": {
-            "kernel": "k_fixed_twoshot<bf16>", "bound": "hbm",
-            "achieved": round(gbs_min, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(gbs_min / hbm_peak, 4), "traffic": traffic,
-            "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)",
-            "frac_of_nominal_8TBps": round(gbs_min / 8000.0, 4),
-        },
-        "latency_roofline": {
-            "kernel": f"k_{used_proto}<bf16>", "bound": "latency (L2 round trips)",
-            "achieved_us": round(us_per_ar, 4), "sol_us": round(sol_us, 4),
+
+    l2_us, write_us, sol_us = llar.llar_sol_probe()
+    clocks = ClockSampler(local)
+    clocks.start()
+    lat = bw = None
+    if args.leg in ("all", "latency"):
+        lat = latency_leg(args, llar, inputs, torch, dev, stream, flush, pg, local)
+    if args.leg in ("all", "bandwidth"):
+        bw = bandwidth_leg(args, llar, torch, dev, stream, pg, local)
+    clk = clocks.stop()
+    e2e_us = None
+    if lat is not None and args.leg == "all":
+        e2e_us = e2e_leg(args, llar, torch, stream, lat["x"], pg, local)
+    llar.llar_destroy()
+
+    res = {"metric": METRIC, "unit": "us", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f32-accumulate over bf16",
+           "data": "synthetic: N(0,1)*0.02 activations (latency leg), N(0,1) (bandwidth leg), seeded",
+           "clocks": clk}
+    config = {"replicas": "independent per GPU" if world > 1 else "single GPU",
+              "l2": "latency leg: flushed between timed launches (256 MiB write outside the events); "
+                    "bandwidth leg: inputs+outputs larger than L2"}
+    if lat is not None:
+        us = max_over_ranks(pg, lat["us_per_ar"], dev)
+        total = sum_over_ranks(pg, args.iters * args.steps, dev)
+        res.update({"value": round(us, 4), "ms_per_step": round(lat["step_ms"], 4),
+                    "gpu_launches": args.steps, "total_allreduces": int(total),
+                    "aggregate_allreduces_per_s": round(total / (lat["step_ms"] * 1e-3 * args.steps), 1),
+                    "wall_s_latency_leg": round(lat["wall_s"], 3)})
+        config.update({"workload": f"8 virtual ranks x 16 KiB bf16 (8192 elements) AllReduce, "
+                                   f"{args.iters} back-to-back per persistent launch",
+                       "nranks": NRANKS, "count": COUNT, "iters_per_launch": args.iters,
+                       "protocol": lat["proto"], "ctas_per_rank": lat["G"], "threads_per_cta": lat["T"]})
+        res["latency_roofline"] = {
+            "kernel": f"k_{lat['proto']}<bf16>", "bound": "latency (L2 round trips)",
+            "achieved_us": round(us, 4), "sol_us": round(sol_us, 4),
             "l2_round_trip_us": round(l2_us, 4), "write_us": round(write_us, 4),
-            "frac": round(sol_us / us_per_ar, 4),
-            "within_2x_sol": bool(us_per_ar <= 2 * sol_us),
-            "definition": "SoL = 2 x L2 round trip + one remote write, measured in this run",
-        },
-        "e2e": {"value": round(e2e_us, 3), "unit": "us",
-                "h2d_bytes_per_step": NRANKS * COUNT * 2, "d2h_bytes_per_step": NRANKS * COUNT * 2,
-                "api": "llar_allreduce_host (pinned host [8][8192] bf16 in and out, one AllReduce per call)"},
-        "gpu_launches": args.steps,
-        "gpu_launches_bandwidth_leg": args.steps * BW_REPS,
-        "total_allreduces": int(total_ars),
-        "wall_s_latency_leg": round(wall_lat, 3),
-        "clocks": clk,
-    }
-    return result
+            "frac": round(sol_us / us, 4), "within_2x_sol": bool(us <= 2 * sol_us),
+            "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run"}
+    if bw is not None:
+        gbs = -max_over_ranks(pg, -bw["gbs"], dev)
+        mib = args.bw_mib
+        wl = f"8 ranks x {mib} MiB bf16, fixed-order two-shot"
+        res["bandwidth"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "workload": wl,
+            "us_per_allreduce": round(bw["launch_s"] * 1e6, 2), "algorithmic_bytes": bw["alg_bytes"],
+            "algbw_gbs": round(bw["count"] * 2 / bw["launch_s"] / 1e9, 1),
+            "busbw_gbs": round(bw["count"] * 2 / bw["launch_s"] / 1e9 * 2 * (NRANKS - 1) / NRANKS, 1),
+            "ctas_per_rank": bw["G"], "threads_per_cta": bw["T"], "launches": args.steps * BW_REPS}
+        res["roofline"] = {
+            "kernel": "k_fixed_twoshot<bf16>", "bound": "hbm", "achieved": round(gbs, 1),
+            "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+            "traffic": recorded_traffic("k_fixed_twoshot<bf16>", wl),
+            "algorithmic_bytes_per_launch": bw["alg_bytes"],
+            "peak_source": f"{peak_src} hbm_gbs (copy bandwidth, burst)",
+            "frac_of_nominal_8TBps": round(gbs / 8000.0, 4)}
+        config["bandwidth_workload"] = wl
+        if lat is None:
+            res.update({"value": round(gbs, 1), "unit": "GB/s", "higher_is_better": True,
+                        "ms_per_step": round(bw["launch_s"] * 1e3 * BW_REPS, 4),
+                        "gpu_launches": args.steps * BW_REPS})
+    if e2e_us is not None:
+        res["e2e"] = {"value": round(max_over_ranks(pg, e2e_us, dev), 3), "unit": "us",
+                      "h2d_bytes_per_step": NRANKS * COUNT * 2, "d2h_bytes_per_step": NRANKS * COUNT * 2,
+                      "api": "llar_allreduce_host: pinned host [8][8192] bf16 in, out; one AllReduce per call"}
+    res["config"] = config
+    return res
 
 
 # ------------------------------------------------------- CPU oracle timing

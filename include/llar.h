@@ -153,6 +153,9 @@ int llar_debug_inject(int rank, int mode);
  * different SMs; sol_us = 2 * l2_rt_us + write_us. Needs llar_init. */
 int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us);
 
+/* The speed-of-light bound itself (host only): 2 * l2_rt_us + write_us. */
+double llar_sol_bound_us(double l2_rt_us, double write_us);
+
 /* The raw measurements behind llar_sol_probe. Arrays hold at least 256
  * (chase) and 128 (pairs) entries. chase_ns[i]: ns per dependent load of
  * the chasing thread on SM chase_smid[i]; rt_ns[k]: ns per round trip of

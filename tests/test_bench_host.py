@@ -1,0 +1,76 @@
+"""Host-side logic of bench.py on CPU: cross-rank aggregation over a
+world-size-2 gloo group, the clock-record parser, and the reference arm's
+JSON line. Nothing here touches a GPU."""
+
+import os
+import socket
+import sys
+import types
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench as b
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q.put((rank, b.max_over_ranks(dist, 10.0 + rank), b.sum_over_ranks(dist, 1000.0),
+           -b.max_over_ranks(dist, -(5.0 + rank))))
+    b.barrier(dist)
+    dist.destroy_process_group()
+
+
+def test_aggregation_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # slowest rank's latency, units summed over ranks, smallest bandwidth
+    assert res == [(0, 11.0, 2000.0, 5.0), (1, 11.0, 2000.0, 5.0)]
+
+
+def test_clock_record_parser():
+    lines = ["0, 1900, 2032, 700.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "0, 1920, 2032, 800.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "0, 1880, 2032, 650.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "garbage"]
+    rec = bench.ClockSampler.parse(lines)
+    assert rec["sm_mhz"] == 1900 and rec["sm_max_mhz"] == 2032
+    assert rec["reasons"] == ["sw_power_cap"] and rec["samples"] == 3
+
+
+def test_reference_arm_line(monkeypatch):
+    monkeypatch.setattr(bench, "time_oracle", lambda seconds, **k: (123.0, 10))
+    args = types.SimpleNamespace(steps=2, warmup=1)
+    line = bench.run_reference(args, world=1, rank=0)
+    assert line["impl"] == "reference" and line["value"] == 123.0 and line["unit"] == "us"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert bench.run_reference(args, world=2, rank=1) is None
+
+
+def test_oracle_timing_runs():
+    us, n = bench.time_oracle(0.05, count=256, nranks=4)
+    assert us > 0 and n >= 1

@@ -460,6 +460,8 @@ static double median(std::vector<double> v) {
   return v.size() % 2 ? v[m] : 0.5 * (v[m - 1] + v[m]);
 }
 
+double llar_sol_bound_us(double l2_rt_us, double write_us) { return 2.0 * l2_rt_us + write_us; }
+
 int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us) {
   std::vector<double> chase(llar::kSolMaxBlocks), rt(llar::kSolMaxBlocks / 2);
   int nchase = 0, npairs = 0;
@@ -474,7 +476,7 @@ int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us) {
   const double wr = 0.5 * median(ok) * 1e-3;
   if (l2_rt_us) *l2_rt_us = l2;
   if (write_us) *write_us = wr;
-  if (sol_us) *sol_us = 2.0 * l2 + wr;
+  if (sol_us) *sol_us = llar_sol_bound_us(l2, wr);
   return LLAR_OK;
 }
 

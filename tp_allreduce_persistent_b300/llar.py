@@ -62,6 +62,7 @@ def lib():
                                 ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
         "llar_epoch": (c_ull, []),
+        "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
         "llar_strerror": (ctypes.c_char_p, [c_int]),
     }
@@ -172,6 +173,11 @@ def llar_sol_probe():
     a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
     _check(lib().llar_sol_probe(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "llar_sol_probe")
     return a.value, b.value, c.value
+
+
+def llar_sol_bound_us(l2_rt_us, write_us):
+    """Speed-of-light bound 2 * L2 round trip + one write (host arithmetic)."""
+    return float(lib().llar_sol_bound_us(float(l2_rt_us), float(write_us)))
 
 
 def llar_sol_probe_detail():
