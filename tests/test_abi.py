@@ -40,7 +40,7 @@ def test_speed_of_light_formula_matches_page_numbers():
 def test_layout_constants(dtype):
     e = {"fp32": 4, "fp16": 2, "bf16": 2}[dtype]
     lb, pl, st = llar.llar_layout("ll", dtype, 4, 8192)
-    assert (lb, pl * e) == (16, 8) and st == 2 * 4 * oproto.ll_staging_bytes(8192 * e)
+    assert (lb, pl * e) == (16, 8) and st == 2 * oproto.ll_staging_bytes(8192 * e)
     lb, pl, st = llar.llar_layout("ll128", dtype, 8, 1 << 20)
     assert lb == 128 and pl == oproto.ll128_payload_elems(dtype)
     assert st == 2 * oproto.ll128_round_staging_bytes(1 << 20, 8, dtype)

@@ -79,7 +79,7 @@ def test_layout_matches_page_constants():
         lb, pl, st = llar.llar_layout("ll", dtype, 8, 8192)
         e = inputs.ELEM_BYTES[dtype]
         assert lb == 16 and pl * e == 8
-        assert st == 2 * 8 * oproto.ll_staging_bytes(8192 * e)
+        assert st == 2 * oproto.ll_staging_bytes(8192 * e)
         lb, pl, st = llar.llar_layout("ll128", dtype, 8, 1 << 18)
         assert lb == oproto.LL128_LINE_BYTES and pl == oproto.ll128_payload_elems(dtype)
         assert st == 2 * oproto.ll128_round_staging_bytes(1 << 18, 8, dtype)

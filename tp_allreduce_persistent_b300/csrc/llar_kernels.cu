@@ -71,17 +71,84 @@ __device__ __forceinline__ void store_vec16(char* base, size_t v, size_t count, 
 
 __device__ __forceinline__ uint4 u4(const unsigned* w) { return make_uint4(w[0], w[1], w[2], w[3]); }
 
-// ============================================================ LL one-shot
-// Technique 1: each 8 bytes of data leave with an 8-byte flag (the launch
-// epoch of this AllReduce) as one 16-byte store into every peer's slot
-// [epoch & 1][source rank][word]; the receiver polls that 16-byte line
-// until the flag equals the epoch, so no separate signal and no barrier is
-// needed. Epochs only grow, so slots never need a reset.
+// One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
+// the thread pushes its unit of my data to every peer, polls the unit every
+// peer sent, adds the N values in rank order and stores the result. The
+// kernels are instantiated per N, so the peer loops unroll without guards.
+// Staging is [slot][source][unit]: a warp's store to one peer, and a warp's
+// poll of one source, cover 32 consecutive units.
+
+// float32 values of the elements of a 32-bit word
 template <int DT>
+__device__ __forceinline__ void unpack2(unsigned w, float& a, float& b) {
+  if (DT == 2) {  // bf16: the value is the upper half of a float32
+    a = __uint_as_float(w << 16);
+    b = __uint_as_float(w & 0xFFFF0000u);
+  } else if (DT == 1) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    a = f.x;
+    b = f.y;
+  }
+}
+// two float32 values rounded (roundTiesToEven) into one 32-bit word
+template <int DT>
+__device__ __forceinline__ unsigned pack2(float a, float b) {
+  if (DT == 2) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const unsigned*>(&h);
+  }
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const unsigned*>(&h);
+}
+
+// acc (n32*PER32 floats) = values of the words of `w`, or += them
+template <int DT, int NW>
+__device__ __forceinline__ void acc_words(float* acc, const unsigned* w, bool first) {
+#pragma unroll
+  for (int k = 0; k < NW; ++k) {
+    if (DT == 0) {
+      const float f = __uint_as_float(w[k]);
+      acc[k] = first ? f : __fadd_rn(acc[k], f);
+    } else {
+      float a, b;
+      unpack2<DT>(w[k], a, b);
+      acc[2 * k] = first ? a : __fadd_rn(acc[2 * k], a);
+      acc[2 * k + 1] = first ? b : __fadd_rn(acc[2 * k + 1], b);
+    }
+  }
+}
+template <int DT, int NW>
+__device__ __forceinline__ void round_words(const float* acc, unsigned* w) {
+#pragma unroll
+  for (int k = 0; k < NW; ++k) w[k] = (DT == 0) ? __float_as_uint(acc[k]) : pack2<DT>(acc[2 * k], acc[2 * k + 1]);
+}
+template <int DT, int NW>
+__device__ __forceinline__ void chain_words_fast(const float* acc, const unsigned* y, unsigned* nx, float scale) {
+  // next input = roundTiesToEven(scale * y), y being the rounded output
+  float t[NW * 2];
+  acc_words<DT, NW>(t, y, true);
+  (void)acc;
+#pragma unroll
+  for (int k = 0; k < NW * (DT == 0 ? 1 : 2); ++k) t[k] = __fmul_rn(scale, t[k]);
+  round_words<DT, NW>(t, nx);
+}
+
+// ============================================================ LL one-shot
+// Technique 1: each 8 bytes of data leave with an 8-byte flag (the epoch of
+// this AllReduce) as one 16-byte store; the reader polls that 16-byte line
+// until the flag equals the epoch, so no separate signal and no barrier is
+// needed, and epochs only grow, so lines never need a reset. On one GPU a
+// store into the reader's staging and a load of the writer's staging both
+// travel to the same L2, so each rank publishes its lines once, in its own
+// staging [epoch & 1][word], and every peer reads them there (one store per
+// word instead of N-1). Credit (technique 3): the owner of word w of rank r
+// rewrites slot (E & 1) at epoch E + 2 only after it read word w of epoch
+// E + 1 from every peer, and each peer's owner of word w published that
+// only after reading my epoch-E word w.
+template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER8 = 8 / EB;
-  const int N = p.nranks;
   const int r = blockIdx.x / p.G;
   const int c = blockIdx.x - r * p.G;
   const size_t W = (p.count + PER8 - 1) / PER8;
@@ -89,10 +156,12 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   const size_t w0 = min(W, (size_t)c * per);
   const size_t w1 = min(W, w0 + per);
   const bool injected = (p.inject_rank == r);
-  const size_t src_stride = p.ll_slot_words * kLLLine;
-  const size_t slot_stride = (size_t)N * src_stride;
+  const bool skip = injected && p.inject_mode == LLAR_INJECT_SKIP_;
+  const size_t slot_stride = p.ll_slot_words * (size_t)kLLLine;
   char* const mine = p.ll + (size_t)r * p.ll_stride;
-  const unsigned peers = ((1u << N) - 1u) & ~(1u << r);
+  const char* from[N];  // publisher q's lines
+#pragma unroll
+  for (int q = 0; q < N; ++q) from[q] = p.ll + (size_t)q * p.ll_stride;
 
   for (int e = 0; e < p.iters; ++e) {
     const u64 E = p.epoch0 + (u64)e;
@@ -101,61 +170,49 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
     char* dst = rank_output<DT>(p, r, e);
     if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
 
-    // push my words to every peer
-    if (!(injected && p.inject_mode == LLAR_INJECT_SKIP_)) {
+    if (!skip) {
       const u64 flag = (injected && p.inject_mode == LLAR_INJECT_POISON_) ? E + 2 : E;
-      for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
-        const u64 x = load_word8<DT>(src, w, p.count);
-        char* line = p.ll + slot_off + (size_t)r * src_stride + w * kLLLine;
-#pragma unroll
-        for (int q = 0; q < kMaxRanks; ++q)
-          if (q < N && q != r) st_relaxed_b128(line + (size_t)q * p.ll_stride, x, flag);
-      }
+      for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x)
+        st_relaxed_b128(mine + slot_off + w * kLLLine, load_word8<DT>(src, w, p.count), flag);
     }
 
-    // poll, reduce in rank order, store
     for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
+      const size_t off = slot_off + w * kLLLine;
+      u64 d[N];
+      unsigned ready = 1u << r;
       const u64 own = load_word8<DT>(src, w, p.count);
-      const char* line = mine + slot_off + w * kLLLine;
-      u64 d[kMaxRanks];
-      unsigned pending = peers;
       Waiter wt;
       while (true) {
-        u64 lo[kMaxRanks], hi[kMaxRanks];
+        u64 lo[N], hi[N];
 #pragma unroll
-        for (int q = 0; q < kMaxRanks; ++q)
-          if ((pending >> q) & 1u) ld_relaxed_b128(line + (size_t)q * src_stride, lo[q], hi[q]);
+        for (int q = 0; q < N; ++q)
+          if (!((ready >> q) & 1u)) ld_relaxed_b128(from[q] + off, lo[q], hi[q]);
 #pragma unroll
-        for (int q = 0; q < kMaxRanks; ++q)
-          if (((pending >> q) & 1u) && hi[q] == E) {
+        for (int q = 0; q < N; ++q)
+          if (!((ready >> q) & 1u) && hi[q] == E) {
             d[q] = lo[q];
-            pending &= ~(1u << q);
+            ready |= 1u << q;
           }
-        if (pending == 0u) break;
+        if (ready == (1u << N) - 1u) break;
         if (wt.expired(p)) {
           report_timeout(p, r, c, E);
           return;
         }
+        if (p.poll_sleep_ns > 0) __nanosleep(p.poll_sleep_ns);
       }
       float acc[PER8];
-      {
-        const u64 v0 = (r == 0) ? own : d[0];
-        const unsigned w2[2] = {(unsigned)v0, (unsigned)(v0 >> 32)};
-        init_acc<DT, 2>(acc, w2);
-      }
 #pragma unroll
-      for (int q = 1; q < kMaxRanks; ++q)
-        if (q < N) {
-          const u64 v = (q == r) ? own : d[q];
-          const unsigned w2[2] = {(unsigned)v, (unsigned)(v >> 32)};
-          accumulate<DT, 2>(acc, w2);
-        }
+      for (int q = 0; q < N; ++q) {
+        const u64 v = (q == r) ? own : d[q];
+        const unsigned w2[2] = {(unsigned)v, (unsigned)(v >> 32)};
+        acc_words<DT, 2>(acc, w2, q == 0);
+      }
       unsigned y[2];
-      pack_acc<DT, 2>(acc, y);
+      round_words<DT, 2>(acc, y);
       store_word8<DT>(dst, w, p.count, (u64)y[0] | ((u64)y[1] << 32));
       if (p.chain) {
         unsigned nx[2];
-        chain_words<DT, 2>(y, nx, p.chain_scale);
+        chain_words_fast<DT, 2>(acc, y, nx, p.chain_scale);
         store_word8<DT>(chain_next_buf(p, r, e), w, p.count, (u64)nx[0] | ((u64)nx[1] << 32));
       }
     }
@@ -165,16 +222,17 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
 // ====================================================== sentinel one-shot
 // Technique 2 with technique 3's chunking: staging slot
 // [seq & 1][source][vector] is prefilled with the all-ones (-NaN) pattern;
-// the sender stores raw 16-byte vectors, the receiver polls until no
-// element of the vector is the sentinel, reduces, and writes the sentinel
-// back (the reset). Chunk seq+1 is pushed only after chunk seq was received
-// from every peer, so a peer's slot (seq+1) & 1 was consumed and reset in
-// its chunk seq-1. The reset is ordered before the next push by a fence.
-template <int DT>
+// the owner of vector j pushes my raw 16-byte vector to every peer, polls
+// the vector every peer sent until none of its elements is the sentinel,
+// and writes the sentinel back (the reset). Chunk seq+1 is pushed to peer q
+// only after chunk seq was received from peer q, so peer q's slot
+// (seq+1) & 1 for me was consumed and reset in its chunk seq-1 by the
+// owner of the same vector; a fence orders that reset before the owner's
+// next push.
+template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER16 = 16 / EB;
-  const int N = p.nranks;
   const int r = blockIdx.x / p.G;
   const int c = blockIdx.x - r * p.G;
   const size_t NV = (p.count + PER16 - 1) / PER16;
@@ -185,20 +243,27 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
   const size_t j1 = min(CV, j0 + per);
   const size_t src_stride = CV * 16;
   const size_t slot_stride = (size_t)N * src_stride;
-  char* const mine = p.sen + (size_t)r * p.sen_stride;
   const bool injected = (p.inject_rank == r);
-  const unsigned peers = ((1u << N) - 1u) & ~(1u << r);
   const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  const bool own_stream = !p.chain;  // user input: read-only for the launch
+  char* to[N];
+  char* from[N];
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    to[q] = p.sen + (size_t)q * p.sen_stride + (size_t)r * src_stride;
+    from[q] = p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride;
+  }
+  const char* const lead_line =
+      p.sen + (size_t)r * p.sen_stride + (size_t)((r == N - 1) ? N - 2 : N - 1) * src_stride;
   unsigned long long seq = 0;
 
   for (int e = 0; e < p.iters; ++e) {
     const u64 E = p.epoch0 + (u64)e;
     const char* src = rank_input<DT>(p, r, e);
     char* dst = rank_output<DT>(p, r, e);
-    const bool own_stream = !p.chain;  // user input: read-only for the launch
     for (size_t k = 0; k < nchunks; ++k, ++seq) {
       const size_t slot_off = (size_t)(seq & 1) * slot_stride;
-      if (seq > 0) fence_gpu();  // previous chunk's resets before this chunk's pushes
+      if (seq > 0) fence_gpu();  // my resets of the previous chunk before this chunk's pushes
       if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
       if (!(injected && p.inject_mode == LLAR_INJECT_SKIP_)) {
         const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
@@ -206,60 +271,57 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
           const size_t v = k * CV + j;
           if (v >= NV) break;
           const uint4 x = poison ? ones : load_vec16<DT>(src, v, p.count, own_stream);
-          char* line = p.sen + slot_off + (size_t)r * src_stride + j * 16;
 #pragma unroll
-          for (int q = 0; q < kMaxRanks; ++q)
-            if (q < N && q != r) st_relaxed_v4(line + (size_t)q * p.sen_stride, x);
+          for (int q = 0; q < N; ++q)
+            if (q != r) st_relaxed_v4(to[q] + slot_off + j * 16, x);
         }
       }
       for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
         const size_t v = k * CV + j;
         if (v >= NV) break;
+        const size_t off = slot_off + j * 16;
         const uint4 own = load_vec16<DT>(src, v, p.count, own_stream);
-        char* line = mine + slot_off + j * 16;
-        uint4 d[kMaxRanks];
-        unsigned pending = peers;
+        uint4 d[N];
+        unsigned ready = 1u << r;
         Waiter wt;
+        bool lead_seen = p.poll_mode == 0;
         while (true) {
-          uint4 t[kMaxRanks];
+          uint4 t[N];
+          if (!lead_seen) lead_seen = !has_sentinel<DT>(ld_relaxed_v4(lead_line + off));
+          if (lead_seen) {
 #pragma unroll
-          for (int q = 0; q < kMaxRanks; ++q)
-            if ((pending >> q) & 1u) t[q] = ld_relaxed_v4(line + (size_t)q * src_stride);
+            for (int q = 0; q < N; ++q)
+              if (!((ready >> q) & 1u)) t[q] = ld_relaxed_v4(from[q] + off);
 #pragma unroll
-          for (int q = 0; q < kMaxRanks; ++q)
-            if (((pending >> q) & 1u) && !has_sentinel<DT>(t[q])) {
-              d[q] = t[q];
-              pending &= ~(1u << q);
-            }
-          if (pending == 0u) break;
+            for (int q = 0; q < N; ++q)
+              if (!((ready >> q) & 1u) && !has_sentinel<DT>(t[q])) {
+                d[q] = t[q];
+                ready |= 1u << q;
+              }
+            if (ready == (1u << N) - 1u) break;
+          }
           if (wt.expired(p)) {
             report_timeout(p, r, c, E);
             return;
           }
+          if (p.poll_sleep_ns > 0) __nanosleep(p.poll_sleep_ns);
         }
-        // reset my slot for the next use of this parity
 #pragma unroll
-        for (int q = 0; q < kMaxRanks; ++q)
-          if (q < N && q != r) st_relaxed_v4(line + (size_t)q * src_stride, ones);
+        for (int q = 0; q < N; ++q)
+          if (q != r) st_relaxed_v4(from[q] + off, ones);  // reset for the next use of this slot
         float acc[PER16];
-        {
-          const uint4 v0 = (r == 0) ? own : d[0];
-          const unsigned w4[4] = {v0.x, v0.y, v0.z, v0.w};
-          init_acc<DT, 4>(acc, w4);
-        }
 #pragma unroll
-        for (int q = 1; q < kMaxRanks; ++q)
-          if (q < N) {
-            const uint4 vq = (q == r) ? own : d[q];
-            const unsigned w4[4] = {vq.x, vq.y, vq.z, vq.w};
-            accumulate<DT, 4>(acc, w4);
-          }
+        for (int q = 0; q < N; ++q) {
+          const uint4 vq = (q == r) ? own : d[q];
+          const unsigned w4[4] = {vq.x, vq.y, vq.z, vq.w};
+          acc_words<DT, 4>(acc, w4, q == 0);
+        }
         unsigned y[4];
-        pack_acc<DT, 4>(acc, y);
+        round_words<DT, 4>(acc, y);
         store_vec16<DT>(dst, v, p.count, u4(y));
         if (p.chain) {
           unsigned nx[4];
-          chain_words<DT, 4>(y, nx, p.chain_scale);
+          chain_words_fast<DT, 4>(acc, y, nx, p.chain_scale);
           store_vec16<DT>(chain_next_buf(p, r, e), v, p.count, u4(nx));
         }
       }
@@ -687,11 +749,38 @@ static cudaError_t coop_launch(K kernel, const Params& p, int threads, cudaStrea
     default: return cudaErrorInvalidValue;                                      \
   }
 
+template <int DT, int N>
+static const void* one_shot_kernel(int proto) {
+  return proto == 1 ? (const void*)k_ll<DT, N> : (const void*)k_sentinel<DT, N>;
+}
+template <int DT>
+static const void* one_shot_kernel_n(int proto, int n) {
+  switch (n) {
+    case 2: return one_shot_kernel<DT, 2>(proto);
+    case 3: return one_shot_kernel<DT, 3>(proto);
+    case 4: return one_shot_kernel<DT, 4>(proto);
+    case 5: return one_shot_kernel<DT, 5>(proto);
+    case 6: return one_shot_kernel<DT, 6>(proto);
+    case 7: return one_shot_kernel<DT, 7>(proto);
+    case 8: return one_shot_kernel<DT, 8>(proto);
+    default: return nullptr;
+  }
+}
+static const void* one_shot_kernel_for(int proto, int dtype, int n) {
+  return dtype == 0 ? one_shot_kernel_n<0>(proto, n)
+                    : dtype == 1 ? one_shot_kernel_n<1>(proto, n) : one_shot_kernel_n<2>(proto, n);
+}
+static cudaError_t launch_one_shot(int proto, int dtype, const Params& p, int threads, cudaStream_t s) {
+  const void* k = one_shot_kernel_for(proto, dtype, p.nranks);
+  if (!k) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<Params*>(&p)};
+  return cudaLaunchCooperativeKernel(k, dim3(p.nranks * p.G), dim3(threads), args, 0, s);
+}
 cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s) {
-  LLAR_DISPATCH(k_ll, true)
+  return launch_one_shot(1, dtype, p, threads, s);
 }
 cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_t s) {
-  LLAR_DISPATCH(k_sentinel, true)
+  return launch_one_shot(2, dtype, p, threads, s);
 }
 cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s) {
   LLAR_DISPATCH(k_ll128, true)
@@ -706,8 +795,6 @@ cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaSt
 template <int DT>
 static const void* kernel_for(int proto) {
   switch (proto) {
-    case 1: return (const void*)k_ll<DT>;
-    case 2: return (const void*)k_sentinel<DT>;
     case 3: return (const void*)k_ll128<DT>;
     case 4: return (const void*)k_fixed_oneshot<DT>;
     case 5: return (const void*)k_fixed_twoshot<DT>;
@@ -715,8 +802,9 @@ static const void* kernel_for(int proto) {
   }
 }
 
-int max_resident_ctas(int proto, int dtype, int /*chain*/, int threads) {
-  const void* k = dtype == 0 ? kernel_for<0>(proto) : dtype == 1 ? kernel_for<1>(proto) : kernel_for<2>(proto);
+int max_resident_ctas(int proto, int dtype, int nranks, int threads) {
+  const void* k = (proto == 1 || proto == 2) ? one_shot_kernel_for(proto, dtype, nranks)
+                  : dtype == 0 ? kernel_for<0>(proto) : dtype == 1 ? kernel_for<1>(proto) : kernel_for<2>(proto);
   if (!k) return 0;
   int per_sm = 0, dev = 0, sms = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess) return 0;

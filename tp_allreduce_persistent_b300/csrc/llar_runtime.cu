@@ -57,6 +57,7 @@ std::mutex g_mu;
 Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
+int g_poll_mode = 0, g_poll_sleep_ns = 0;
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
@@ -197,6 +198,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   p.chain_slot_bytes = c.chain_slot;
   p.flags = reinterpret_cast<unsigned long long*>(c.base + c.flags_off);
   p.flags_gmax = kFlagsGmax;
+  p.poll_mode = g_poll_mode;
+  p.poll_sleep_ns = g_poll_sleep_ns;
   p.timeout_ns = g_timeout_ns;
   p.inject_rank = g_inject_rank;
   p.inject_mode = g_inject_mode;
@@ -208,7 +211,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
                     proto == LLAR_PROTO_LL128_ATOMIC || chain;
   if (coop) {
-    const int cap = llar::max_resident_ctas(proto, c.dtype, chain, T);
+    const int cap = llar::max_resident_ctas(proto, c.dtype, c.n, T);
     if (cap <= 0) return LLAR_ERR_CUDA;
     if (c.n * G > cap) {
       if (g_force_G > 0) return LLAR_ERR_OCCUPANCY;
@@ -270,6 +273,8 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_timeout_ns = env_size("LLAR_TIMEOUT_NS", g_timeout_ns);
   g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", (size_t)g_force_G);
   g_force_T = (int)env_size("LLAR_THREADS", (size_t)g_force_T);
+  g_poll_mode = (int)env_size("LLAR_POLL_MODE", (size_t)g_poll_mode);
+  g_poll_sleep_ns = (int)env_size("LLAR_POLL_SLEEP_NS", (size_t)g_poll_sleep_ns);
 
   cudaError_t err = cudaGetDevice(&c->dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);
@@ -286,7 +291,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
     off += *stride * n;
   };
   c->ll_words = (c->ll_cap + 7) / 8;
-  region(2 * (size_t)n * c->ll_words * llar::kLLLine, &c->ll_off, &c->ll_stride);
+  region(2 * c->ll_words * llar::kLLLine, &c->ll_off, &c->ll_stride);  // [slot][word] published lines
   region(2 * (size_t)n * kMaxChunk, &c->sen_off, &c->sen_stride);
   c->l128_lines = ll128_lines_for(c->ll128_cap / c->esize, n, dtype);
   region(2 * c->l128_lines * llar::kLL128Line, &c->l128_off, &c->l128_stride);
@@ -486,7 +491,7 @@ int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes, size_t
   const Ctx& c = *g;
   size_t off = 0, stride = 0, used = 0;
   switch (protocol) {
-    case LLAR_PROTO_LL: off = c.ll_off; stride = c.ll_stride; used = 2 * c.n * c.ll_words * llar::kLLLine; break;
+    case LLAR_PROTO_LL: off = c.ll_off; stride = c.ll_stride; used = 2 * c.ll_words * llar::kLLLine; break;
     case LLAR_PROTO_SENTINEL: off = c.sen_off; stride = c.sen_stride; used = 2 * c.n * c.chunk_bytes; break;
     case LLAR_PROTO_LL128_ATOMIC: off = c.l128_off; stride = c.l128_stride; used = 2 * c.l128_lines * llar::kLL128Line; break;
     default: return LLAR_ERR_UNSUPPORTED;
@@ -507,7 +512,7 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
   switch (protocol) {
     case LLAR_PROTO_LL:
       pl = 8 / e;
-      st = 2 * (size_t)nranks * ((count * e + 7) / 8) * llar::kLLLine;
+      st = 2 * ((count * e + 7) / 8) * llar::kLLLine;  // two slots of the rank's published lines
       break;
     case LLAR_PROTO_SENTINEL: {
       const size_t chunk = g ? g->chunk_bytes : kDefaultChunk;
