@@ -186,6 +186,27 @@ unsigned long long llar_epoch(void);
  * threads per CTA, iterations. Any pointer may be NULL. */
 int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters);
 
+/* One LL AllReduce that allocates nothing: no cudaMalloc, no cudaFree and
+ * no allocating library routine, before or during the call, and no
+ * llar_init needed. (No page describes this entry point; it exists for
+ * callers whose device memory is all owned by a caching allocator or a
+ * fixed budget, e.g. an inference-server plugin, and for latency-critical
+ * paths where cudaMalloc's implicit device synchronisation is not
+ * acceptable.) The LL staging lives in a fixed 1 MiB + 512 B device array
+ * inside this library, held by every GPU that loads it until the process
+ * exits. in[r] / out[r] are as for llar_allreduce; nranks 2..8; dtype an
+ * llar_dtype_t; count * element size must be at most 32 KiB per rank,
+ * else LLAR_ERR_TOO_LARGE. The first call on a device resolves the array's
+ * device address (cudaGetSymbolAddress), so make that first call before
+ * any stream capture. Every call shares the array: calls that overlap on
+ * the GPU (other streams, other threads) race and must be avoided; calls
+ * in one stream are safe. Each call uses a fresh epoch, so no clearing is
+ * needed between calls. A device wait that ran out in an earlier call is
+ * returned as LLAR_ERR_TIMEOUT by a later call made once the stream is
+ * idle (checked with cudaStreamQuery; a 4-byte device-to-host copy). */
+int llar_allreduce_noalloc(const void* const* in, void* const* out, size_t count,
+                           int nranks, int dtype, void* stream);
+
 /* Static description of a status code. */
 const char* llar_strerror(int status);
 

@@ -9,8 +9,11 @@
 // No kernel contains a grid-wide barrier; the only waits are per-line polls
 // (techniques 1, 2, 4) and, on the fixed-order chained paths, per-CTA-pair
 // epoch flags.
+#include <cstring>
+#include <mutex>
 #include <vector>
 
+#include "llar.h"
 #include "llar_device.cuh"
 
 namespace llar {
@@ -956,3 +959,127 @@ done:
 }
 
 }  // namespace llar
+
+// ==================================================== allocation-free LL
+// Some callers cannot allocate device memory at the point where they need
+// an AllReduce: code whose device memory is owned entirely by a caching
+// allocator or a fixed memory budget (an inference server plugin, a
+// framework pool that forbids raw cudaMalloc), or latency-critical paths
+// where cudaMalloc's implicit device synchronisation is not acceptable.
+// For them, llar_allreduce_noalloc runs the LL kernel above with its
+// staging in the fixed-size device array below instead of llar_init's
+// allocation. The array exists once per device for the life of the process.
+using namespace llar;
+namespace {
+
+constexpr size_t kNoAllocMaxBytes = 32u << 10;                   // per rank
+constexpr size_t kNoAllocWords = kNoAllocMaxBytes / 8;           // LL words per rank
+constexpr size_t kNoAllocRankBytes = 2 * kNoAllocWords * kLLLine;  // two slots of lines
+constexpr size_t kNoAllocHeader = 512;                           // abort word + status
+constexpr size_t kNoAllocBytes = kNoAllocHeader + kMaxRanks * kNoAllocRankBytes;
+constexpr int kNoAllocMaxDevices = 64;
+
+// header: [0, 4) abort word, [256, 256 + sizeof(DevStatus)) status; then
+// rank r's LL lines [slot][word] at kNoAllocHeader + r * kNoAllocRankBytes.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sms = 0;
+  unsigned long long epoch = 1;
+};
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+}  // namespace
+
+extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, size_t count,
+                                      int nranks, int dtype, void* stream) {
+  if (nranks < 2 || nranks > kMaxRanks || dtype < 0 || dtype > 2) return LLAR_ERR_INVALID;
+  if (!in || !out) return LLAR_ERR_INVALID;
+  const size_t esize = dtype == 0 ? 4 : 2;
+  const size_t bytes = count * esize;
+  if (bytes > kNoAllocMaxBytes) return LLAR_ERR_TOO_LARGE;
+  for (int r = 0; r < nranks; ++r) {
+    if (!in[r] || !out[r] || (((uintptr_t)in[r] | (uintptr_t)out[r]) & 15u)) return LLAR_ERR_INVALID;
+    for (int q = 0; q < nranks; ++q) {
+      const uintptr_t o0 = (uintptr_t)out[r], i0 = (uintptr_t)in[q];
+      if (o0 < i0 + bytes && i0 < o0 + bytes) return LLAR_ERR_INVALID;
+      const uintptr_t p0 = (uintptr_t)out[q];
+      if (q != r && o0 < p0 + bytes && p0 < o0 + bytes) return LLAR_ERR_INVALID;
+    }
+  }
+  if (count == 0) return LLAR_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    cudaGetLastError();
+    return LLAR_ERR_CUDA;
+  }
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    // first call on this device: resolve the array's device address (the
+    // host-side name is only a stand-in) and the SM count
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return LLAR_ERR_CUDA;
+    }
+    d.scratch = static_cast<char*>(ptr);
+    d.ready = true;
+  }
+  // a wait that ran out in an earlier call is reported once that call has
+  // drained from the stream; the word is then cleared
+  if (cudaStreamQuery(s) == cudaSuccess) {
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, d.scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaGetLastError();
+      return LLAR_ERR_CUDA;
+    }
+    if (word != 0) {
+      cudaMemsetAsync(d.scratch, 0, kNoAllocHeader, s);
+      return LLAR_ERR_TIMEOUT;
+    }
+  } else {
+    cudaGetLastError();  // cudaErrorNotReady: still busy, check on a later call
+  }
+
+  Params p;
+  memset(&p, 0, sizeof(p));
+  for (int r = 0; r < nranks; ++r) {
+    p.in[r] = static_cast<const char*>(in[r]);
+    p.out[r] = static_cast<char*>(out[r]);
+  }
+  p.count = count;
+  p.nranks = nranks;
+  p.iters = 1;
+  p.epoch0 = d.epoch;
+  p.ll = d.scratch + kNoAllocHeader;
+  p.ll_stride = kNoAllocRankBytes;
+  p.ll_slot_words = kNoAllocWords;
+  p.timeout_ns = 1000000000ull;
+  p.inject_rank = -1;
+  p.abort_flag = reinterpret_cast<unsigned*>(d.scratch);
+  p.status = reinterpret_cast<DevStatus*>(d.scratch + 256);
+  const size_t words = (bytes + 7) / 8;
+  const int threads = 128;
+  int G = (int)((words + threads - 1) / threads);
+  G = G < 1 ? 1 : G;
+  const int one_per_sm = d.sms / nranks > 0 ? d.sms / nranks : 1;
+  G = G > one_per_sm ? one_per_sm : G;
+  const int cap = max_resident_ctas(1, dtype, nranks, threads);
+  if (cap <= 0) return LLAR_ERR_CUDA;
+  if (nranks * G > cap) G = cap / nranks > 0 ? cap / nranks : 1;
+  p.G = G;
+  const cudaError_t err = launch_ll(dtype, p, threads, s);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return err == cudaErrorCooperativeLaunchTooLarge ? LLAR_ERR_OCCUPANCY : LLAR_ERR_CUDA;
+  }
+  d.epoch += 1;
+  return LLAR_OK;
+}

@@ -46,6 +46,7 @@ def lib():
         "llar_allreduce": (c_int, [pp, pp, c_size, c_int, c_vp]),
         "llar_allreduce_iters": (c_int, [pp, pp, c_size, c_int, c_int, c_size, c_size, ctypes.c_float, c_vp]),
         "llar_allreduce_host": (c_int, [c_vp, c_vp, c_size, c_int, c_vp]),
+        "llar_allreduce_noalloc": (c_int, [pp, pp, c_size, c_int, c_int, c_vp]),
         "llar_get_status": (c_int, [ctypes.POINTER(c_int), ctypes.POINTER(c_int), ctypes.POINTER(c_ull)]),
         "llar_reset": (c_int, [c_vp]),
         "llar_set_timeout_ns": (None, [c_ull]),
@@ -139,6 +140,13 @@ def llar_allreduce_host(in_host, out_host, count, protocol="auto", stream=None):
                                      int(count), _enum(PROTOCOLS, protocol),
                                      ctypes.c_void_p(_stream(stream))),
            "llar_allreduce_host")
+
+
+def llar_allreduce_noalloc(ins, outs, count, nranks, dtype, stream=None):
+    """LL AllReduce with library-internal static staging (no allocation, no init)."""
+    _check(lib().llar_allreduce_noalloc(_ptr_array(ins), _ptr_array(outs), int(count), int(nranks),
+                                        _enum(DTYPES, dtype), ctypes.c_void_p(_stream(stream))),
+           "llar_allreduce_noalloc")
 
 
 def llar_get_status():
