@@ -155,7 +155,8 @@ def compare_atomic(got_bits, want_bits, x_bits, dtype):
     nan_ok = np.isnan(got) == np.isnan(want)
     inf_ok = np.where(np.isinf(want) | np.isinf(got), got == want, True)
     finite = np.isfinite(got) & np.isfinite(want)
-    err = np.where(finite, np.abs(got - want), 0.0)
+    with np.errstate(invalid="ignore", over="ignore"):
+        err = np.where(finite, np.abs(got - want), 0.0)
     ok = bool(np.all(nan_ok) and np.all(inf_ok) and np.all(err <= tol))
     rel = float(np.max(err / tol)) if err.size else 0.0
     return ok, float(err.max()) if err.size else 0.0, rel
