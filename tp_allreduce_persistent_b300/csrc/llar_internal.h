@@ -38,6 +38,7 @@ struct Params {
   size_t count;               // elements per rank
   int nranks;
   int G;                      // CTAs per rank
+  int clustered;              // launch in clusters of nranks blocks (one CTA per rank, same range)
   int iters;
   int chain;                  // 1: next input = RNE(chain_scale * output)
   float chain_scale;
@@ -58,9 +59,6 @@ struct Params {
   unsigned long long* flags;                    // [N][Gmax][2] ready/done epochs
   int flags_gmax;
 
-  int poll_mode;      // 0: poll every pending line each round; 1: poll one lead line until it
-                      // is ready, then the rest
-  int poll_sleep_ns;  // pause between unsuccessful poll rounds (0 = spin)
   unsigned long long timeout_ns;
   int inject_rank;
   int inject_mode;
@@ -76,8 +74,9 @@ cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaSt
 cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s);
 
 // Largest number of CTAs of the kernel for (proto, dtype, nranks) that can
-// be resident at once with `threads` threads each (0 on error).
-int max_resident_ctas(int proto, int dtype, int nranks, int threads);
+// be resident at once with `threads` threads each, in clusters of nranks
+// blocks if `clustered` (0 on error).
+int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered);
 
 // Speed-of-light probes: per-SM pointer-chase latency (ns per dependent
 // L2 load) and per-pair ping-pong round trips (ns per store-observe-reply).

@@ -74,6 +74,12 @@ __device__ __forceinline__ void store_vec16(char* base, size_t v, size_t count, 
 
 __device__ __forceinline__ uint4 u4(const unsigned* w) { return make_uint4(w[0], w[1], w[2], w[3]); }
 
+// Block b is CTA c = b / N of virtual rank r = b % N: the N CTAs that serve
+// the same range c of every rank are consecutive, so a launch with a
+// cluster of N blocks puts each such group on one GPC.
+__device__ __forceinline__ int rank_of_block(const Params& p) { return blockIdx.x % p.nranks; }
+__device__ __forceinline__ int cta_of_block(const Params& p) { return blockIdx.x / p.nranks; }
+
 // One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
 // the thread pushes its unit of my data to every peer, polls the unit every
 // peer sent, adds the N values in rank order and stores the result. The
@@ -148,61 +154,72 @@ __device__ __forceinline__ void chain_words_fast(const float* acc, const unsigne
 // rewrites slot (E & 1) at epoch E + 2 only after it read word w of epoch
 // E + 1 from every peer, and each peer's owner of word w published that
 // only after reading my epoch-E word w.
-template <int DT, int N>
+template <int DT, int N, bool CHAIN>
 __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER8 = 8 / EB;
-  const int r = blockIdx.x / p.G;
-  const int c = blockIdx.x - r * p.G;
-  const size_t W = (p.count + PER8 - 1) / PER8;
-  const size_t per = (W + p.G - 1) / p.G;
-  const size_t w0 = min(W, (size_t)c * per);
-  const size_t w1 = min(W, w0 + per);
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const unsigned W = (unsigned)((p.count + PER8 - 1) / PER8);
+  const unsigned per = (W + p.G - 1) / p.G;
+  const unsigned w0 = min(W, (unsigned)c * per);
+  const unsigned w1 = min(W, w0 + per);
+  const bool full = (p.count % PER8) == 0;  // no partial word at the end
   const bool injected = (p.inject_rank == r);
   const bool skip = injected && p.inject_mode == LLAR_INJECT_SKIP_;
+  const u64 flag_add = (injected && p.inject_mode == LLAR_INJECT_POISON_) ? 2 : 0;
   const size_t slot_stride = p.ll_slot_words * (size_t)kLLLine;
   char* const mine = p.ll + (size_t)r * p.ll_stride;
   const char* from[N];  // publisher q's lines
 #pragma unroll
   for (int q = 0; q < N; ++q) from[q] = p.ll + (size_t)q * p.ll_stride;
+  const unsigned others = ((1u << N) - 1u) & ~(1u << r);
 
   for (int e = 0; e < p.iters; ++e) {
     const u64 E = p.epoch0 + (u64)e;
     const size_t slot_off = (size_t)(E & 1) * slot_stride;
-    const char* src = rank_input<DT>(p, r, e);
+    const char* src = CHAIN ? rank_input<DT>(p, r, e) : p.in[r] + (size_t)e * p.in_stride * EB;
     char* dst = rank_output<DT>(p, r, e);
     if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
 
     if (!skip) {
-      const u64 flag = (injected && p.inject_mode == LLAR_INJECT_POISON_) ? E + 2 : E;
-      for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x)
-        st_relaxed_b128(mine + slot_off + w * kLLLine, load_word8<DT>(src, w, p.count), flag);
+      for (unsigned w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
+        const u64 x = (full || w + 1 < W) ? *reinterpret_cast<const u64*>(src + (size_t)w * 8)
+                                          : load_word8<DT>(src, w, p.count);
+        st_relaxed_b128(mine + slot_off + (size_t)w * kLLLine, x, E + flag_add);
+      }
     }
 
-    for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
-      const size_t off = slot_off + w * kLLLine;
+    for (unsigned w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
+      const size_t off = slot_off + (size_t)w * kLLLine;
+      const u64 own = (full || w + 1 < W) ? *reinterpret_cast<const u64*>(src + (size_t)w * 8)
+                                          : load_word8<DT>(src, w, p.count);
       u64 d[N];
-      unsigned ready = 1u << r;
-      const u64 own = load_word8<DT>(src, w, p.count);
-      Waiter wt;
+      unsigned pend = others;
+      unsigned spins = 0;
+      u64 deadline = 0;
       while (true) {
         u64 lo[N], hi[N];
 #pragma unroll
         for (int q = 0; q < N; ++q)
-          if (!((ready >> q) & 1u)) ld_relaxed_b128(from[q] + off, lo[q], hi[q]);
+          if ((pend >> q) & 1u) ld_relaxed_b128(from[q] + off, lo[q], hi[q]);
 #pragma unroll
         for (int q = 0; q < N; ++q)
-          if (!((ready >> q) & 1u) && hi[q] == E) {
+          if (((pend >> q) & 1u) && hi[q] == E) {
             d[q] = lo[q];
-            ready |= 1u << q;
+            pend &= ~(1u << q);
           }
-        if (ready == (1u << N) - 1u) break;
-        if (wt.expired(p)) {
-          report_timeout(p, r, c, E);
-          return;
+        if (pend == 0u) break;
+        if ((++spins & 63u) == 0u) {  // bounded wait: clock and abort word every 64 rounds
+          const u64 now = globaltimer_ns();
+          if (deadline == 0) deadline = now + p.timeout_ns;
+          if (now > deadline || ld_relaxed_u32(p.abort_flag) != 0) {
+            report_timeout(p, r, c, E);
+            return;
+          }
         }
-        if (p.poll_sleep_ns > 0) __nanosleep(p.poll_sleep_ns);
       }
+      // rank-order float32 sum, one rounding
       float acc[PER8];
 #pragma unroll
       for (int q = 0; q < N; ++q) {
@@ -212,8 +229,10 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
       }
       unsigned y[2];
       round_words<DT, 2>(acc, y);
-      store_word8<DT>(dst, w, p.count, (u64)y[0] | ((u64)y[1] << 32));
-      if (p.chain) {
+      const u64 yw = (u64)y[0] | ((u64)y[1] << 32);
+      if (full || w + 1 < W) *reinterpret_cast<u64*>(dst + (size_t)w * 8) = yw;
+      else store_word8<DT>(dst, w, p.count, yw);
+      if (CHAIN) {
         unsigned nx[2];
         chain_words_fast<DT, 2>(acc, y, nx, p.chain_scale);
         store_word8<DT>(chain_next_buf(p, r, e), w, p.count, (u64)nx[0] | ((u64)nx[1] << 32));
@@ -236,8 +255,8 @@ template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER16 = 16 / EB;
-  const int r = blockIdx.x / p.G;
-  const int c = blockIdx.x - r * p.G;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
   const size_t NV = (p.count + PER16 - 1) / PER16;
   const size_t CV = (size_t)p.sen_chunk_vecs;
   const size_t nchunks = (NV + CV - 1) / CV;
@@ -256,8 +275,6 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
     to[q] = p.sen + (size_t)q * p.sen_stride + (size_t)r * src_stride;
     from[q] = p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride;
   }
-  const char* const lead_line =
-      p.sen + (size_t)r * p.sen_stride + (size_t)((r == N - 1) ? N - 2 : N - 1) * src_stride;
   unsigned long long seq = 0;
 
   for (int e = 0; e < p.iters; ++e) {
@@ -287,27 +304,22 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
         uint4 d[N];
         unsigned ready = 1u << r;
         Waiter wt;
-        bool lead_seen = p.poll_mode == 0;
         while (true) {
           uint4 t[N];
-          if (!lead_seen) lead_seen = !has_sentinel<DT>(ld_relaxed_v4(lead_line + off));
-          if (lead_seen) {
 #pragma unroll
-            for (int q = 0; q < N; ++q)
-              if (!((ready >> q) & 1u)) t[q] = ld_relaxed_v4(from[q] + off);
+          for (int q = 0; q < N; ++q)
+            if (!((ready >> q) & 1u)) t[q] = ld_relaxed_v4(from[q] + off);
 #pragma unroll
-            for (int q = 0; q < N; ++q)
-              if (!((ready >> q) & 1u) && !has_sentinel<DT>(t[q])) {
-                d[q] = t[q];
-                ready |= 1u << q;
-              }
-            if (ready == (1u << N) - 1u) break;
-          }
+          for (int q = 0; q < N; ++q)
+            if (!((ready >> q) & 1u) && !has_sentinel<DT>(t[q])) {
+              d[q] = t[q];
+              ready |= 1u << q;
+            }
+          if (ready == (1u << N) - 1u) break;
           if (wt.expired(p)) {
             report_timeout(p, r, c, E);
             return;
           }
-          if (p.poll_sleep_ns > 0) __nanosleep(p.poll_sleep_ns);
         }
 #pragma unroll
         for (int q = 0; q < N; ++q)
@@ -375,8 +387,8 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
   constexpr int EL = 128 / EB;  // elements per line
   constexpr int P = EL - 1;     // data elements per line
   const int N = p.nranks;
-  const int r = blockIdx.x / p.G;
-  const int c = blockIdx.x - r * p.G;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
   const size_t count = p.count;
   const size_t seg = (count + N - 1) / N;
   const size_t L = (seg + P - 1) / P;
@@ -676,8 +688,8 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
   constexpr int PER16 = 16 / Fmt<DT>::kBytes;
   __shared__ int s_fail;
-  const int r = blockIdx.x / p.G;
-  const int c = blockIdx.x - r * p.G;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
   const size_t NV = (p.count + PER16 - 1) / PER16;
   const size_t per = (NV + p.G - 1) / p.G;
   const size_t v0 = min(NV, (size_t)c * per);
@@ -702,8 +714,8 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
   constexpr int PER16 = 16 / Fmt<DT>::kBytes;
   __shared__ int s_fail;
   const int N = p.nranks;
-  const int r = blockIdx.x / p.G;
-  const int c = blockIdx.x - r * p.G;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
   const size_t NV = (p.count + PER16 - 1) / PER16;
   const size_t segv = (NV + N - 1) / N;
   const size_t per = (segv + p.G - 1) / p.G;
@@ -735,49 +747,75 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
 }
 
 // ============================================================ launchers
-template <typename K>
-static cudaError_t coop_launch(K kernel, const Params& p, int threads, cudaStream_t s) {
+// Launch N x G blocks: cooperative when CTAs wait on each other (the
+// runtime refuses a grid that cannot be fully resident), in clusters of N
+// blocks (one CTA of every rank for the same range, on one GPC) when
+// p.clustered is set.
+static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream_t s, bool coop,
+                                        cudaLaunchAttribute* at) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nranks * p.G);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  int na = 0;
+  if (coop) {
+    at[na].id = cudaLaunchAttributeCooperative;
+    at[na].val.cooperative = 1;
+    ++na;
+  }
+  if (p.clustered) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = p.nranks;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cfg;
+}
+static cudaError_t launch_kernel(const void* k, const Params& p, int threads, cudaStream_t s, bool coop) {
+  cudaLaunchAttribute at[2];
+  cudaLaunchConfig_t cfg = launch_config(p, threads, s, coop, at);
   void* args[] = {const_cast<Params*>(&p)};
-  return cudaLaunchCooperativeKernel((const void*)kernel, dim3(p.nranks * p.G), dim3(threads), args, 0, s);
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
-#define LLAR_DISPATCH(KERNEL, COOP)                                             \
-  switch (dtype) {                                                              \
-    case 0: return (COOP) ? coop_launch(KERNEL<0>, p, threads, s)                \
-                          : (KERNEL<0><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
-    case 1: return (COOP) ? coop_launch(KERNEL<1>, p, threads, s)                \
-                          : (KERNEL<1><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
-    case 2: return (COOP) ? coop_launch(KERNEL<2>, p, threads, s)                \
-                          : (KERNEL<2><<<p.nranks * p.G, threads, 0, s>>>(p), cudaGetLastError()); \
-    default: return cudaErrorInvalidValue;                                      \
+#define LLAR_DISPATCH(KERNEL, COOP)                                                        \
+  switch (dtype) {                                                                         \
+    case 0: return launch_kernel((const void*)KERNEL<0>, p, threads, s, (COOP));           \
+    case 1: return launch_kernel((const void*)KERNEL<1>, p, threads, s, (COOP));           \
+    case 2: return launch_kernel((const void*)KERNEL<2>, p, threads, s, (COOP));           \
+    default: return cudaErrorInvalidValue;                                                 \
   }
 
 template <int DT, int N>
-static const void* one_shot_kernel(int proto) {
-  return proto == 1 ? (const void*)k_ll<DT, N> : (const void*)k_sentinel<DT, N>;
+static const void* one_shot_kernel(int proto, bool chain) {
+  if (proto == 1) return chain ? (const void*)k_ll<DT, N, true> : (const void*)k_ll<DT, N, false>;
+  return (const void*)k_sentinel<DT, N>;
 }
 template <int DT>
-static const void* one_shot_kernel_n(int proto, int n) {
+static const void* one_shot_kernel_n(int proto, int n, bool chain) {
   switch (n) {
-    case 2: return one_shot_kernel<DT, 2>(proto);
-    case 3: return one_shot_kernel<DT, 3>(proto);
-    case 4: return one_shot_kernel<DT, 4>(proto);
-    case 5: return one_shot_kernel<DT, 5>(proto);
-    case 6: return one_shot_kernel<DT, 6>(proto);
-    case 7: return one_shot_kernel<DT, 7>(proto);
-    case 8: return one_shot_kernel<DT, 8>(proto);
+    case 2: return one_shot_kernel<DT, 2>(proto, chain);
+    case 3: return one_shot_kernel<DT, 3>(proto, chain);
+    case 4: return one_shot_kernel<DT, 4>(proto, chain);
+    case 5: return one_shot_kernel<DT, 5>(proto, chain);
+    case 6: return one_shot_kernel<DT, 6>(proto, chain);
+    case 7: return one_shot_kernel<DT, 7>(proto, chain);
+    case 8: return one_shot_kernel<DT, 8>(proto, chain);
     default: return nullptr;
   }
 }
-static const void* one_shot_kernel_for(int proto, int dtype, int n) {
-  return dtype == 0 ? one_shot_kernel_n<0>(proto, n)
-                    : dtype == 1 ? one_shot_kernel_n<1>(proto, n) : one_shot_kernel_n<2>(proto, n);
+static const void* one_shot_kernel_for(int proto, int dtype, int n, bool chain) {
+  return dtype == 0 ? one_shot_kernel_n<0>(proto, n, chain)
+                    : dtype == 1 ? one_shot_kernel_n<1>(proto, n, chain) : one_shot_kernel_n<2>(proto, n, chain);
 }
 static cudaError_t launch_one_shot(int proto, int dtype, const Params& p, int threads, cudaStream_t s) {
-  const void* k = one_shot_kernel_for(proto, dtype, p.nranks);
+  const void* k = one_shot_kernel_for(proto, dtype, p.nranks, p.chain != 0);
   if (!k) return cudaErrorInvalidValue;
-  void* args[] = {const_cast<Params*>(&p)};
-  return cudaLaunchCooperativeKernel(k, dim3(p.nranks * p.G), dim3(threads), args, 0, s);
+  return launch_kernel(k, p, threads, s, true);
 }
 cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s) {
   return launch_one_shot(1, dtype, p, threads, s);
@@ -805,10 +843,26 @@ static const void* kernel_for(int proto) {
   }
 }
 
-int max_resident_ctas(int proto, int dtype, int nranks, int threads) {
-  const void* k = (proto == 1 || proto == 2) ? one_shot_kernel_for(proto, dtype, nranks)
+int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered) {
+  const void* k = (proto == 1 || proto == 2) ? one_shot_kernel_for(proto, dtype, nranks, false)
                   : dtype == 0 ? kernel_for<0>(proto) : dtype == 1 ? kernel_for<1>(proto) : kernel_for<2>(proto);
   if (!k) return 0;
+  if (clustered) {
+    // how many clusters of nranks blocks fit at once, times the cluster size
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.nranks = nranks;
+    p.G = 1;
+    p.clustered = 1;
+    cudaLaunchAttribute at[2];
+    cudaLaunchConfig_t cfg = launch_config(p, threads, 0, false, at);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return clusters * nranks;
+  }
   int per_sm = 0, dev = 0, sms = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess) return 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1071,7 +1125,12 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
   G = G < 1 ? 1 : G;
   const int one_per_sm = d.sms / nranks > 0 ? d.sms / nranks : 1;
   G = G > one_per_sm ? one_per_sm : G;
-  const int cap = max_resident_ctas(1, dtype, nranks, threads);
+  p.clustered = 1;
+  int cap = max_resident_ctas(1, dtype, nranks, threads, true);
+  if (cap <= 0) {
+    p.clustered = 0;
+    cap = max_resident_ctas(1, dtype, nranks, threads, false);
+  }
   if (cap <= 0) return LLAR_ERR_CUDA;
   if (nranks * G > cap) G = cap / nranks > 0 ? cap / nranks : 1;
   p.G = G;

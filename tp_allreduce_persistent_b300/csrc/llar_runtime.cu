@@ -57,7 +57,7 @@ std::mutex g_mu;
 Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
-int g_poll_mode = 0, g_poll_sleep_ns = 0;
+int g_cluster = 1, g_log = 0;
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
@@ -198,8 +198,6 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   p.chain_slot_bytes = c.chain_slot;
   p.flags = reinterpret_cast<unsigned long long*>(c.base + c.flags_off);
   p.flags_gmax = kFlagsGmax;
-  p.poll_mode = g_poll_mode;
-  p.poll_sleep_ns = g_poll_sleep_ns;
   p.timeout_ns = g_timeout_ns;
   p.inject_rank = g_inject_rank;
   p.inject_mode = g_inject_mode;
@@ -210,8 +208,15 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   choose_shape(c, proto, count, chain, &G, &T);
   const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
                     proto == LLAR_PROTO_LL128_ATOMIC || chain;
+  // ranks that exchange data run their CTA c in one cluster (one GPC):
+  // measured 20-25% lower latency than spreading them over the GPU
+  p.clustered = (coop && g_cluster) ? 1 : 0;
   if (coop) {
-    const int cap = llar::max_resident_ctas(proto, c.dtype, c.n, T);
+    int cap = llar::max_resident_ctas(proto, c.dtype, c.n, T, p.clustered != 0);
+    if (cap <= 0 && p.clustered) {
+      p.clustered = 0;
+      cap = llar::max_resident_ctas(proto, c.dtype, c.n, T, false);
+    }
     if (cap <= 0) return LLAR_ERR_CUDA;
     if (c.n * G > cap) {
       if (g_force_G > 0) return LLAR_ERR_OCCUPANCY;
@@ -219,6 +224,9 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     }
   }
   p.G = G;
+  if (g_log)
+    std::fprintf(stderr, "llar: protocol %d, %d ranks x %d CTAs x %d threads, clustered %d, iters %d, count %zu\n",
+                 proto, c.n, G, T, p.clustered, iters, count);
   cudaError_t err;
   switch (proto) {
     case LLAR_PROTO_LL: err = llar::launch_ll(c.dtype, p, T, stream); break;
@@ -273,8 +281,8 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_timeout_ns = env_size("LLAR_TIMEOUT_NS", g_timeout_ns);
   g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", (size_t)g_force_G);
   g_force_T = (int)env_size("LLAR_THREADS", (size_t)g_force_T);
-  g_poll_mode = (int)env_size("LLAR_POLL_MODE", (size_t)g_poll_mode);
-  g_poll_sleep_ns = (int)env_size("LLAR_POLL_SLEEP_NS", (size_t)g_poll_sleep_ns);
+  g_cluster = (int)env_size("LLAR_CLUSTER", (size_t)g_cluster);
+  g_log = (int)env_size("LLAR_LOG", (size_t)g_log);
 
   cudaError_t err = cudaGetDevice(&c->dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);
