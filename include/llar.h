@@ -179,7 +179,10 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
 /* The protocol LLAR_PROTO_AUTO picks for this size (host-only). */
 int llar_select_protocol(int nranks, int dtype, size_t count);
 
-/* Epoch the next launch starts from; strictly increasing, never reset. */
+/* Epoch the next launch will use for its first AllReduce; strictly
+ * increasing, never reset. The counter lives in device memory (each launch
+ * advances it when its last CTA finishes), so launches captured in a CUDA
+ * graph get fresh epochs on every replay. Synchronises the device to read it. */
 unsigned long long llar_epoch(void);
 
 /* Launch shape of the most recent launch: protocol used, CTAs per rank,

@@ -49,7 +49,7 @@ def test_layout_constants(dtype):
 
 
 def test_protocol_selection_is_monotone_in_size():
-    order = ["ll", "sentinel", "ll128", "fixed_twoshot"]
+    order = ["ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"]
     last = 0
     for nbytes in [16, 4096, 16384, 65536, 1 << 18, 1 << 20, 1 << 22, 1 << 26]:
         p = llar.llar_select_protocol(8, "bf16", nbytes // 2)

@@ -44,7 +44,8 @@ struct Params {
   float chain_scale;
   size_t in_stride;           // elements between iterations' inputs
   size_t out_stride;          // elements between iterations' outputs
-  unsigned long long epoch0;  // epoch of iteration 0 (>= 1, strictly increasing)
+  unsigned long long* epoch_dev;  // device epoch counter: iteration e uses *epoch_dev + 1 + e
+  unsigned int* done_count;       // CTAs of this launch that finished (last one advances the epoch)
 
   // staging regions (device memory), rank r's region at base + r * stride
   char* ll;            size_t ll_stride;        // [2][N][W][16]

@@ -80,6 +80,28 @@ __device__ __forceinline__ uint4 u4(const unsigned* w) { return make_uint4(w[0],
 __device__ __forceinline__ int rank_of_block(const Params& p) { return blockIdx.x % p.nranks; }
 __device__ __forceinline__ int cta_of_block(const Params& p) { return blockIdx.x / p.nranks; }
 
+// Epochs live in device memory, so a launch captured in a CUDA graph and
+// replayed still gets fresh epochs: every CTA reads the counter when it
+// starts (iteration e of the launch uses counter + 1 + e), and the last CTA
+// to finish, which knows that every CTA has read it, advances it by the
+// launch's iteration count.
+__device__ __forceinline__ u64 launch_epoch(const Params& p) {
+  return *reinterpret_cast<volatile const u64*>(p.epoch_dev) + 1;
+}
+__device__ __forceinline__ void finish_launch(const Params& p) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.done_count, 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(p.done_count, 0u);
+      volatile u64* ep = p.epoch_dev;
+      *ep = *ep + (u64)p.iters;
+      __threadfence();
+    }
+  }
+}
+
 // One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
 // the thread pushes its unit of my data to every peer, polls the unit every
 // peer sent, adds the N values in rank order and stores the result. The
@@ -155,7 +177,7 @@ __device__ __forceinline__ void chain_words_fast(const float* acc, const unsigne
 // E + 1 from every peer, and each peer's owner of word w published that
 // only after reading my epoch-E word w.
 template <int DT, int N, bool CHAIN>
-__global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
+__device__ __forceinline__ void body_ll(const Params& p, const u64 epoch0) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER8 = 8 / EB;
   const int r = rank_of_block(p);
@@ -176,7 +198,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   const unsigned others = ((1u << N) - 1u) & ~(1u << r);
 
   for (int e = 0; e < p.iters; ++e) {
-    const u64 E = p.epoch0 + (u64)e;
+    const u64 E = epoch0 + (u64)e;
     const size_t slot_off = (size_t)(E & 1) * slot_stride;
     const char* src = CHAIN ? rank_input<DT>(p, r, e) : p.in[r] + (size_t)e * p.in_stride * EB;
     char* dst = rank_output<DT>(p, r, e);
@@ -241,6 +263,13 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   }
 }
 
+template <int DT, int N, bool CHAIN>
+__global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_ll<DT, N, CHAIN>(p, epoch0);
+  finish_launch(p);
+}
+
 // ====================================================== sentinel one-shot
 // Technique 2 with technique 3's chunking: staging slot
 // [seq & 1][source][vector] is prefilled with the all-ones (-NaN) pattern;
@@ -251,74 +280,86 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
 // (seq+1) & 1 for me was consumed and reset in its chunk seq-1 by the
 // owner of the same vector; a fence orders that reset before the owner's
 // next push.
-template <int DT, int N>
-__global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
+template <int DT, int N, bool CHAIN>
+__device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int PER16 = 16 / EB;
   const int r = rank_of_block(p);
   const int c = cta_of_block(p);
-  const size_t NV = (p.count + PER16 - 1) / PER16;
-  const size_t CV = (size_t)p.sen_chunk_vecs;
-  const size_t nchunks = (NV + CV - 1) / CV;
-  const size_t per = (CV + p.G - 1) / p.G;
-  const size_t j0 = min(CV, (size_t)c * per);
-  const size_t j1 = min(CV, j0 + per);
-  const size_t src_stride = CV * 16;
+  const unsigned NV = (unsigned)((p.count + PER16 - 1) / PER16);
+  const bool full = (p.count % PER16) == 0;  // no partial vector at the end
+  const unsigned CV = (unsigned)p.sen_chunk_vecs;
+  const unsigned nchunks = (NV + CV - 1) / CV;
+  const unsigned per = (CV + p.G - 1) / p.G;
+  const unsigned j0 = min(CV, (unsigned)c * per);
+  const unsigned j1 = min(CV, j0 + per);
+  const size_t src_stride = (size_t)CV * 16;
   const size_t slot_stride = (size_t)N * src_stride;
   const bool injected = (p.inject_rank == r);
+  const bool skip = injected && p.inject_mode == LLAR_INJECT_SKIP_;
+  const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
   const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-  const bool own_stream = !p.chain;  // user input: read-only for the launch
-  char* to[N];
-  char* from[N];
+  char* to[N];    // my slots in peer q's staging
+  char* from[N];  // peer q's slots in my staging
 #pragma unroll
   for (int q = 0; q < N; ++q) {
     to[q] = p.sen + (size_t)q * p.sen_stride + (size_t)r * src_stride;
     from[q] = p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride;
   }
+  const unsigned others = ((1u << N) - 1u) & ~(1u << r);
   unsigned long long seq = 0;
 
   for (int e = 0; e < p.iters; ++e) {
-    const u64 E = p.epoch0 + (u64)e;
-    const char* src = rank_input<DT>(p, r, e);
+    const u64 E = epoch0 + (u64)e;
+    const char* src = CHAIN ? rank_input<DT>(p, r, e) : p.in[r] + (size_t)e * p.in_stride * EB;
     char* dst = rank_output<DT>(p, r, e);
-    for (size_t k = 0; k < nchunks; ++k, ++seq) {
+    for (unsigned k = 0; k < nchunks; ++k, ++seq) {
       const size_t slot_off = (size_t)(seq & 1) * slot_stride;
       if (seq > 0) fence_gpu();  // my resets of the previous chunk before this chunk's pushes
       if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
-      if (!(injected && p.inject_mode == LLAR_INJECT_SKIP_)) {
-        const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
-        for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-          const size_t v = k * CV + j;
+      if (!skip) {
+        for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+          const unsigned v = k * CV + j;
           if (v >= NV) break;
-          const uint4 x = poison ? ones : load_vec16<DT>(src, v, p.count, own_stream);
+          const uint4 x = poison ? ones
+                          : (full || v + 1 < NV) ? (CHAIN ? ld_cg_v4(src + (size_t)v * 16)
+                                                          : ld_stream_v4(src + (size_t)v * 16))
+                                                 : load_vec16<DT>(src, v, p.count, !CHAIN);
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if (q != r) st_relaxed_v4(to[q] + slot_off + j * 16, x);
+            if (q != r) st_relaxed_v4(to[q] + slot_off + (size_t)j * 16, x);
         }
       }
-      for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
-        const size_t v = k * CV + j;
+      for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+        const unsigned v = k * CV + j;
         if (v >= NV) break;
-        const size_t off = slot_off + j * 16;
-        const uint4 own = load_vec16<DT>(src, v, p.count, own_stream);
+        const size_t off = slot_off + (size_t)j * 16;
+        const uint4 own = (full || v + 1 < NV) ? (CHAIN ? ld_cg_v4(src + (size_t)v * 16)
+                                                        : ld_stream_v4(src + (size_t)v * 16))
+                                               : load_vec16<DT>(src, v, p.count, !CHAIN);
         uint4 d[N];
-        unsigned ready = 1u << r;
-        Waiter wt;
+        unsigned pend = others;
+        unsigned spins = 0;
+        u64 deadline = 0;
         while (true) {
           uint4 t[N];
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if (!((ready >> q) & 1u)) t[q] = ld_relaxed_v4(from[q] + off);
+            if ((pend >> q) & 1u) t[q] = ld_relaxed_v4(from[q] + off);
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if (!((ready >> q) & 1u) && !has_sentinel<DT>(t[q])) {
+            if (((pend >> q) & 1u) && !has_sentinel<DT>(t[q])) {
               d[q] = t[q];
-              ready |= 1u << q;
+              pend &= ~(1u << q);
             }
-          if (ready == (1u << N) - 1u) break;
-          if (wt.expired(p)) {
-            report_timeout(p, r, c, E);
-            return;
+          if (pend == 0u) break;
+          if ((++spins & 63u) == 0u) {
+            const u64 now = globaltimer_ns();
+            if (deadline == 0) deadline = now + p.timeout_ns;
+            if (now > deadline || ld_relaxed_u32(p.abort_flag) != 0) {
+              report_timeout(p, r, c, E);
+              return;
+            }
           }
         }
 #pragma unroll
@@ -333,8 +374,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
         }
         unsigned y[4];
         round_words<DT, 4>(acc, y);
-        store_vec16<DT>(dst, v, p.count, u4(y));
-        if (p.chain) {
+        if (full || v + 1 < NV) st_v4(dst + (size_t)v * 16, u4(y));
+        else store_vec16<DT>(dst, v, p.count, u4(y));
+        if (CHAIN) {
           unsigned nx[4];
           chain_words_fast<DT, 4>(acc, y, nx, p.chain_scale);
           store_vec16<DT>(chain_next_buf(p, r, e), v, p.count, u4(nx));
@@ -342,6 +384,13 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
       }
     }
   }
+}
+
+template <int DT, int N, bool CHAIN>
+__global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_sentinel<DT, N, CHAIN>(p, epoch0);
+  finish_launch(p);
 }
 
 // ======================================================= LL128 two-shot
@@ -381,7 +430,7 @@ __device__ __forceinline__ void red_add_flag(void* a, unsigned one_bits) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
+__device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
   constexpr int EB = Fmt<DT>::kBytes;
   constexpr int V = 16 / EB;    // elements per lane
   constexpr int EL = 128 / EB;  // elements per line
@@ -411,7 +460,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
   bool failed = false;
 
   for (int e = 0; e < p.iters; ++e) {
-    const u64 E = p.epoch0 + (u64)e;
+    const u64 E = epoch0 + (u64)e;
     const int slot = (int)(E & 1);
     const char* src = rank_input<DT>(p, r, e);
     char* dst = rank_output<DT>(p, r, e);
@@ -561,6 +610,13 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
   }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_ll128<DT>(p, epoch0);
+  finish_launch(p);
+}
+
 // ==================================================== fixed-order paths
 // Deterministic direct-read variants: the reader loads every rank's input
 // itself, adds in rank order 0..N-1 in float32 and rounds once. Inputs of a
@@ -685,7 +741,7 @@ __device__ __forceinline__ void chain_range(const Params& p, int r, int e, size_
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
+__device__ __forceinline__ void body_fixed_oneshot(const Params& p, const u64 epoch0) {
   constexpr int PER16 = 16 / Fmt<DT>::kBytes;
   __shared__ int s_fail;
   const int r = rank_of_block(p);
@@ -695,7 +751,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
   const size_t v0 = min(NV, (size_t)c * per);
   const size_t v1 = min(NV, v0 + per);
   for (int e = 0; e < p.iters; ++e) {
-    const u64 E = p.epoch0 + (u64)e;
+    const u64 E = epoch0 + (u64)e;
     if (p.chain && e > 0 && !wait_flags(p, r, c, 0, E, r, E, &s_fail)) return;
     reduce_range<DT>(p, e, v0, v1, !p.chain || e == 0, r);
     if (p.chain) {
@@ -707,10 +763,17 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
   }
 }
 
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_fixed_oneshot<DT>(p, epoch0);
+  finish_launch(p);
+}
+
 // Two-shot: rank s owns vectors [s*ceil(NV/N), ...) of the message; CTA c
 // of every rank covers sub-range c of every segment.
 template <int DT>
-__global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
+__device__ __forceinline__ void body_fixed_twoshot(const Params& p, const u64 epoch0) {
   constexpr int PER16 = 16 / Fmt<DT>::kBytes;
   __shared__ int s_fail;
   const int N = p.nranks;
@@ -726,7 +789,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
     v1 = min(send, v0 + per);
   };
   for (int e = 0; e < p.iters; ++e) {
-    const u64 E = p.epoch0 + (u64)e;
+    const u64 E = epoch0 + (u64)e;
     // phase 1, owner of segment r: reduce sub-range c, write it to every rank
     if (p.chain && e > 0 && !wait_flags(p, r, c, 0, E, r, E, &s_fail)) return;
     size_t v0, v1;
@@ -744,6 +807,13 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
     }
     publish_flag(p, r, c, 0, E + 1);
   }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_fixed_twoshot<DT>(p, epoch0);
+  finish_launch(p);
 }
 
 // ============================================================ launchers
@@ -793,7 +863,7 @@ static cudaError_t launch_kernel(const void* k, const Params& p, int threads, cu
 template <int DT, int N>
 static const void* one_shot_kernel(int proto, bool chain) {
   if (proto == 1) return chain ? (const void*)k_ll<DT, N, true> : (const void*)k_ll<DT, N, false>;
-  return (const void*)k_sentinel<DT, N>;
+  return chain ? (const void*)k_sentinel<DT, N, true> : (const void*)k_sentinel<DT, N, false>;
 }
 template <int DT>
 static const void* one_shot_kernel_n(int proto, int n, bool chain) {
@@ -1033,7 +1103,8 @@ constexpr size_t kNoAllocHeader = 512;                           // abort word +
 constexpr size_t kNoAllocBytes = kNoAllocHeader + kMaxRanks * kNoAllocRankBytes;
 constexpr int kNoAllocMaxDevices = 64;
 
-// header: [0, 4) abort word, [256, 256 + sizeof(DevStatus)) status; then
+// header: [0, 4) abort word, [64, 68) CTAs finished, [128, 136) epoch,
+// [256, 256 + sizeof(DevStatus)) status; then
 // rank r's LL lines [slot][word] at kNoAllocHeader + r * kNoAllocRankBytes.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
@@ -1041,7 +1112,6 @@ struct NoAllocDevice {
   bool ready = false;
   char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sms = 0;
-  unsigned long long epoch = 1;
 };
 NoAllocDevice g_noalloc[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
@@ -1095,7 +1165,8 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
       return LLAR_ERR_CUDA;
     }
     if (word != 0) {
-      cudaMemsetAsync(d.scratch, 0, kNoAllocHeader, s);
+      cudaMemsetAsync(d.scratch, 0, 4, s);          // abort word
+      cudaMemsetAsync(d.scratch + 256, 0, 256, s);  // status
       return LLAR_ERR_TIMEOUT;
     }
   } else {
@@ -1111,7 +1182,8 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
   p.count = count;
   p.nranks = nranks;
   p.iters = 1;
-  p.epoch0 = d.epoch;
+  p.epoch_dev = reinterpret_cast<unsigned long long*>(d.scratch + 128);
+  p.done_count = reinterpret_cast<unsigned*>(d.scratch + 64);
   p.ll = d.scratch + kNoAllocHeader;
   p.ll_stride = kNoAllocRankBytes;
   p.ll_slot_words = kNoAllocWords;
@@ -1139,6 +1211,5 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
     cudaGetLastError();
     return err == cudaErrorCooperativeLaunchTooLarge ? LLAR_ERR_OCCUPANCY : LLAR_ERR_CUDA;
   }
-  d.epoch += 1;
   return LLAR_OK;
 }

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -47,10 +48,12 @@ struct Ctx {
   size_t flags_off = 0, abort_off = 0;
   llar::DevStatus* status_host = nullptr;
   llar::DevStatus* status_dev = nullptr;
-  unsigned long long epoch = 1;
   // host-API staging
   char* io = nullptr;
   size_t io_stride = 0;
+  // resident-CTA capacity per (protocol, chain, threads, clustered): the
+  // occupancy queries cost microseconds, so each is made once
+  std::map<long long, int> capacity;
 };
 
 std::mutex g_mu;
@@ -85,8 +88,11 @@ int select_protocol(int n, int dtype, size_t count) {
   }
   const size_t bytes = count * elem_bytes(dtype);
   (void)n;
+  // measured on a B300 with 8 ranks (persistent per-AllReduce time): LL is
+  // fastest up to 64 KiB per rank, direct-read one-shot from there to
+  // 256 KiB, direct-read two-shot beyond
   if (bytes <= (64u << 10)) return LLAR_PROTO_LL;
-  if (bytes <= (512u << 10)) return LLAR_PROTO_SENTINEL;
+  if (bytes <= (256u << 10)) return LLAR_PROTO_FIXED_ONESHOT;
   return LLAR_PROTO_FIXED_TWOSHOT;
 }
 
@@ -110,6 +116,13 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
     const size_t want = (per_rank + 2 * t - 1) / (2 * t);
     const int cap = chain ? one_per_sm : std::max(1, (c.sms * 4) / n);
     g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)cap);
+  } else if (proto == LLAR_PROTO_SENTINEL) {
+    // every vector costs N-1 pushes, polls and resets plus a fence per
+    // chunk: spread the chunk thinly over as many SMs as possible
+    t = 64;
+    const size_t want = (units + t - 1) / t;
+    g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)std::max(1, 2 * c.sms / n));
+    if (want > (size_t)g) t = (int)std::min<size_t>(llar::kMaxThreads, round_up((units + g - 1) / g, 32));
   } else {
     const size_t want = (units + t - 1) / t;
     if (want <= (size_t)one_per_sm) {
@@ -181,7 +194,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   p.chain_scale = chain_scale;
   p.in_stride = in_stride;
   p.out_stride = out_stride;
-  p.epoch0 = c.epoch;
+  p.epoch_dev = reinterpret_cast<unsigned long long*>(c.base + c.abort_off + 128);
+  p.done_count = reinterpret_cast<unsigned*>(c.base + c.abort_off + 64);
   p.ll = c.base + c.ll_off;
   p.ll_stride = c.ll_stride;
   p.ll_slot_words = c.ll_words;
@@ -212,10 +226,18 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   // measured 20-25% lower latency than spreading them over the GPU
   p.clustered = (coop && g_cluster) ? 1 : 0;
   if (coop) {
-    int cap = llar::max_resident_ctas(proto, c.dtype, c.n, T, p.clustered != 0);
+    auto capacity = [&](bool clustered) {
+      const long long key = ((long long)proto * 2 + chain) * 4096 * 2 + (long long)T * 2 + (clustered ? 1 : 0);
+      auto it = c.capacity.find(key);
+      if (it != c.capacity.end()) return it->second;
+      const int v = llar::max_resident_ctas(proto, c.dtype, c.n, T, clustered);
+      c.capacity[key] = v;
+      return v;
+    };
+    int cap = capacity(p.clustered != 0);
     if (cap <= 0 && p.clustered) {
       p.clustered = 0;
-      cap = llar::max_resident_ctas(proto, c.dtype, c.n, T, false);
+      cap = capacity(false);
     }
     if (cap <= 0) return LLAR_ERR_CUDA;
     if (c.n * G > cap) {
@@ -239,7 +261,6 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     cudaGetLastError();
     return cuda_status(err);
   }
-  c.epoch += (unsigned long long)iters;
   g_last_proto = proto;
   g_last_G = G;
   g_last_T = T;
@@ -255,7 +276,8 @@ int fill_staging(Ctx& c, cudaStream_t s) {
   ok(cudaMemsetAsync(c.base + c.l128_off, 0, c.l128_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.ag_off, 0, c.ag_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.flags_off, 0, (size_t)c.n * kFlagsGmax * 2 * 8, s));
-  ok(cudaMemsetAsync(c.base + c.abort_off, 0, kAlign, s));
+  // abort word only: the epoch counter at +128 keeps counting across resets
+  ok(cudaMemsetAsync(c.base + c.abort_off, 0, 4, s));
   ok(cudaStreamSynchronize(s));
   std::memset(c.status_host, 0, sizeof(llar::DevStatus));
   return cuda_status(err);
@@ -318,6 +340,13 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
     cudaGetLastError();
     if (c->base) cudaFree(c->base);
     if (c->status_host) cudaFreeHost(c->status_host);
+    delete c;
+    return LLAR_ERR_CUDA;
+  }
+  if (cudaMemset(c->base + c->abort_off, 0, kAlign) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(c->base);
+    cudaFreeHost(c->status_host);
     delete c;
     return LLAR_ERR_CUDA;
   }
@@ -547,7 +576,13 @@ int llar_select_protocol(int nranks, int dtype, size_t count) {
 
 unsigned long long llar_epoch(void) {
   std::lock_guard<std::mutex> lk(g_mu);
-  return g ? g->epoch : 0ull;
+  if (!g) return 0ull;
+  unsigned long long done = 0;  // epochs used so far, kept on the device
+  if (cudaMemcpy(&done, g->base + g->abort_off + 128, sizeof(done), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return 0ull;
+  }
+  return done + 1;
 }
 
 int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters) {
