@@ -40,23 +40,27 @@ def up_to_date():
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force=False, verbose=False):
-    """Compile every CUDA source into libllar.so (skipped when up to date)."""
-    if not force and up_to_date():
+def build(force=False, verbose=False, defines=(), out=None):
+    """Compile every CUDA source into libllar.so (skipped when up to date).
+
+    `defines` (e.g. ["LLAR_BULK_TILE=4096"]) and `out` build a variant
+    library elsewhere, for tuning sweeps; the default build is LIB."""
+    if out is None and not defines and not force and up_to_date():
         return LIB
     nvcc = nvcc_path()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    tmp = LIB + ".tmp"
+    target = out or LIB
+    tmp = target + ".tmp"
     cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
            "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
            "-cudart", "shared", "-Xlinker", "-rpath=" + cuda_lib,
-           "-o", tmp] + [os.path.join(CSRC, f) for f in SOURCES]
+           "-o", tmp] + ["-D" + d for d in defines] + [os.path.join(CSRC, f) for f in SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

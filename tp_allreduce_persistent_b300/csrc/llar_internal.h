@@ -39,6 +39,7 @@ struct Params {
   int nranks;
   int G;                      // CTAs per rank
   int clustered;              // launch in clusters of nranks blocks (one CTA per rank, same range)
+  int spread_smem;            // dynamic shared memory reserved only to keep one CTA per SM
   int iters;
   int chain;                  // 1: next input = RNE(chain_scale * output)
   float chain_scale;
@@ -73,11 +74,15 @@ cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_
 cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s);
+// TMA bulk-copy variant of the fixed two-shot (no chain), one CTA per SM
+cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, cudaStream_t s);
+size_t bulk_smem_bytes(int nranks);
+size_t bulk_tile_vectors();  // 16-byte vectors per rank tile of the bulk ring
 
 // Largest number of CTAs of the kernel for (proto, dtype, nranks) that can
 // be resident at once with `threads` threads each, in clusters of nranks
 // blocks if `clustered` (0 on error).
-int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered);
+int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered, int spread_smem);
 
 // Speed-of-light probes: per-SM pointer-chase latency (ns per dependent
 // L2 load) and per-pair ping-pong round trips (ns per store-observe-reply).

@@ -196,26 +196,35 @@ __device__ __forceinline__ void body_ll(const Params& p, const u64 epoch0) {
 #pragma unroll
   for (int q = 0; q < N; ++q) from[q] = p.ll + (size_t)q * p.ll_stride;
   const unsigned others = ((1u << N) - 1u) & ~(1u << r);
+  auto own_word = [&](const char* src, unsigned w) -> u64 {
+    return (full || w + 1 < W) ? *reinterpret_cast<const u64*>(src + (size_t)w * 8) : load_word8<DT>(src, w, p.count);
+  };
+  auto publish = [&](int e, unsigned w, u64 x) {
+    if (skip) return;
+    const u64 E = epoch0 + (u64)e;
+    st_relaxed_b128(mine + (size_t)(E & 1) * slot_stride + (size_t)w * kLLLine, x, E + flag_add);
+  };
 
+  // AllReduce 0's lines go out first; afterwards each word's line for
+  // AllReduce e+1 goes out as soon as that word of AllReduce e has been
+  // received from every peer (technique 3: receiving is the permission to
+  // send the next one), before the reduction of e is computed.
+  if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+  {
+    const char* src0 = rank_input<DT>(p, r, 0);
+    for (unsigned w = w0 + threadIdx.x; w < w1; w += blockDim.x) publish(0, w, own_word(src0, w));
+  }
   for (int e = 0; e < p.iters; ++e) {
     const u64 E = epoch0 + (u64)e;
     const size_t slot_off = (size_t)(E & 1) * slot_stride;
-    const char* src = CHAIN ? rank_input<DT>(p, r, e) : p.in[r] + (size_t)e * p.in_stride * EB;
+    const char* src = rank_input<DT>(p, r, e);
+    const char* src_next = (!CHAIN && e + 1 < p.iters) ? rank_input<DT>(p, r, e + 1) : nullptr;
     char* dst = rank_output<DT>(p, r, e);
-    if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
-
-    if (!skip) {
-      for (unsigned w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
-        const u64 x = (full || w + 1 < W) ? *reinterpret_cast<const u64*>(src + (size_t)w * 8)
-                                          : load_word8<DT>(src, w, p.count);
-        st_relaxed_b128(mine + slot_off + (size_t)w * kLLLine, x, E + flag_add);
-      }
-    }
+    if (e > 0 && injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
 
     for (unsigned w = w0 + threadIdx.x; w < w1; w += blockDim.x) {
       const size_t off = slot_off + (size_t)w * kLLLine;
-      const u64 own = (full || w + 1 < W) ? *reinterpret_cast<const u64*>(src + (size_t)w * 8)
-                                          : load_word8<DT>(src, w, p.count);
+      const u64 own = own_word(src, w);
       u64 d[N];
       unsigned pend = others;
       unsigned spins = 0;
@@ -241,6 +250,7 @@ __device__ __forceinline__ void body_ll(const Params& p, const u64 epoch0) {
           }
         }
       }
+      if (!CHAIN && src_next) publish(e + 1, w, own_word(src_next, w));
       // rank-order float32 sum, one rounding
       float acc[PER8];
 #pragma unroll
@@ -252,13 +262,15 @@ __device__ __forceinline__ void body_ll(const Params& p, const u64 epoch0) {
       unsigned y[2];
       round_words<DT, 2>(acc, y);
       const u64 yw = (u64)y[0] | ((u64)y[1] << 32);
-      if (full || w + 1 < W) *reinterpret_cast<u64*>(dst + (size_t)w * 8) = yw;
-      else store_word8<DT>(dst, w, p.count, yw);
-      if (CHAIN) {
+      if (CHAIN && e + 1 < p.iters) {
         unsigned nx[2];
         chain_words_fast<DT, 2>(acc, y, nx, p.chain_scale);
-        store_word8<DT>(chain_next_buf(p, r, e), w, p.count, (u64)nx[0] | ((u64)nx[1] << 32));
+        const u64 nw = (u64)nx[0] | ((u64)nx[1] << 32);
+        publish(e + 1, w, nw);  // the next input is known now: send it before storing
+        store_word8<DT>(chain_next_buf(p, r, e), w, p.count, nw);
       }
+      if (full || w + 1 < W) *reinterpret_cast<u64*>(dst + (size_t)w * 8) = yw;
+      else store_word8<DT>(dst, w, p.count, yw);
     }
   }
 }
@@ -816,6 +828,131 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
   finish_launch(p);
 }
 
+// Large two-shot without a chain: the owner's CTAs stream their sub-range
+// through shared memory with TMA bulk copies. Stage k of a kBulkStages-deep
+// ring holds one tile (kBulkTileBytes) of every rank's input, filled by one
+// thread with N cp.async.bulk copies that complete on the stage's mbarrier.
+// All threads wait for the stage, add the N tiles in rank order (float32,
+// one rounding) and store the result to every rank's output; after a CTA
+// barrier the same thread refills the stage with the tile kBulkStages
+// further on. Tiles of every iteration form one sequence, so the ring keeps
+// running across iterations. Measured at 8 x 64 MiB bf16: one stage of
+// 20 KiB tiles (160 KiB of shared memory, one CTA per SM) beats deeper
+// rings (3 x 8 KiB: 5.4 TB/s, 2 x 8 KiB: 5.8, 1 x 20 KiB: 5.9): with more
+// reads in flight the writes of the same kernel lose DRAM time.
+#ifndef LLAR_BULK_STAGES
+#define LLAR_BULK_STAGES 1
+#endif
+#ifndef LLAR_BULK_TILE
+#define LLAR_BULK_TILE 20480
+#endif
+#ifndef LLAR_BULK_CS
+#define LLAR_BULK_CS 0
+#endif
+constexpr int kBulkStages = LLAR_BULK_STAGES;
+constexpr int kBulkTileBytes = LLAR_BULK_TILE;
+
+template <int DT>
+__device__ __forceinline__ void body_fixed_twoshot_bulk(const Params& p, const u64 epoch0) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  constexpr unsigned TV = kBulkTileBytes / 16;  // vectors per tile
+  const int N = p.nranks;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t NV = (p.count + PER16 - 1) / PER16;
+  const size_t nfull = p.count / PER16;
+  const size_t segv = (NV + N - 1) / N;
+  const size_t per = (segv + p.G - 1) / p.G;
+  const size_t sbeg = min(NV, (size_t)r * segv);
+  const size_t send = min(NV, sbeg + segv);
+  const size_t v0 = min(send, sbeg + (size_t)c * per);
+  const size_t v1 = min(send, v0 + per);
+  const size_t v1f = min(v1, nfull);  // full vectors go through the ring
+  const size_t span = v1f > v0 ? v1f - v0 : 0;
+  const unsigned tiles = (unsigned)((span + TV - 1) / TV);
+  const unsigned long long total = (unsigned long long)tiles * p.iters;
+  const size_t stage_bytes = (size_t)N * kBulkTileBytes;
+  const unsigned base = smem_addr(smem);
+  const unsigned bars = base + (unsigned)(kBulkStages * stage_bytes);
+  (void)epoch0;
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kBulkStages; ++k) mbar_init(bars + 8 * k, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](unsigned long long g) {
+    const int e = (int)(g / tiles);
+    const unsigned t = (unsigned)(g % tiles);
+    const int k = (int)(g % kBulkStages);
+    const size_t vb = v0 + (size_t)t * TV;
+    const unsigned nv = (unsigned)min((size_t)TV, v1f - vb);
+    mbar_arrive_expect_tx(bars + 8 * k, nv * 16u * (unsigned)N);
+    for (int q = 0; q < N; ++q)
+      bulk_load(base + (unsigned)(k * stage_bytes + (size_t)q * kBulkTileBytes),
+                rank_input<DT>(p, q, e) + vb * 16, nv * 16u, bars + 8 * k);
+  };
+  if (threadIdx.x == 0)
+    for (unsigned long long g = 0; g < total && g < (unsigned long long)kBulkStages; ++g) issue(g);
+
+  bool failed = false;
+  for (unsigned long long g = 0; g < total; ++g) {
+    const int e = (int)(g / tiles);
+    const unsigned t = (unsigned)(g % tiles);
+    const int k = (int)(g % kBulkStages);
+    const unsigned parity = (unsigned)((g / kBulkStages) & 1u);
+    const size_t vb = v0 + (size_t)t * TV;
+    const unsigned nv = (unsigned)min((size_t)TV, v1f - vb);
+    if (!failed) {
+      unsigned spins = 0;
+      u64 deadline = 0;
+      while (!mbar_try_wait(bars + 8 * k, parity)) {
+        if ((++spins & 1023u) == 0u) {
+          const u64 now = globaltimer_ns();
+          if (deadline == 0) deadline = now + p.timeout_ns;
+          if (now > deadline) {
+            report_timeout(p, r, c, epoch0 + (u64)e);
+            failed = true;
+            break;
+          }
+        }
+      }
+    }
+    const unsigned sb = base + (unsigned)(k * stage_bytes);
+    for (unsigned v = threadIdx.x; v < nv; v += blockDim.x) {
+      float acc[PER16];
+      for (int q = 0; q < N; ++q) {
+        const uint4 x = ld_shared_v4(sb + (unsigned)q * kBulkTileBytes + v * 16u);
+        const unsigned w4[4] = {x.x, x.y, x.z, x.w};
+        acc_words<DT, 4>(acc, w4, q == 0);
+      }
+      unsigned y[4];
+      round_words<DT, 4>(acc, y);
+      const uint4 yv = u4(y);
+      if (LLAR_BULK_CS)
+        for (int q = 0; q < N; ++q) st_cs_v4(rank_output<DT>(p, q, e) + (vb + v) * 16, yv);
+      else
+        for (int q = 0; q < N; ++q) st_v4(rank_output<DT>(p, q, e) + (vb + v) * 16, yv);
+    }
+    __syncthreads();  // every thread is done with stage k
+    if (threadIdx.x == 0 && !failed && g + kBulkStages < total) issue(g + kBulkStages);
+  }
+  // the ragged last vector of the message, if it falls in my range
+  if (v0 <= nfull && nfull < v1 && nfull < NV && threadIdx.x == 0)
+    for (int e = 0; e < p.iters; ++e) {
+      const uint4 y = sum_ranks_vec<DT>(p, e, v1f, true);
+      for (int q = 0; q < N; ++q) store_vec16<DT>(rank_output<DT>(p, q, e), v1f, p.count, y);
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot_bulk(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_fixed_twoshot_bulk<DT>(p, epoch0);
+  finish_launch(p);
+}
+
 // ============================================================ launchers
 // Launch N x G blocks: cooperative when CTAs wait on each other (the
 // runtime refuses a grid that cannot be fully resident), in clusters of N
@@ -826,7 +963,7 @@ static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nranks * p.G);
   cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = p.spread_smem;
   cfg.stream = s;
   int na = 0;
   if (coop) {
@@ -846,6 +983,10 @@ static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream
   return cfg;
 }
 static cudaError_t launch_kernel(const void* k, const Params& p, int threads, cudaStream_t s, bool coop) {
+  if (p.spread_smem > 0) {
+    const cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.spread_smem);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchAttribute at[2];
   cudaLaunchConfig_t cfg = launch_config(p, threads, s, coop, at);
   void* args[] = {const_cast<Params*>(&p)};
@@ -903,6 +1044,22 @@ cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaSt
   LLAR_DISPATCH(k_fixed_twoshot, p.chain != 0)
 }
 
+size_t bulk_smem_bytes(int nranks) { return (size_t)kBulkStages * nranks * kBulkTileBytes + 8 * kBulkStages; }
+size_t bulk_tile_vectors() { return kBulkTileBytes / 16; }
+
+cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, cudaStream_t s) {
+  const void* k = dtype == 0 ? (const void*)k_fixed_twoshot_bulk<0>
+                  : dtype == 1 ? (const void*)k_fixed_twoshot_bulk<1> : (const void*)k_fixed_twoshot_bulk<2>;
+  const int smem = (int)bulk_smem_bytes(p.nranks);
+  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute at[2];
+  cudaLaunchConfig_t cfg = launch_config(p, threads, s, false, at);
+  cfg.dynamicSmemBytes = smem;
+  void* args[] = {const_cast<Params*>(&p)};
+  return cudaLaunchKernelExC(&cfg, k, args);
+}
+
 template <int DT>
 static const void* kernel_for(int proto) {
   switch (proto) {
@@ -913,7 +1070,7 @@ static const void* kernel_for(int proto) {
   }
 }
 
-int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered) {
+int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool clustered, int spread_smem) {
   const void* k = (proto == 1 || proto == 2) ? one_shot_kernel_for(proto, dtype, nranks, false)
                   : dtype == 0 ? kernel_for<0>(proto) : dtype == 1 ? kernel_for<1>(proto) : kernel_for<2>(proto);
   if (!k) return 0;
@@ -924,6 +1081,11 @@ int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool cluste
     p.nranks = nranks;
     p.G = 1;
     p.clustered = 1;
+    p.spread_smem = spread_smem;
+    if (spread_smem > 0 && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, spread_smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
     cudaLaunchAttribute at[2];
     cudaLaunchConfig_t cfg = launch_config(p, threads, 0, false, at);
     int clusters = 0;
@@ -934,7 +1096,11 @@ int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool cluste
     return clusters * nranks;
   }
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess) return 0;
+  if (spread_smem > 0 && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, spread_smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, spread_smem) != cudaSuccess) return 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return per_sm * sms;
@@ -1197,12 +1363,8 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
   G = G < 1 ? 1 : G;
   const int one_per_sm = d.sms / nranks > 0 ? d.sms / nranks : 1;
   G = G > one_per_sm ? one_per_sm : G;
-  p.clustered = 1;
-  int cap = max_resident_ctas(1, dtype, nranks, threads, true);
-  if (cap <= 0) {
-    p.clustered = 0;
-    cap = max_resident_ctas(1, dtype, nranks, threads, false);
-  }
+  p.clustered = 0;  // the LL kernel runs faster with its CTAs spread over the GPU
+  const int cap = max_resident_ctas(1, dtype, nranks, threads, false, 0);
   if (cap <= 0) return LLAR_ERR_CUDA;
   if (nranks * G > cap) G = cap / nranks > 0 ? cap / nranks : 1;
   p.G = G;

@@ -60,7 +60,8 @@ std::mutex g_mu;
 Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
-int g_cluster = 1, g_log = 0;
+int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0;
+constexpr size_t kBulkMinBytes = 1u << 20;  // per rank: TMA bulk path from 1 MiB
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
@@ -222,15 +223,22 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   choose_shape(c, proto, count, chain, &G, &T);
   const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
                     proto == LLAR_PROTO_LL128_ATOMIC || chain;
-  // ranks that exchange data run their CTA c in one cluster (one GPC):
-  // measured 20-25% lower latency than spreading them over the GPU
-  p.clustered = (coop && g_cluster) ? 1 : 0;
+  // Thread-block clusters put the N CTAs that serve one range on one GPC.
+  // Measured on B300 (8 ranks, bf16, CTAs per rank as chosen above): they
+  // help the sentinel protocol (64 KiB in 8 KiB chunks: 18.0 -> 15.1 us)
+  // and the chained fixed-order paths (two-shot, 128 KiB: 16.3 -> 14.9 us),
+  // and hurt LL (16 KiB: 0.79 -> 0.87 us) and LL128 (1 MiB: 21 -> 31 us).
+  // LLAR_CLUSTER: 0 never, 1 per protocol (default), 2 always.
+  const bool cluster_helps = proto == LLAR_PROTO_SENTINEL || proto == LLAR_PROTO_FIXED_ONESHOT ||
+                             proto == LLAR_PROTO_FIXED_TWOSHOT;
+  p.clustered = (coop && (g_cluster == 2 || (g_cluster == 1 && cluster_helps))) ? 1 : 0;
+  p.spread_smem = (coop && (proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL)) ? g_spread : 0;
   if (coop) {
     auto capacity = [&](bool clustered) {
       const long long key = ((long long)proto * 2 + chain) * 4096 * 2 + (long long)T * 2 + (clustered ? 1 : 0);
       auto it = c.capacity.find(key);
       if (it != c.capacity.end()) return it->second;
-      const int v = llar::max_resident_ctas(proto, c.dtype, c.n, T, clustered);
+      const int v = llar::max_resident_ctas(proto, c.dtype, c.n, T, clustered, p.spread_smem);
       c.capacity[key] = v;
       return v;
     };
@@ -255,7 +263,18 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     case LLAR_PROTO_SENTINEL: err = llar::launch_sentinel(c.dtype, p, T, stream); break;
     case LLAR_PROTO_LL128_ATOMIC: err = llar::launch_ll128(c.dtype, p, T, stream); break;
     case LLAR_PROTO_FIXED_ONESHOT: err = llar::launch_fixed_oneshot(c.dtype, p, T, stream); break;
-    default: err = llar::launch_fixed_twoshot(c.dtype, p, T, stream); break;
+    default:
+      if (!chain && g_bulk && bytes >= kBulkMinBytes && g_force_G == 0) {
+        // as many CTAs as the ring's shared memory lets each SM hold
+        const int per_sm = std::max(1, (int)((227u << 10) / llar::bulk_smem_bytes(c.n)));
+        p.G = std::max(1, per_sm * c.sms / c.n);
+        T = (int)std::min<size_t>(llar::kMaxThreads, std::max<size_t>(128, llar::bulk_tile_vectors()));
+        G = p.G;
+        err = llar::launch_fixed_twoshot_bulk(c.dtype, p, T, stream);
+      } else {
+        err = llar::launch_fixed_twoshot(c.dtype, p, T, stream);
+      }
+      break;
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -305,6 +324,8 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_force_T = (int)env_size("LLAR_THREADS", (size_t)g_force_T);
   g_cluster = (int)env_size("LLAR_CLUSTER", (size_t)g_cluster);
   g_log = (int)env_size("LLAR_LOG", (size_t)g_log);
+  g_bulk = (int)env_size("LLAR_BULK", (size_t)g_bulk);
+  g_spread = (int)env_size("LLAR_SPREAD_SMEM", (size_t)g_spread);
 
   cudaError_t err = cudaGetDevice(&c->dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);

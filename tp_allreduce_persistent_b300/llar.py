@@ -10,7 +10,8 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libllar.so")
+# LLAR_LIBRARY selects another build of the same sources (tuning variants)
+LIB_PATH = os.environ.get("LLAR_LIBRARY") or os.path.join(HERE, "libllar.so")
 
 DTYPES = {"fp32": 0, "fp16": 1, "bf16": 2}
 PROTOCOLS = {"auto": 0, "ll": 1, "sentinel": 2, "ll128": 3,
