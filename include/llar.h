@@ -111,10 +111,14 @@ int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
                          size_t out_stride_elems, float chain_scale, void* stream);
 
 /* One AllReduce on HOST buffers: in_host and out_host are [N][count]
- * contiguous arrays in host memory (pinned memory makes the copies
- * asynchronous). Copies in, runs, copies out, all on `stream`, through
- * device buffers the library allocates on first use; returns once the
- * work is queued (synchronise the stream before reading out_host). */
+ * contiguous arrays in host memory. If both are page-locked and
+ * device-addressable (cudaHostAlloc / cudaHostRegister memory under
+ * unified addressing) and count * element size is a multiple of 16, the
+ * kernel reads the inputs and writes the outputs across the bus directly
+ * (one launch, no staging copies). Otherwise the call copies in, runs and
+ * copies out on `stream` through device buffers the library allocates on
+ * first use. Returns once the work is queued (synchronise the stream
+ * before reading out_host). */
 int llar_allreduce_host(const void* in_host, void* out_host, size_t count,
                         int protocol, void* stream);
 

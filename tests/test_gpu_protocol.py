@@ -190,6 +190,20 @@ def test_host_buffer_entry_point():
             assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
 
 
+def test_host_buffer_entry_point_pageable_and_ragged():
+    # pageable host memory (and a row size that is not a multiple of 16
+    # bytes) takes the staged-copy path
+    n, dtype = 4, "fp16"
+    with context(n, dtype, 1 << 20):
+        for count in (8192, 8191):
+            x = inputs.normal(n, count, dtype, seed=10 + count)
+            out = torch.empty_like(x)
+            for proto in ("ll", "fixed_oneshot"):
+                llar.llar_allreduce_host(x, out, count, proto)
+                torch.cuda.synchronize()
+                assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
+
+
 def test_sol_probe_is_consistent():
     with context(2, "fp32", 1 << 12):
         l2, wr, sol = llar.llar_sol_probe()

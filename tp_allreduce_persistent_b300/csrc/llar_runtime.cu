@@ -416,6 +416,24 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
   if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
   if (count == 0) return LLAR_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Pinned host buffers that the device can address (page-locked memory
+  // under unified addressing): the kernel reads the inputs and writes the
+  // outputs across the bus itself, one launch and no staging copies.
+  if (bytes % 16 == 0) {
+    cudaPointerAttributes ai, ao;
+    if (cudaPointerGetAttributes(&ai, in_host) == cudaSuccess && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
+        ai.type == cudaMemoryTypeHost && ao.type == cudaMemoryTypeHost && ai.devicePointer && ao.devicePointer &&
+        ((((uintptr_t)ai.devicePointer) | ((uintptr_t)ao.devicePointer)) & 15u) == 0) {
+      const void* ins[llar::kMaxRanks];
+      void* outs[llar::kMaxRanks];
+      for (int r = 0; r < c.n; ++r) {
+        ins[r] = static_cast<const char*>(ai.devicePointer) + r * bytes;
+        outs[r] = static_cast<char*>(ao.devicePointer) + r * bytes;
+      }
+      return run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
+    }
+    cudaGetLastError();  // pageable memory: not an error, take the copy path
+  }
   if (!c.io) {
     c.io_stride = round_up(c.max_bytes, kAlign);
     if (cudaMalloc(&c.io, 2 * c.io_stride * c.n) != cudaSuccess) {

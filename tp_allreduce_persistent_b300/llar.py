@@ -91,16 +91,24 @@ def _ptr(x):
 
 
 def _ptr_array(xs):
-    arr = (ctypes.c_void_p * len(xs))()
-    for i, x in enumerate(xs):
-        arr[i] = _ptr(x)
-    return arr
+    return (ctypes.c_void_p * len(xs))(*[x.data_ptr() if hasattr(x, "data_ptr") else int(x) for x in xs])
+
+
+_raw_stream = None
 
 
 def _stream(stream):
+    """cudaStream_t of `stream`; None means torch's current stream."""
+    global _raw_stream
     if stream is None:
         import torch
-        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+        if not torch.cuda.is_available():
+            return 0
+        if _raw_stream is None:
+            getter = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            _raw_stream = (lambda: getter(torch.cuda.current_device())) if getter else \
+                (lambda: torch.cuda.current_stream().cuda_stream)
+        return _raw_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
