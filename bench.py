@@ -56,6 +56,7 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
     ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth"],
                     help="run one leg only (small profiling cases)")
     ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
@@ -281,6 +282,53 @@ def e2e_leg(args, llar, torch, stream, x, pg, local):
     return e0.elapsed_time(e1) * 1e3 / calls
 
 
+def configs_leg(llar, torch, dev, stream):
+    """Per-AllReduce time of each workload configuration (persistent launches)."""
+    def timed(n, dtype, count, proto, iters, chain=0.0, chunk=None, max_bytes=None):
+        from tp_allreduce_persistent_b300 import inputs
+        llar.llar_init(n, dtype, max_bytes or max(count * inputs.ELEM_BYTES[dtype], 4096))
+        try:
+            if chunk:
+                llar.llar_set_sentinel_chunk(chunk)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(7)
+            td = inputs.TORCH_DTYPE[dtype]
+            ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(td) for _ in range(n)]
+            outs = [torch.empty_like(t) for t in ins]
+            llar.llar_allreduce_iters(ins, outs, count, proto, min(iters, 20), 0, 0, chain)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            llar.llar_allreduce_iters(ins, outs, count, proto, iters, 0, 0, chain)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if llar.llar_get_status()[0] != llar.OK:
+                raise RuntimeError("device status not ok")
+            return round(a.elapsed_time(b) * 1e3 / iters, 3)
+        finally:
+            llar.llar_destroy()
+
+    out = {
+        "C1_2ranks_128B_fp32_us": {p: timed(2, "fp32", 32, p, 1000) for p in ("ll", "fixed_oneshot")},
+        "C2_4ranks_16KiB_bf16_us": {p: timed(4, "bf16", 8192, p, 10000, chunk=16384) for p in ("ll", "sentinel")},
+        "C3_ll128_8ranks_bf16_us": {f"{kb}KiB": timed(8, "bf16", kb * 512, "ll128", 200 if kb > 64 else 1000)
+                                    for kb in (4, 16, 64, 256, 1024)},
+        "C4_sentinel_8ranks_64KiB_fp16_8KiB_chunks_us": timed(8, "fp16", 32768, "sentinel", 1000, chunk=8192),
+        "C5_chain_160_layers_128KiB_bf16_us": {
+            f"N{n}": {p: timed(n, "bf16", 65536, p, 160, chain=0.5, chunk=16384)
+                      for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")}
+            for n in (4, 8)},
+    }
+    sweep = {}
+    for mib in (1, 4, 16, 64, 256):
+        count = (mib << 20) // 2
+        iters = 3 if mib >= 64 else 10
+        us = timed(8, "bf16", count, "fixed_twoshot", iters, max_bytes=mib << 20)
+        sweep[f"{mib}MiB"] = {"us": us, "GB/s": round(2 * 8 * count * 2 / (us * 1e-6) / 1e9, 1)}
+    out["C5_sweep_8ranks_bf16_fixed_twoshot"] = sweep
+    return out
+
+
 def run_ours(args, world, rank, local, pg):
     import torch
     from tp_allreduce_persistent_b300 import inputs, llar
@@ -306,6 +354,9 @@ def run_ours(args, world, rank, local, pg):
     if lat is not None and args.leg == "all":
         e2e_us = e2e_leg(args, llar, torch, stream, lat["x"], pg, local)
     llar.llar_destroy()
+    per_config = None
+    if args.leg == "all" and not args.no_configs:
+        per_config = configs_leg(llar, torch, dev, stream)
 
     res = {"metric": METRIC, "unit": "us", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
@@ -359,6 +410,8 @@ def run_ours(args, world, rank, local, pg):
                       "h2d_bytes_per_step": NRANKS * COUNT * 2, "d2h_bytes_per_step": NRANKS * COUNT * 2,
                       "api": "llar_allreduce_host: pinned host [8][8192] bf16 in, out; one AllReduce per call"}
     res["config"] = config
+    if per_config is not None:
+        res["per_config"] = per_config
     return res
 
 
