@@ -319,6 +319,46 @@ def configs_leg(llar, torch, dev, stream):
                       for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")}
             for n in (4, 8)},
     }
+    # single calls, one launch each, replayed from a CUDA graph of 200 calls
+    # (GPU time per call including launch gaps, without host overhead)
+    def graph_call_us(kind, proto, n=8, count=8192, dtype="bf16"):
+        from tp_allreduce_persistent_b300 import inputs
+        llar.llar_init(n, dtype, count * inputs.ELEM_BYTES[dtype])
+        try:
+            td = inputs.TORCH_DTYPE[dtype]
+            seg = -(-count // n)
+            full_in = [torch.randn(count, device=dev).to(td) for _ in range(n)]
+            seg_in = [torch.randn(seg, device=dev).to(td) for _ in range(n)]
+            full_out = [torch.empty(count, dtype=td, device=dev) for _ in range(n)]
+            seg_out = [torch.empty(seg, dtype=td, device=dev) for _ in range(n)]
+            call = {"allreduce": lambda: llar.llar_allreduce(full_in, full_out, count, proto),
+                    "reduce_scatter": lambda: llar.llar_reduce_scatter(full_in, seg_out, count, proto),
+                    "all_gather": lambda: llar.llar_all_gather(seg_in, full_out, count, proto)}[kind]
+            call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(200):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(5):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if llar.llar_get_status()[0] != llar.OK:
+                raise RuntimeError("device status not ok")
+            return round(a.elapsed_time(b) * 1e3 / 1000, 3)
+        finally:
+            llar.llar_destroy()
+
+    out["single_call_graph_8ranks_16KiB_bf16_us"] = {
+        "allreduce": {p: graph_call_us("allreduce", p) for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")},
+        "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "fixed_oneshot")},
+        "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "fixed_oneshot")},
+    }
     sweep = {}
     for mib in (1, 4, 16, 64, 256):
         count = (mib << 20) // 2

@@ -110,6 +110,25 @@ int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
                          int protocol, int iters, size_t in_stride_elems,
                          size_t out_stride_elems, float chain_scale, void* stream);
 
+/* ReduceScatter, the first half of the two-shot AllReduce ("zcube network
+ * architecture for LLM inference", collectives table, Reduce-Scatter row:
+ * after it each rank keeps one reduced segment). Segment s of the
+ * count-element vector is [s*S, min(count, (s+1)*S)), S = ceil(count/N).
+ * in[r]: count elements; out[r]: the S (or fewer) elements of segment r,
+ * = sum over q of in[q][segment r], added in rank order in float32 and
+ * rounded once. protocol: LLAR_PROTO_LL (flag-in-data lines),
+ * LLAR_PROTO_FIXED_ONESHOT (direct reads) or LLAR_PROTO_AUTO; others give
+ * LLAR_ERR_UNSUPPORTED. One collective per launch. */
+int llar_reduce_scatter(const void* const* in, void* const* out, size_t count,
+                        int protocol, void* stream);
+
+/* AllGather, the second half of the two-shot AllReduce (same table,
+ * All-Gather row: each rank collects every rank's segment). in[r]: segment
+ * r of a count-element vector (segments as for llar_reduce_scatter);
+ * out[r]: all count elements, segment q at offset q*S. Same protocols. */
+int llar_all_gather(const void* const* in, void* const* out, size_t count,
+                    int protocol, void* stream);
+
 /* One AllReduce on HOST buffers: in_host and out_host are [N][count]
  * contiguous arrays in host memory. If both are page-locked and
  * device-addressable (cudaHostAlloc / cudaHostRegister memory under

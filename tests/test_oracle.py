@@ -151,6 +151,22 @@ def test_shard_bounds_partition(n, count):
     assert seen == list(range(count))
 
 
+@pytest.mark.parametrize("n,count", [(3, 10), (8, 8195), (4, 2)])
+def test_reduce_scatter_and_all_gather_closed_forms(n, count):
+    # rank-id inputs: every element of every segment sums to n(n-1)/2
+    x = inputs.bits_of(inputs.rank_ids(n, count, "fp32"))
+    segs = orc.reduce_scatter(x, "fp32")
+    assert [len(sg) for sg in segs] == [hi - lo for lo, hi in (orc.shard_bounds(count, n, s) for s in range(n))]
+    assert all(np.all(fp.decode(sg, "fp32") == n * (n - 1) / 2) for sg in segs)
+    # gathering segments filled with their own rank id puts value s at
+    # exactly the elements of segment s, on every rank
+    own = [fp.encode_rne(np.full(len(sg), s, np.float32), "fp32") for s, sg in enumerate(segs)]
+    out = fp.decode(orc.all_gather(own, count), "fp32")
+    per = -(-count // n)
+    want = np.array([i // per for i in range(count)], np.float32)
+    assert all(np.array_equal(out[q], want) for q in range(n))
+
+
 # ---------------------------------------------------------------- chains
 @pytest.mark.parametrize("dtype", fp.DTYPES)
 @pytest.mark.parametrize("n", [4, 8])

@@ -74,6 +74,10 @@ cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_
 cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s);
+// ReduceScatter / AllGather: which = 0 RS over LL, 1 AG over LL, 2 RS fixed,
+// 3 AG fixed (one collective per launch)
+cudaError_t launch_segment(int which, int dtype, const Params& p, int threads, cudaStream_t s);
+int max_resident_segment_ctas(int which, int dtype, int nranks, int threads);
 // TMA bulk-copy variant of the fixed two-shot (no chain), one CTA per SM
 cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, cudaStream_t s);
 size_t bulk_smem_bytes(int nranks);

@@ -953,6 +953,223 @@ __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot_bulk(const Params
   finish_launch(p);
 }
 
+// ============================================ ReduceScatter / AllGather
+// The two halves of the two-shot AllReduce as collectives of their own
+// ("zcube network architecture for LLM inference", collectives table, rows
+// Reduce-Scatter and All-Gather; "Every Microsecond Matters", technique 4).
+// Segment s of a count-element vector is [s*S, min(count, (s+1)*S)) with
+// S = ceil(count/N). One collective per launch: the launch boundary orders
+// every reuse of staging, so no credits are needed inside.
+__device__ __forceinline__ void segment_of(size_t count, int N, int s, size_t& lo, size_t& hi) {
+  const size_t per = (count + N - 1) / N;
+  lo = min(count, (size_t)s * per);
+  hi = min(count, lo + per);
+}
+
+// ReduceScatter over LL lines: every rank publishes all its words once;
+// owner r polls the words of segment r from every peer, adds in rank order
+// and stores segment r to out[r].
+template <int DT, int N>
+__device__ __forceinline__ void body_rs_ll(const Params& p, const u64 E) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int PER8 = 8 / EB;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t W = (count + PER8 - 1) / PER8;
+  char* const mine = p.ll + (size_t)r * p.ll_stride + (size_t)(E & 1) * p.ll_slot_words * kLLLine;
+  const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  const u64 flag = (p.inject_rank == r && p.inject_mode == LLAR_INJECT_POISON_) ? E + 2 : E;
+  if (p.inject_rank == r && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+  const char* src = p.in[r];
+  {
+    const size_t per = (W + p.G - 1) / p.G;
+    const size_t a = min(W, (size_t)c * per), b = min(W, a + per);
+    if (!skip)
+      for (size_t w = a + threadIdx.x; w < b; w += blockDim.x)
+        st_relaxed_b128(mine + w * kLLLine, load_word8<DT>(src, w, count), flag);
+  }
+  size_t lo, hi;
+  segment_of(count, N, r, lo, hi);
+  if (lo >= hi) return;
+  const size_t wa = lo / PER8, wb = (hi + PER8 - 1) / PER8;
+  const size_t per = (wb - wa + p.G - 1) / p.G;
+  const size_t a = min(wb, wa + (size_t)c * per), b = min(wb, a + per);
+  char* dst = p.out[r];
+  for (size_t w = a + threadIdx.x; w < b; w += blockDim.x) {
+    const size_t off = (size_t)(E & 1) * p.ll_slot_words * kLLLine + w * kLLLine;
+    u64 d[N];
+    unsigned pend = ((1u << N) - 1u) & ~(1u << r);
+    unsigned spins = 0;
+    u64 deadline = 0;
+    while (pend) {
+      u64 l[N], h[N];
+#pragma unroll
+      for (int q = 0; q < N; ++q)
+        if ((pend >> q) & 1u) ld_relaxed_b128(p.ll + (size_t)q * p.ll_stride + off, l[q], h[q]);
+#pragma unroll
+      for (int q = 0; q < N; ++q)
+        if (((pend >> q) & 1u) && h[q] == E) {
+          d[q] = l[q];
+          pend &= ~(1u << q);
+        }
+      if (pend && (++spins & 63u) == 0u) {
+        const u64 now = globaltimer_ns();
+        if (deadline == 0) deadline = now + p.timeout_ns;
+        if (now > deadline || ld_relaxed_u32(p.abort_flag) != 0) {
+          report_timeout(p, r, c, E);
+          return;
+        }
+      }
+    }
+    const u64 own = load_word8<DT>(src, w, count);
+    float acc[PER8];
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      const u64 v = (q == r) ? own : d[q];
+      const unsigned w2[2] = {(unsigned)v, (unsigned)(v >> 32)};
+      acc_words<DT, 2>(acc, w2, q == 0);
+    }
+    unsigned y[2];
+    round_words<DT, 2>(acc, y);
+#pragma unroll
+    for (int k = 0; k < PER8; ++k) {
+      const size_t g = w * PER8 + k;
+      if (g >= lo && g < hi) Fmt<DT>::store(dst, g - lo, word_elem<DT>(y[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+    }
+  }
+}
+
+// AllGather over LL lines: rank r publishes the words of its segment
+// (in[r] holds that segment only); every rank polls every peer's words and
+// places them at the segment's offset in its output.
+template <int DT, int N>
+__device__ __forceinline__ void body_ag_ll(const Params& p, const u64 E) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int PER8 = 8 / EB;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t S = (count + N - 1) / N;
+  const size_t WS = (S + PER8 - 1) / PER8;  // words of the longest segment
+  const size_t slot_off = (size_t)(E & 1) * p.ll_slot_words * kLLLine;
+  const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  const u64 flag = (p.inject_rank == r && p.inject_mode == LLAR_INJECT_POISON_) ? E + 2 : E;
+  if (p.inject_rank == r && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+  size_t lo, hi;
+  segment_of(count, N, r, lo, hi);
+  const size_t my_len = hi - lo;
+  const size_t my_words = (my_len + PER8 - 1) / PER8;
+  {
+    const size_t per = (my_words + p.G - 1) / p.G;
+    const size_t a = min(my_words, (size_t)c * per), b = min(my_words, a + per);
+    char* mine = p.ll + (size_t)r * p.ll_stride + slot_off;
+    if (!skip)
+      for (size_t w = a + threadIdx.x; w < b; w += blockDim.x)
+        st_relaxed_b128(mine + w * kLLLine, load_word8<DT>(p.in[r], w, my_len), flag);
+  }
+  // items: (segment q, word w) for all q, split over my CTAs
+  const size_t items = (size_t)N * WS;
+  const size_t per = (items + p.G - 1) / p.G;
+  const size_t a = min(items, (size_t)c * per), b = min(items, a + per);
+  char* dst = p.out[r];
+  for (size_t i = a + threadIdx.x; i < b; i += blockDim.x) {
+    const int q = (int)(i / WS);
+    const size_t w = i - (size_t)q * WS;
+    size_t qlo, qhi;
+    segment_of(count, N, q, qlo, qhi);
+    if (w * PER8 >= qhi - qlo) continue;
+    u64 v;
+    if (q == r) {
+      v = load_word8<DT>(p.in[r], w, my_len);
+    } else {
+      const char* line = p.ll + (size_t)q * p.ll_stride + slot_off + w * kLLLine;
+      unsigned spins = 0;
+      u64 deadline = 0;
+      while (true) {
+        u64 hv;
+        ld_relaxed_b128(line, v, hv);
+        if (hv == E) break;
+        if ((++spins & 63u) == 0u) {
+          const u64 now = globaltimer_ns();
+          if (deadline == 0) deadline = now + p.timeout_ns;
+          if (now > deadline || ld_relaxed_u32(p.abort_flag) != 0) {
+            report_timeout(p, r, c, E);
+            return;
+          }
+        }
+      }
+    }
+    const unsigned y[2] = {(unsigned)v, (unsigned)(v >> 32)};
+#pragma unroll
+    for (int k = 0; k < PER8; ++k) {
+      const size_t g = qlo + w * PER8 + k;
+      if (g < qhi) Fmt<DT>::store(dst, g, word_elem<DT>(y[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+    }
+  }
+}
+
+// Fixed-order ReduceScatter by direct reads: owner r reads segment r of
+// every rank's input, adds in rank order, stores to out[r].
+template <int DT>
+__device__ __forceinline__ void body_rs_fixed(const Params& p, const u64 E) {
+  (void)E;
+  const int N = p.nranks;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  size_t lo, hi;
+  segment_of(p.count, N, r, lo, hi);
+  const size_t stride = (size_t)p.G * blockDim.x;
+  char* dst = p.out[r];
+  for (size_t g = lo + (size_t)c * blockDim.x + threadIdx.x; g < hi; g += stride) {
+    float acc = Fmt<DT>::to_f(Fmt<DT>::load(p.in[0], g));
+    for (int q = 1; q < N; ++q) acc = __fadd_rn(acc, Fmt<DT>::to_f(Fmt<DT>::load(p.in[q], g)));
+    Fmt<DT>::store(dst, g - lo, Fmt<DT>::from_f(acc));
+  }
+}
+
+// Fixed AllGather by direct reads: rank r copies every segment into out[r].
+template <int DT>
+__device__ __forceinline__ void body_ag_fixed(const Params& p, const u64 E) {
+  (void)E;
+  const int N = p.nranks;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t stride = (size_t)p.G * blockDim.x;
+  char* dst = p.out[r];
+  for (int q = 0; q < N; ++q) {
+    size_t lo, hi;
+    segment_of(p.count, N, q, lo, hi);
+    for (size_t g = lo + (size_t)c * blockDim.x + threadIdx.x; g < hi; g += stride)
+      Fmt<DT>::store(dst, g, Fmt<DT>::load(p.in[q], g - lo));
+  }
+}
+
+template <int DT, int N>
+__global__ void __launch_bounds__(kMaxThreads) k_rs_ll(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_rs_ll<DT, N>(p, epoch0);
+  finish_launch(p);
+}
+template <int DT, int N>
+__global__ void __launch_bounds__(kMaxThreads) k_ag_ll(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_ag_ll<DT, N>(p, epoch0);
+  finish_launch(p);
+}
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_rs_fixed(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_rs_fixed<DT>(p, epoch0);
+  finish_launch(p);
+}
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_ag_fixed(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_ag_fixed<DT>(p, epoch0);
+  finish_launch(p);
+}
+
 // ============================================================ launchers
 // Launch N x G blocks: cooperative when CTAs wait on each other (the
 // runtime refuses a grid that cannot be fully resident), in clusters of N
@@ -1028,6 +1245,37 @@ static cudaError_t launch_one_shot(int proto, int dtype, const Params& p, int th
   if (!k) return cudaErrorInvalidValue;
   return launch_kernel(k, p, threads, s, true);
 }
+template <int DT>
+static const void* segment_kernel(int which, int n) {
+  // which: 0 = ReduceScatter LL, 1 = AllGather LL, 2 = ReduceScatter fixed, 3 = AllGather fixed
+  if (which == 2) return (const void*)k_rs_fixed<DT>;
+  if (which == 3) return (const void*)k_ag_fixed<DT>;
+  switch (n) {
+#define LLAR_SEG_CASE(NN) \
+    case NN: return which == 0 ? (const void*)k_rs_ll<DT, NN> : (const void*)k_ag_ll<DT, NN>;
+    LLAR_SEG_CASE(2) LLAR_SEG_CASE(3) LLAR_SEG_CASE(4) LLAR_SEG_CASE(5)
+    LLAR_SEG_CASE(6) LLAR_SEG_CASE(7) LLAR_SEG_CASE(8)
+#undef LLAR_SEG_CASE
+    default: return nullptr;
+  }
+}
+const void* segment_kernel_for(int which, int dtype, int n) {
+  return dtype == 0 ? segment_kernel<0>(which, n) : dtype == 1 ? segment_kernel<1>(which, n) : segment_kernel<2>(which, n);
+}
+cudaError_t launch_segment(int which, int dtype, const Params& p, int threads, cudaStream_t s) {
+  const void* k = segment_kernel_for(which, dtype, p.nranks);
+  if (!k) return cudaErrorInvalidValue;
+  return launch_kernel(k, p, threads, s, which < 2);
+}
+int max_resident_segment_ctas(int which, int dtype, int nranks, int threads) {
+  const void* k = segment_kernel_for(which, dtype, nranks);
+  int per_sm = 0, dev = 0, sms = 0;
+  if (!k || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return per_sm * sms;
+}
+
 cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s) {
   return launch_one_shot(1, dtype, p, threads, s);
 }

@@ -141,23 +141,123 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
   *T = t;
 }
 
-int check_ptrs(const void* const* in, void* const* out, int n, size_t in_span, size_t out_span) {
+// Pointers non-null and 16-byte aligned; no output overlaps an input or
+// another output. Spans are per rank, in bytes.
+int check_ptrs_spans(const void* const* in, void* const* out, int n, const size_t* in_span,
+                     const size_t* out_span) {
   if (!in || !out) return LLAR_ERR_INVALID;
   for (int r = 0; r < n; ++r) {
     if (!in[r] || !out[r]) return LLAR_ERR_INVALID;
     if (((uintptr_t)in[r] | (uintptr_t)out[r]) & 15u) return LLAR_ERR_INVALID;
   }
   for (int r = 0; r < n; ++r) {
-    const uintptr_t o0 = (uintptr_t)out[r], o1 = o0 + out_span;
+    const uintptr_t o0 = (uintptr_t)out[r], o1 = o0 + out_span[r];
     for (int q = 0; q < n; ++q) {
-      const uintptr_t i0 = (uintptr_t)in[q], i1 = i0 + in_span;
+      const uintptr_t i0 = (uintptr_t)in[q], i1 = i0 + in_span[q];
       if (o0 < i1 && i0 < o1) return LLAR_ERR_INVALID;  // output overlaps an input
       if (q != r) {
-        const uintptr_t p0 = (uintptr_t)out[q], p1 = p0 + out_span;
+        const uintptr_t p0 = (uintptr_t)out[q], p1 = p0 + out_span[q];
         if (o0 < p1 && p0 < o1) return LLAR_ERR_INVALID;  // two outputs overlap
       }
     }
   }
+  return LLAR_OK;
+}
+int check_ptrs(const void* const* in, void* const* out, int n, size_t in_span, size_t out_span) {
+  size_t is[llar::kMaxRanks], os[llar::kMaxRanks];
+  for (int r = 0; r < n; ++r) {
+    is[r] = in_span;
+    os[r] = out_span;
+  }
+  return check_ptrs_spans(in, out, n, is, os);
+}
+
+// Pointers, sizes, staging bases, status and injection settings shared by
+// every launch of the context.
+void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, size_t count) {
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < c.n; ++r) {
+    p.in[r] = static_cast<const char*>(in[r]);
+    p.out[r] = static_cast<char*>(out[r]);
+  }
+  p.count = count;
+  p.nranks = c.n;
+  p.iters = 1;
+  p.epoch_dev = reinterpret_cast<unsigned long long*>(c.base + c.abort_off + 128);
+  p.done_count = reinterpret_cast<unsigned*>(c.base + c.abort_off + 64);
+  p.ll = c.base + c.ll_off;
+  p.ll_stride = c.ll_stride;
+  p.ll_slot_words = c.ll_words;
+  p.sen = c.base + c.sen_off;
+  p.sen_stride = c.sen_stride;
+  p.sen_chunk_vecs = (int)(c.chunk_bytes / 16);
+  p.l128 = c.base + c.l128_off;
+  p.l128_stride = c.l128_stride;
+  p.l128ag = c.base + c.ag_off;
+  p.l128ag_stride = c.ag_stride;
+  p.l128_lines = c.l128_lines;
+  p.chainbuf = c.base + c.chain_off;
+  p.chain_stride = c.chain_stride;
+  p.chain_slot_bytes = c.chain_slot;
+  p.flags = reinterpret_cast<unsigned long long*>(c.base + c.flags_off);
+  p.flags_gmax = kFlagsGmax;
+  p.timeout_ns = g_timeout_ns;
+  p.inject_rank = g_inject_rank;
+  p.inject_mode = g_inject_mode;
+  p.abort_flag = reinterpret_cast<unsigned*>(c.base + c.abort_off);
+  p.status = c.status_dev;
+}
+
+// ReduceScatter (rs) or AllGather over segments of a count-element vector.
+int run_segment(bool rs, const void* const* in, void* const* out, size_t count, int proto, cudaStream_t stream) {
+  if (!g) return LLAR_ERR_NOT_INIT;
+  Ctx& c = *g;
+  const size_t e = c.esize;
+  const size_t bytes = count * e;
+  const size_t seg_bytes = (count + c.n - 1) / c.n * e;
+  if (proto == LLAR_PROTO_AUTO) proto = bytes <= (64u << 10) ? LLAR_PROTO_LL : LLAR_PROTO_FIXED_ONESHOT;
+  if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_FIXED_ONESHOT) return LLAR_ERR_UNSUPPORTED;
+  if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
+  if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
+  size_t full[llar::kMaxRanks], seg[llar::kMaxRanks];
+  for (int r = 0; r < c.n; ++r) {
+    const size_t per = (count + c.n - 1) / c.n;
+    const size_t lo = std::min(count, (size_t)r * per), hi = std::min(count, lo + per);
+    full[r] = bytes;
+    seg[r] = (hi - lo) * e;
+  }
+  const int st = check_ptrs_spans(in, out, c.n, rs ? full : seg, rs ? seg : full);
+  if (st != LLAR_OK) return st;
+  if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
+  if (count == 0) return LLAR_OK;
+  Params p;
+  fill_params(c, p, in, out, count);
+  const int which = rs ? (proto == LLAR_PROTO_LL ? 0 : 2) : (proto == LLAR_PROTO_LL ? 1 : 3);
+  int T = proto == LLAR_PROTO_LL ? 128 : 256;
+  size_t units;
+  if (proto == LLAR_PROTO_LL) {
+    const size_t words = (bytes + 7) / 8, seg_words = (seg_bytes + 7) / 8;
+    units = rs ? std::max(words, seg_words) : seg_words * c.n;
+  } else {
+    units = rs ? seg_bytes / e : count;
+  }
+  int G = (int)std::max<size_t>(1, (units + T - 1) / T);
+  const int cap = proto == LLAR_PROTO_LL ? llar::max_resident_segment_ctas(which, c.dtype, c.n, T)
+                                         : 4 * c.sms;
+  if (cap <= 0) return LLAR_ERR_CUDA;
+  G = std::min(G, std::max(1, cap / c.n));
+  if (g_force_G > 0) G = g_force_G;
+  if (g_force_T > 0) T = g_force_T;
+  p.G = G;
+  const cudaError_t err = llar::launch_segment(which, c.dtype, p, T, stream);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(err);
+  }
+  g_last_proto = proto;
+  g_last_G = G;
+  g_last_T = T;
+  g_last_iters = 1;
   return LLAR_OK;
 }
 
@@ -183,41 +283,12 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   if (count == 0) return LLAR_OK;
 
   Params p;
-  std::memset(&p, 0, sizeof(p));
-  for (int r = 0; r < c.n; ++r) {
-    p.in[r] = static_cast<const char*>(in[r]);
-    p.out[r] = static_cast<char*>(out[r]);
-  }
-  p.count = count;
-  p.nranks = c.n;
+  fill_params(c, p, in, out, count);
   p.iters = iters;
   p.chain = chain;
   p.chain_scale = chain_scale;
   p.in_stride = in_stride;
   p.out_stride = out_stride;
-  p.epoch_dev = reinterpret_cast<unsigned long long*>(c.base + c.abort_off + 128);
-  p.done_count = reinterpret_cast<unsigned*>(c.base + c.abort_off + 64);
-  p.ll = c.base + c.ll_off;
-  p.ll_stride = c.ll_stride;
-  p.ll_slot_words = c.ll_words;
-  p.sen = c.base + c.sen_off;
-  p.sen_stride = c.sen_stride;
-  p.sen_chunk_vecs = (int)(c.chunk_bytes / 16);
-  p.l128 = c.base + c.l128_off;
-  p.l128_stride = c.l128_stride;
-  p.l128ag = c.base + c.ag_off;
-  p.l128ag_stride = c.ag_stride;
-  p.l128_lines = c.l128_lines;
-  p.chainbuf = c.base + c.chain_off;
-  p.chain_stride = c.chain_stride;
-  p.chain_slot_bytes = c.chain_slot;
-  p.flags = reinterpret_cast<unsigned long long*>(c.base + c.flags_off);
-  p.flags_gmax = kFlagsGmax;
-  p.timeout_ns = g_timeout_ns;
-  p.inject_rank = g_inject_rank;
-  p.inject_mode = g_inject_mode;
-  p.abort_flag = reinterpret_cast<unsigned*>(c.base + c.abort_off);
-  p.status = c.status_dev;
 
   int G = 1, T = 128;
   choose_shape(c, proto, count, chain, &G, &T);
@@ -404,6 +475,16 @@ int llar_allreduce_iters(const void* const* in, void* const* out, size_t count, 
   std::lock_guard<std::mutex> lk(g_mu);
   return run(in, out, count, protocol, iters, in_stride_elems, out_stride_elems, chain_scale,
              static_cast<cudaStream_t>(stream));
+}
+
+int llar_reduce_scatter(const void* const* in, void* const* out, size_t count, int protocol, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return run_segment(true, in, out, count, protocol, static_cast<cudaStream_t>(stream));
+}
+
+int llar_all_gather(const void* const* in, void* const* out, size_t count, int protocol, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return run_segment(false, in, out, count, protocol, static_cast<cudaStream_t>(stream));
 }
 
 int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int protocol, void* stream) {

@@ -47,6 +47,8 @@ def lib():
         "llar_allreduce": (c_int, [pp, pp, c_size, c_int, c_vp]),
         "llar_allreduce_iters": (c_int, [pp, pp, c_size, c_int, c_int, c_size, c_size, ctypes.c_float, c_vp]),
         "llar_allreduce_host": (c_int, [c_vp, c_vp, c_size, c_int, c_vp]),
+        "llar_reduce_scatter": (c_int, [pp, pp, c_size, c_int, c_vp]),
+        "llar_all_gather": (c_int, [pp, pp, c_size, c_int, c_vp]),
         "llar_allreduce_noalloc": (c_int, [pp, pp, c_size, c_int, c_int, c_vp]),
         "llar_get_status": (c_int, [ctypes.POINTER(c_int), ctypes.POINTER(c_int), ctypes.POINTER(c_ull)]),
         "llar_reset": (c_int, [c_vp]),
@@ -141,6 +143,20 @@ def llar_allreduce_iters(ins, outs, count, protocol, iters, in_stride=0, out_str
                                       int(out_stride), float(chain_scale),
                                       ctypes.c_void_p(_stream(stream))),
            "llar_allreduce_iters")
+
+
+def llar_reduce_scatter(ins, outs, count, protocol="auto", stream=None):
+    """outs[r] = rank-order sum of segment r of every ins[q] (count = full length)."""
+    _check(lib().llar_reduce_scatter(_ptr_array(ins), _ptr_array(outs), int(count),
+                                     _enum(PROTOCOLS, protocol), ctypes.c_void_p(_stream(stream))),
+           "llar_reduce_scatter")
+
+
+def llar_all_gather(ins, outs, count, protocol="auto", stream=None):
+    """outs[r] = concatenation of every rank's segment ins[q] (count = full length)."""
+    _check(lib().llar_all_gather(_ptr_array(ins), _ptr_array(outs), int(count),
+                                 _enum(PROTOCOLS, protocol), ctypes.c_void_p(_stream(stream))),
+           "llar_all_gather")
 
 
 def llar_allreduce_host(in_host, out_host, count, protocol="auto", stream=None):
