@@ -500,6 +500,8 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
   // Pinned host buffers that the device can address (page-locked memory
   // under unified addressing): the kernel reads the inputs and writes the
   // outputs across the bus itself, one launch and no staging copies.
+  // Measured against one DMA each way (or DMA in, zero-copy out), this is
+  // the fastest of the three for the small messages this entry serves.
   if (bytes % 16 == 0) {
     cudaPointerAttributes ai, ao;
     if (cudaPointerGetAttributes(&ai, in_host) == cudaSuccess && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
@@ -525,17 +527,23 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
   }
   char* din = c.io;
   char* dout = c.io + c.io_stride * c.n;
-  cudaError_t err = cudaMemcpy2DAsync(din, c.io_stride, in_host, bytes, bytes, c.n, cudaMemcpyHostToDevice, s);
+  const bool rows16 = bytes % 16 == 0;
+  // Rows that are 16-byte multiples go in one 1-D copy each way (contiguous
+  // staging rows keep every rank's pointer 16-byte aligned).
+  const size_t dstride = rows16 ? bytes : c.io_stride;
+  cudaError_t err = rows16 ? cudaMemcpyAsync(din, in_host, bytes * c.n, cudaMemcpyHostToDevice, s)
+                           : cudaMemcpy2DAsync(din, c.io_stride, in_host, bytes, bytes, c.n, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) return cuda_status(err);
   const void* ins[llar::kMaxRanks];
   void* outs[llar::kMaxRanks];
   for (int r = 0; r < c.n; ++r) {
-    ins[r] = din + r * c.io_stride;
-    outs[r] = dout + r * c.io_stride;
+    ins[r] = din + r * dstride;
+    outs[r] = dout + r * dstride;
   }
   const int st = run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
   if (st != LLAR_OK) return st;
-  err = cudaMemcpy2DAsync(out_host, bytes, dout, c.io_stride, bytes, c.n, cudaMemcpyDeviceToHost, s);
+  err = rows16 ? cudaMemcpyAsync(out_host, dout, bytes * c.n, cudaMemcpyDeviceToHost, s)
+               : cudaMemcpy2DAsync(out_host, bytes, dout, c.io_stride, bytes, c.n, cudaMemcpyDeviceToHost, s);
   return cuda_status(err);
 }
 
