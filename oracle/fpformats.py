@@ -78,6 +78,40 @@ def encode_rne(f32, dtype):
     raise ValueError(dtype)
 
 
+def encode_rne64(x64, dtype):
+    """float64 values -> raw bits of `dtype`, ONE roundTiesToEven rounding.
+
+    For values that are not float32 numbers (an exact float64 dot product)
+    rounding through float32 first could round twice. fp32 and fp16 use
+    numpy's direct float64 casts (IEEE conversions, roundTiesToEven); bf16
+    is written out from the definition: the value's spacing in bf16 is
+    2^(max(floor(log2|x|), emin) - p + 1); x / spacing is rounded to the
+    nearest integer, ties to even (np.rint), and scaled back, which is then
+    a bf16 number, exact in float32. Magnitudes at or beyond the largest
+    finite value plus half its spacing become infinities.
+    """
+    x = np.asarray(x64, dtype=np.float64)
+    if dtype == FP32:
+        with np.errstate(over="ignore", invalid="ignore"):
+            return x.astype(np.float32).view(np.uint32)
+    if dtype == FP16:
+        with np.errstate(over="ignore", invalid="ignore"):
+            return x.astype(np.float16).view(np.uint16)
+    if dtype == BF16:
+        p, emin = PRECISION[BF16], EMIN[BF16]
+        ax = np.abs(x)
+        with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+            _, e2 = np.frexp(ax)
+            expo = np.maximum(np.where(ax > 0, e2 - 1, emin), emin)
+            spacing = np.ldexp(1.0, (expo - p + 1).astype(np.int64))
+            r = np.rint(x / spacing) * spacing
+            big = np.abs(r) > max_finite(BF16)
+            r = np.where(big, np.copysign(np.inf, x), r)
+            r = np.where(np.isfinite(x), r, x)
+        return _bf16_rne(r.astype(np.float32))
+    raise ValueError(dtype)
+
+
 def is_nan_bits(bits, dtype):
     """True where the bit pattern is a NaN of `dtype`."""
     return np.isnan(decode(bits, dtype))

@@ -11,13 +11,16 @@ from oracle import protocol as oproto
 from tp_allreduce_persistent_b300 import build, llar
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "llar.h")
+HEADERS = [os.path.join(ROOT, "include", n) for n in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if n.endswith(".h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(llar_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(llar_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_library_builds_and_exports_every_declared_symbol():
@@ -90,3 +93,49 @@ def test_init_without_gpu_fails_cleanly():
         llar.llar_init(8, "bf16", 1 << 20)
     assert ei.value.code == llar.ERR_CUDA
     llar.llar_set_launch(0, 0)
+
+
+def test_llbuffer_descriptor_layout_matches_c():
+    """The ctypes mirror of llar_llbuffer has the C compiler's offsets and size."""
+    import shutil
+    import subprocess
+    import tempfile
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in llar.LLBufferDesc._fields_]
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"llar_llbuffer.h\"\nint main(void){\n"
+    src += 'printf("%zu\\n", sizeof(llar_llbuffer));\n'
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof(llar_llbuffer, {f}));\n'
+    src += 'printf("%zu %zu\\n", sizeof(llar_llbuffer_status), offsetof(llar_llbuffer_status, epoch));\n'
+    src += "return 0;}\n"
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write(src)
+        subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
+    want = [ctypes.sizeof(llar.LLBufferDesc)] + [getattr(llar.LLBufferDesc, f).offset for f in fields]
+    want += [ctypes.sizeof(llar.LLBufferStatus), llar.LLBufferStatus.epoch.offset]
+    assert [int(x) for x in got] == want
+
+
+def test_llbuffer_argument_checks_without_device():
+    for n, b in [(1, 1024), (9, 1024), (4, 0), (4, (1 << 30) + 1)]:
+        with pytest.raises(llar.LlarError) as ei:
+            llar.LLBuffer(n, b)
+        assert ei.value.code == llar.ERR_INVALID
+    desc = llar.LLBufferDesc()  # never created
+    assert llar.lib().llar_llbuffer_destroy(ctypes.byref(desc)) == llar.ERR_INVALID
+    assert llar.lib().llar_llbuffer_get_status(ctypes.byref(desc), None, None) == llar.ERR_INVALID
+    pp = (ctypes.c_void_p * 8)()
+    assert llar.lib().llar_llbuffer_allreduce(ctypes.byref(desc), pp, pp, 16, 0, 1, 1, None) == llar.ERR_INVALID
+    # the plain GEMV checks its shape before touching the device
+    assert llar.lib().llar_linear_partials(pp, pp, pp, 2, 17, 8, 8, 2, None) == llar.ERR_INVALID  # M > 16
+    assert llar.lib().llar_linear_partials(pp, pp, pp, 2, 1, 8, 12, 2, None) == llar.ERR_INVALID  # H % 8
+    import torch
+    if not torch.cuda.is_available():
+        with pytest.raises(llar.LlarError) as ei:
+            llar.LLBuffer(2, 1024)
+        assert ei.value.code == llar.ERR_CUDA

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libllar.so")
-SOURCES = ["llar_runtime.cu", "llar_kernels.cu"]
+SOURCES = ["llar_runtime.cu", "llar_kernels.cu", "llar_llbuffer.cu"]
 HEADERS = ["llar_internal.h", "llar_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -28,7 +28,8 @@ def nvcc_path():
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files.append(os.path.join(INCLUDE, "llar.h"))
+    for name in ("llar.h", "llar_llbuffer.h", "llar_llbuffer.cuh"):
+        files.append(os.path.join(INCLUDE, name))
     files.append(os.path.abspath(__file__))
     return files
 

@@ -81,3 +81,19 @@ def from_bits(bits, dtype):
     if dtype == "fp32":
         return torch.from_numpy(bits.view(np.int32).copy()).view(torch.float32)
     return torch.from_numpy(bits.view(np.int16).copy()).view(TORCH_DTYPE[dtype])
+
+
+def linear_layer(nranks, m, k, h, dtype, seed, integer=False, device="cpu"):
+    """Inputs of a row-parallel linear layer split over `nranks`: activations
+    x [N, M, K] ~ N(0, 1) and weights w [N, K, H] ~ N(0, 1) / sqrt(N * K)
+    (the scale of an initialised layer with N * K inputs), or, with
+    integer=True, x in {-3..3} and w in {-2..2} (every partial sum exact)."""
+    g = _gen(seed, device)
+    if integer:
+        x = torch.randint(-3, 4, (nranks, m, k), generator=g, device=device).to(torch.float32)
+        w = torch.randint(-2, 3, (nranks, k, h), generator=g, device=device).to(torch.float32)
+    else:
+        x = torch.randn((nranks, m, k), generator=g, device=device, dtype=torch.float32)
+        w = torch.randn((nranks, k, h), generator=g, device=device, dtype=torch.float32)
+        w = w * float((nranks * k) ** -0.5)
+    return x.to(TORCH_DTYPE[dtype]), w.to(TORCH_DTYPE[dtype])

@@ -23,6 +23,27 @@ OK, ERR_INVALID, ERR_NOT_INIT, ERR_TOO_LARGE, ERR_UNSUPPORTED, ERR_OCCUPANCY, ER
 _lib = None
 
 
+class LLBufferStatus(ctypes.Structure):
+    """llar_llbuffer_status (include/llar_llbuffer.h)."""
+    _fields_ = [("code", ctypes.c_uint), ("rank", ctypes.c_int), ("epoch", ctypes.c_ulonglong)]
+
+
+class LLBufferDesc(ctypes.Structure):
+    """llar_llbuffer (include/llar_llbuffer.h), field for field."""
+    _fields_ = [("nranks", ctypes.c_int), ("reserved", ctypes.c_int), ("bytes", ctypes.c_size_t),
+                ("timeout_ns", ctypes.c_ulonglong),
+                ("ll", ctypes.c_void_p), ("ll_rank_stride", ctypes.c_size_t),
+                ("ll_slot_stride", ctypes.c_size_t), ("ll_words", ctypes.c_size_t),
+                ("sen", ctypes.c_void_p), ("sen_rank_stride", ctypes.c_size_t),
+                ("sen_slot_stride", ctypes.c_size_t), ("sen_src_stride", ctypes.c_size_t),
+                ("sen_vecs", ctypes.c_size_t),
+                ("ll128", ctypes.c_void_p), ("ll128_rank_stride", ctypes.c_size_t),
+                ("ll128_slot_stride", ctypes.c_size_t), ("ll128_lines", ctypes.c_size_t),
+                ("epoch", ctypes.c_void_p), ("done_count", ctypes.c_void_p),
+                ("abort_word", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("status_host", ctypes.c_void_p)]
+
+
 class LlarError(RuntimeError):
     def __init__(self, code, what):
         self.code = code
@@ -69,6 +90,19 @@ def lib():
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
         "llar_strerror": (ctypes.c_char_p, [c_int]),
+        "llar_llbuffer_create": (c_int, [c_int, c_size, ctypes.POINTER(LLBufferDesc)]),
+        "llar_llbuffer_destroy": (c_int, [ctypes.POINTER(LLBufferDesc)]),
+        "llar_llbuffer_get_status": (c_int, [ctypes.POINTER(LLBufferDesc), ctypes.POINTER(c_int),
+                                             ctypes.POINTER(c_ull)]),
+        "llar_llbuffer_reset": (c_int, [ctypes.POINTER(LLBufferDesc), c_vp]),
+        "llar_llbuffer_set_timeout_ns": (c_int, [ctypes.POINTER(LLBufferDesc), c_ull]),
+        "llar_llbuffer_epoch": (c_int, [ctypes.POINTER(LLBufferDesc), ctypes.POINTER(c_ull)]),
+        "llar_llbuffer_probe_wait": (c_int, [ctypes.POINTER(LLBufferDesc), c_int, c_int, c_ull, c_size, c_vp]),
+        "llar_llbuffer_allreduce": (c_int, [ctypes.POINTER(LLBufferDesc), pp, pp, c_size, c_int, c_int,
+                                            c_int, c_vp]),
+        "llar_fused_linear_allreduce": (c_int, [ctypes.POINTER(LLBufferDesc), pp, pp, pp, c_int, c_int,
+                                                c_int, c_int, c_vp]),
+        "llar_linear_partials": (c_int, [pp, pp, pp, c_int, c_int, c_int, c_int, c_int, c_vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -257,3 +291,110 @@ def llar_last_launch():
     v = [ctypes.c_int() for _ in range(4)]
     lib().llar_last_launch(*[ctypes.byref(x) for x in v])
     return PROTOCOL_NAMES.get(v[0].value, v[0].value), v[1].value, v[2].value, v[3].value
+
+
+# ------------------------------------------------------------ LL buffer API
+class LLBuffer:
+    """An llar_llbuffer descriptor (include/llar_llbuffer.h) and its calls.
+
+    Owns the device staging until close(); usable as a context manager."""
+
+    def __init__(self, nranks, nbytes):
+        self.desc = LLBufferDesc()
+        _check(lib().llar_llbuffer_create(int(nranks), int(nbytes), ctypes.byref(self.desc)),
+               "llar_llbuffer_create")
+
+    def close(self):
+        if self.desc.ll:
+            _check(lib().llar_llbuffer_destroy(ctypes.byref(self.desc)), "llar_llbuffer_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def nranks(self):
+        return self.desc.nranks
+
+    def status(self):
+        """(code, rank, epoch) of the descriptor's error record."""
+        r, e = ctypes.c_int(), ctypes.c_ulonglong()
+        code = lib().llar_llbuffer_get_status(ctypes.byref(self.desc), ctypes.byref(r), ctypes.byref(e))
+        return code, r.value, e.value
+
+    def reset(self, stream=None):
+        _check(lib().llar_llbuffer_reset(ctypes.byref(self.desc), ctypes.c_void_p(_stream(stream))),
+               "llar_llbuffer_reset")
+
+    def set_timeout_ns(self, ns):
+        _check(lib().llar_llbuffer_set_timeout_ns(ctypes.byref(self.desc), int(ns)),
+               "llar_llbuffer_set_timeout_ns")
+
+    def epoch(self):
+        """Exchanges completed so far (the device counter; synchronises the device)."""
+        e = ctypes.c_ulonglong()
+        _check(lib().llar_llbuffer_epoch(ctypes.byref(self.desc), ctypes.byref(e)), "llar_llbuffer_epoch")
+        return e.value
+
+    def probe_wait(self, rank, src, epoch, word, stream=None):
+        _check(lib().llar_llbuffer_probe_wait(ctypes.byref(self.desc), int(rank), int(src), int(epoch),
+                                              int(word), ctypes.c_void_p(_stream(stream))),
+               "llar_llbuffer_probe_wait")
+
+    def allreduce(self, ins, outs, count, dtype, protocol="ll", iters=1, stream=None):
+        _check(lib().llar_llbuffer_allreduce(ctypes.byref(self.desc), _ptr_array(ins), _ptr_array(outs),
+                                             int(count), _enum(DTYPES, dtype), _enum(PROTOCOLS, protocol),
+                                             int(iters), ctypes.c_void_p(_stream(stream))),
+               "llar_llbuffer_allreduce")
+
+    def fused_linear_allreduce(self, xs, ws, outs, m, k, h, dtype, stream=None):
+        _check(lib().llar_fused_linear_allreduce(ctypes.byref(self.desc), _ptr_array(xs), _ptr_array(ws),
+                                                 _ptr_array(outs), int(m), int(k), int(h),
+                                                 _enum(DTYPES, dtype), ctypes.c_void_p(_stream(stream))),
+               "llar_fused_linear_allreduce")
+
+
+def llar_linear_partials(xs, ws, ps, m, k, h, dtype, stream=None):
+    """ps[r] = rounded x[r] @ w[r] (the unfused layer's GEMV launch)."""
+    _check(lib().llar_linear_partials(_ptr_array(xs), _ptr_array(ws), _ptr_array(ps), len(xs), int(m),
+                                      int(k), int(h), _enum(DTYPES, dtype), ctypes.c_void_p(_stream(stream))),
+           "llar_linear_partials")
+
+
+# C-named entry points of the LL buffer API (the LLBuffer methods wrap them)
+def llar_llbuffer_create(nranks, nbytes):
+    return LLBuffer(nranks, nbytes)
+
+
+def llar_llbuffer_destroy(buf):
+    buf.close()
+
+
+def llar_llbuffer_get_status(buf):
+    return buf.status()
+
+
+def llar_llbuffer_reset(buf, stream=None):
+    buf.reset(stream)
+
+
+def llar_llbuffer_set_timeout_ns(buf, ns):
+    buf.set_timeout_ns(ns)
+
+
+def llar_llbuffer_epoch(buf):
+    return buf.epoch()
+
+
+def llar_llbuffer_allreduce(buf, ins, outs, count, dtype, protocol="ll", iters=1, stream=None):
+    buf.allreduce(ins, outs, count, dtype, protocol, iters, stream)
+
+
+def llar_fused_linear_allreduce(buf, xs, ws, outs, m, k, h, dtype, stream=None):
+    buf.fused_linear_allreduce(xs, ws, outs, m, k, h, dtype, stream)
+
+
+def llar_llbuffer_probe_wait(buf, rank, src, epoch, word, stream=None):
+    buf.probe_wait(rank, src, epoch, word, stream)
