@@ -161,8 +161,10 @@ struct Wait {
   }
 };
 
-// Record a timeout of `rank` waiting for epoch E; the first one wins.
-__device__ __noinline__ void fail(const llar_llbuffer& b, int rank, u64 E) {
+// Record a timeout of `rank` waiting for epoch E; the first one wins. Kept
+// out of line (it is cold); internal linkage, so that any number of
+// translation units of one program may include this header.
+static __device__ __noinline__ void fail(const llar_llbuffer& b, int rank, u64 E) {
   if (atomicCAS(b.abort_word, 0u, 7u) == 0u) {
     volatile llar_llbuffer_status* st = b.status;
     st->rank = rank;

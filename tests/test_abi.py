@@ -139,3 +139,25 @@ def test_llbuffer_argument_checks_without_device():
         with pytest.raises(llar.LlarError) as ei:
             llar.LLBuffer(2, 1024)
         assert ei.value.code == llar.ERR_CUDA
+
+
+def test_device_header_links_into_several_translation_units():
+    """Two .cu files of one program both include the device header."""
+    import shutil
+    import subprocess
+    import tempfile
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("no nvcc")
+    src = ('#include "llar_llbuffer.cuh"\n'
+           '__global__ void k_%s(llar_llbuffer b) { llb::u64 d; llb::ll_wait(b, 0, 1, 1, 0, d); }\n')
+    with tempfile.TemporaryDirectory() as d:
+        files = []
+        for name in ("a", "b"):
+            path = os.path.join(d, name + ".cu")
+            open(path, "w").write(src % name)
+            files.append(path)
+        main = os.path.join(d, "main.cu")
+        open(main, "w").write("int main() { return 0; }\n")
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-I", os.path.join(ROOT, "include"),
+                        *files, main, "-o", os.path.join(d, "prog")], check=True, capture_output=True)

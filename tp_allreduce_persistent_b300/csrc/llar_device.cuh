@@ -21,60 +21,26 @@
 #include <cstdint>
 
 #include "llar_internal.h"
+#include "llar_llbuffer.cuh"
 
 namespace llar {
 
 typedef unsigned long long u64;
 
 // ------------------------------------------------------------------ PTX
-__device__ __forceinline__ u64 globaltimer_ns() {
-  u64 t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// The signalling accesses shared with the public device primitives.
+using llb::fence_gpu;
+using llb::globaltimer_ns;
+using llb::ld_acquire_u32;
+using llb::ld_relaxed_b128;
+using llb::ld_relaxed_u32;
+using llb::ld_relaxed_v4;
+using llb::st_relaxed_b128;
+using llb::st_relaxed_v4;
 
-__device__ __forceinline__ void fence_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
-// 16-byte scalar (.b128) relaxed store/load: one single access of 16 bytes,
-// used for LL lines {8 bytes data, 8 bytes flag}.
-__device__ __forceinline__ void st_relaxed_b128(void* p, u64 lo, u64 hi) {
-  asm volatile(
-      "{\n .reg .b128 t;\n mov.b128 t, {%1, %2};\n st.relaxed.gpu.global.b128 [%0], t;\n}"
-      :: "l"(p), "l"(lo), "l"(hi) : "memory");
-}
-__device__ __forceinline__ void ld_relaxed_b128(const void* p, u64& lo, u64& hi) {
-  asm volatile(
-      "{\n .reg .b128 t;\n ld.relaxed.gpu.global.b128 t, [%2];\n mov.b128 {%0, %1}, t;\n}"
-      : "=l"(lo), "=l"(hi) : "l"(p) : "memory");
-}
-
-// 16-byte vector relaxed store/load (four 32-bit single-copy-atomic parts).
-__device__ __forceinline__ void st_relaxed_v4(void* p, uint4 v) {
-  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};"
-               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const void* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ u64 ld_acquire_u64(const void* p) {
   u64 v;
   asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned ld_relaxed_u32(const void* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_relaxed_u64(void* p, u64 v) {

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "llar_llbuffer.h"
+
 namespace llar {
 
 constexpr int kMaxRanks = 8;
@@ -22,14 +24,21 @@ constexpr int LLAR_INJECT_POISON_ = 2;
 constexpr int LLAR_INJECT_DELAY_ = 3;
 
 // Written by the first device wait that runs out; lives in mapped host
-// memory so the host can read it without a device synchronisation.
+// memory so the host can read it without a device synchronisation. Its
+// first three fields are an llar_llbuffer_status, so that the public device
+// primitives (which record code, rank and epoch) can report into it; they
+// leave `cta` as the host set it (-1: not recorded).
 struct DevStatus {
   unsigned int code;  // 0 = ok, else an llar_status_t
   int rank;
+  unsigned long long epoch;
   int cta;
   int pad;
-  unsigned long long epoch;
 };
+static_assert(offsetof(DevStatus, code) == offsetof(llar_llbuffer_status, code) &&
+                  offsetof(DevStatus, rank) == offsetof(llar_llbuffer_status, rank) &&
+                  offsetof(DevStatus, epoch) == offsetof(llar_llbuffer_status, epoch),
+              "DevStatus must start with an llar_llbuffer_status");
 
 // Everything a launch needs. Passed by value as the kernel parameter.
 struct Params {

@@ -65,6 +65,12 @@ constexpr size_t kBulkMinBytes = 1u << 20;  // per rank: TMA bulk path from 1 Mi
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
+// no error recorded; cta -1 until a wait that records its CTA runs out
+void clear_status(llar::DevStatus* st) {
+  std::memset(st, 0, sizeof(*st));
+  st->cta = -1;
+}
+
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return LLAR_OK;
   if (e == cudaErrorCooperativeLaunchTooLarge) return LLAR_ERR_OCCUPANCY;
@@ -369,7 +375,7 @@ int fill_staging(Ctx& c, cudaStream_t s) {
   // abort word only: the epoch counter at +128 keeps counting across resets
   ok(cudaMemsetAsync(c.base + c.abort_off, 0, 4, s));
   ok(cudaStreamSynchronize(s));
-  std::memset(c.status_host, 0, sizeof(llar::DevStatus));
+  clear_status(c.status_host);
   return cuda_status(err);
 }
 
