@@ -359,6 +359,7 @@ def configs_leg(llar, torch, dev, stream):
         "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "fixed_oneshot")},
         "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "fixed_oneshot")},
     }
+    out.update(llbuffer_rows(llar, torch, dev, stream))
     sweep = {}
     for mib in (1, 4, 16, 64, 256):
         count = (mib << 20) // 2
@@ -367,6 +368,98 @@ def configs_leg(llar, torch, dev, stream):
         sweep[f"{mib}MiB"] = {"us": us, "GB/s": round(2 * 8 * count * 2 / (us * 1e-6) / 1e9, 1)}
     out["C5_sweep_8ranks_bf16_fixed_twoshot"] = sweep
     return out
+
+
+def llbuffer_rows(llar, torch, dev, stream):
+    """The LL buffer API: AllReduces built from the public device primitives
+    (among them the two-rank 128-byte one-shot), and the row-parallel decode
+    linear layer with its AllReduce fused into the GEMV epilogue against
+    the unfused pipeline (GEMV launch, then the library's LL AllReduce)."""
+    from tp_allreduce_persistent_b300 import inputs
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def per_call_us(fn, iters):
+        fn(min(iters, 20))
+        torch.cuda.synchronize()
+        a.record(stream)
+        fn(iters)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / iters
+
+    rows = {}
+    for name, n, dtype, count, iters in (("2ranks_128B_fp32", 2, "fp32", 32, 10000),
+                                         ("8ranks_16KiB_bf16", 8, "bf16", 8192, 10000)):
+        with llar.LLBuffer(n, count * inputs.ELEM_BYTES[dtype]) as buf:
+            x = inputs.normal(n, count, dtype, seed=7, scale=0.02, exclude_sentinel=True)
+            ins = [x[r].to(dev) for r in range(n)]
+            outs = [torch.empty_like(t) for t in ins]
+            rows[name] = {}
+            for proto in ("ll", "sentinel", "ll128"):
+                us = per_call_us(lambda it: buf.allreduce(ins, outs, count, dtype, proto, it),
+                                 iters if proto == "ll" else iters // 10)
+                if buf.status()[0] != llar.OK:
+                    raise RuntimeError("LL buffer status not ok")
+                rows[name][proto] = round(us, 3)
+    res = {"llbuffer_allreduce_us": rows}
+
+    # decode layers of a hidden-8192 model over 8 ranks, one token: attention
+    # output projection (K = 8192 / 8) and MLP down projection (K = 28672 / 8);
+    # weight sets rotate so that each call streams weights not in L2
+    peak = measured_peaks()[0]["hbm_gbs"]
+    layers = {}
+    for name, k, sets in (("attn_out_k1024", 1024, 4), ("mlp_down_k3584", 3584, 2)):
+        n, m, h, dtype = 8, 1, 8192, "bf16"
+        xs, ws = [], []
+        for sidx in range(sets):
+            x, w = inputs.linear_layer(n, m, k, h, dtype, seed=100 + sidx)
+            xs.append([x[r].to(dev) for r in range(n)])
+            ws.append([w[r].to(dev) for r in range(n)])
+        outs = [torch.empty(m * h, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        parts = [torch.empty(m * h, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        llar.llar_init(n, dtype, m * h * 2)
+        try:
+            with llar.LLBuffer(n, m * h * 2) as buf:
+                def fused(s_):
+                    buf.fused_linear_allreduce(xs[s_], ws[s_], outs, m, k, h, dtype)
+
+                def unfused(s_):
+                    llar.llar_linear_partials(xs[s_], ws[s_], parts, m, k, h, dtype)
+                    llar.llar_allreduce(parts, outs, m * h, "ll")
+
+                def gemv(s_):
+                    llar.llar_linear_partials(xs[s_], ws[s_], parts, m, k, h, dtype)
+
+                timing = {}
+                for label, fn in (("fused", fused), ("unfused", unfused), ("gemv_only", gemv)):
+                    for s_ in range(sets):
+                        fn(s_)
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    reps = 5
+                    with torch.cuda.graph(g):
+                        for _ in range(reps):
+                            for s_ in range(sets):
+                                fn(s_)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    timing[label] = a.elapsed_time(b) * 1e3 / (reps * sets)
+                if buf.status()[0] != llar.OK or llar.llar_get_status()[0] != llar.OK:
+                    raise RuntimeError("device status not ok")
+        finally:
+            llar.llar_destroy()
+        wbytes = n * k * h * 2
+        gbs = wbytes / (timing["fused"] * 1e-6) / 1e9
+        layers[name] = {"fused_us": round(timing["fused"], 2), "unfused_us": round(timing["unfused"], 2),
+                        "gemv_only_us": round(timing["gemv_only"], 2), "weight_bytes": wbytes,
+                        "fused_weight_GB/s": round(gbs, 1), "fused_frac_of_measured_hbm": round(gbs / peak, 4)}
+        del xs, ws
+    res["fused_linear_allreduce_8ranks_m1_h8192_bf16"] = layers
+    return res
 
 
 def run_ours(args, world, rank, local, pg):
