@@ -57,8 +57,8 @@ def parse(argv=None):
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
-    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth"],
-                    help="run one leg only (small profiling cases)")
+    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer"],
+                    help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone")
     ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
     ap.add_argument("--bw-mib", type=int, default=BW_COUNT * 2 >> 20, help="MiB per rank, bandwidth leg")
     return ap.parse_args(argv)
@@ -113,12 +113,18 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+# the translation unit of the kernels whose DRAM traffic profiles/ records
+KERNEL_SOURCES = ("tp_allreduce_persistent_b300/csrc/llar_kernels.cu",
+                  "tp_allreduce_persistent_b300/csrc/llar_device.cuh",
+                  "tp_allreduce_persistent_b300/csrc/llar_internal.h",
+                  "include/llar_llbuffer.cuh", "include/llar_llbuffer.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "tp_allreduce_persistent_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(os.path.basename(rel).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -469,6 +475,10 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if args.leg == "llbuffer":
+        if rank == 0:
+            print(json.dumps({"leg": "llbuffer", **llbuffer_rows(llar, torch, dev, stream)}))
+        return
     llar.llar_init(NRANKS, DTYPE, max(args.bw_mib << 20, COUNT * 2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peaks, peak_src = measured_peaks()
