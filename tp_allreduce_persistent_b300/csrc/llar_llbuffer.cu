@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kLinearThreads) kb_linear(const llar_llbuffer 
   constexpr int VEC = LW / EB;       // columns per lane
   constexpr int COLS = 32 * VEC;     // columns per tile
   constexpr int WPL = LW / 8;        // LL words per lane per row
-  constexpr int UNROLL = 8;
+  constexpr int UNROLL = (MT <= 2 && LW == 16) ? 16 : 8;  // weight rows in flight per lane
   extern __shared__ __align__(16) unsigned char smem[];
   const u64 E = FUSE ? llb::begin(b) : 0;
   // block b is CTA b / N of rank b % N, as everywhere
