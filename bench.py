@@ -365,6 +365,29 @@ def configs_leg(llar, torch, dev, stream):
         "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "fixed_oneshot")},
         "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "fixed_oneshot")},
     }
+    # point-to-point hand-off along a ring of 8 ranks (every rank sends 16 KiB
+    # bf16 to the next), back-to-back transfers in one launch
+    def p2p_us(proto, iters):
+        n, count = 8, 8192
+        llar.llar_init(n, "bf16", count * 2)
+        try:
+            sends = [torch.randn(count, device=dev).to(torch.bfloat16) for _ in range(n)]
+            recvs = [torch.empty_like(t) for t in sends]
+            ring = [(r + 1) % n for r in range(n)]
+            llar.llar_sendrecv(sends, recvs, ring, count, proto, 20)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            llar.llar_sendrecv(sends, recvs, ring, count, proto, iters)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if llar.llar_get_status()[0] != llar.OK:
+                raise RuntimeError("device status not ok")
+            return round(a.elapsed_time(b) * 1e3 / iters, 3)
+        finally:
+            llar.llar_destroy()
+
+    out["p2p_ring_8ranks_16KiB_bf16_us"] = {p: p2p_us(p, 10000) for p in ("ll", "sentinel")}
     out.update(llbuffer_rows(llar, torch, dev, stream))
     sweep = {}
     for mib in (1, 4, 16, 64, 256):

@@ -129,6 +129,27 @@ int llar_reduce_scatter(const void* const* in, void* const* out, size_t count,
 int llar_all_gather(const void* const* in, void* const* out, size_t count,
                     int protocol, void* stream);
 
+/* Point-to-point transfers between virtual ranks (a pipeline-parallel
+ * stage hand-off; "Every Microsecond Matters", summary page: the LL and
+ * sentinel signalling, double-buffered). Rank r sends `count` elements of
+ * the context's type from send[r] to rank dst[r] (dst: host array of N
+ * ints, -1 = rank r sends nothing; dst[r] != r; every rank receives from at
+ * most one sender) into recv[dst[r]]. `iters` >= 1 transfers run back to
+ * back in one launch; transfer e reads send[r] + e*send_stride and writes
+ * recv[q] + e*recv_stride (strides in elements, 16-byte multiples; 0 =
+ * the same buffers). The receiver of each CTA's share acknowledges it
+ * after consuming it, and the sender waits for that before reusing the
+ * slot two transfers later (a one-way flow has no returning data to act
+ * as the credit). protocol: LLAR_PROTO_LL (count * elem <= the LL
+ * capacity, 1 MiB by default), LLAR_PROTO_SENTINEL (chunked; data must not
+ * contain the all-ones element pattern) or LLAR_PROTO_AUTO (LL up to
+ * 64 KiB). Pointers of ranks that neither send (send) nor receive (recv)
+ * may be NULL; the others are device pointers, 16-byte aligned, and no
+ * receive span overlaps a send span or another receive span. The result
+ * is a bit copy. Asynchronous; status codes as llar_allreduce. */
+int llar_sendrecv(const void* const* send, void* const* recv, const int* dst, size_t count,
+                  int protocol, int iters, size_t send_stride, size_t recv_stride, void* stream);
+
 /* One AllReduce on HOST buffers: in_host and out_host are [N][count]
  * contiguous arrays in host memory. If both are page-locked and
  * device-addressable (cudaHostAlloc / cudaHostRegister memory under

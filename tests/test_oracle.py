@@ -336,3 +336,40 @@ def test_sentinel_is_a_negative_nan(dtype):
     assert np.isnan(v[0]) and np.signbit(v[0])
     assert protocol.sentinel_refilled(np.full(10, protocol.sentinel_bits(dtype), fp.BITS_DTYPE[dtype]), dtype)
     assert not protocol.sentinel_refilled(np.zeros(10, fp.BITS_DTYPE[dtype]), dtype)
+
+
+# ---------------------------------------------------------------- point to point
+def test_p2p_ring_shift_n_times_is_identity():
+    from oracle import p2p
+    rng = np.random.default_rng(31)
+    n = 5
+    x = rng.integers(0, 2 ** 16, (n, 13), dtype=np.uint16)
+    ring = [(r + 1) % n for r in range(n)]
+    y = x
+    for _ in range(n):
+        y = p2p.sendrecv(y, ring, np.zeros_like(x))
+    assert np.array_equal(y, x)
+    # one shift moves row r to row r + 1 (and not the other way round)
+    one = p2p.sendrecv(x, ring, np.zeros_like(x))
+    assert np.array_equal(one[1], x[0]) and np.array_equal(one[0], x[n - 1])
+
+
+def test_p2p_permutation_then_inverse_restores_and_idle_rows_keep_fill():
+    from oracle import p2p
+    rng = np.random.default_rng(32)
+    n = 7
+    perm = [3, 0, 5, 1, 6, 2, 4]
+    inv = [perm.index(q) for q in range(n)]
+    x = rng.integers(0, 2 ** 32, (n, 9), dtype=np.uint32)
+    assert np.array_equal(p2p.sendrecv(p2p.sendrecv(x, perm, 0 * x), inv, 0 * x), x)
+    fill = np.full_like(x, 7)
+    part = p2p.sendrecv(x, [2, -1, -1, -1, -1, -1, 0], fill)
+    assert np.array_equal(part[2], x[0]) and np.array_equal(part[0], x[6])
+    assert all(np.array_equal(part[q], fill[q]) for q in (1, 3, 4, 5, 6))
+
+
+@pytest.mark.parametrize("dst", [[0, 1], [1, 1, -1], [3, 0], [1, 0, 1]])
+def test_p2p_invalid_maps_rejected(dst):
+    from oracle import p2p
+    with pytest.raises(ValueError):
+        p2p.sources(dst)

@@ -17,6 +17,10 @@ constexpr int kLL128Line = 128;    // bytes per LL128 line
 constexpr int kLL128Lanes = 8;     // 16-byte lanes (threads) per line
 constexpr int kLLLine = 16;        // bytes per LL line: 8 data + 8 flag
 constexpr int kAgLineBytes = 256;  // one LL128 line re-sent as 16 LL lines
+// per (rank, CTA) signal words: 0 ready and 1 done epochs of the fixed-order
+// chains, 2 consumption acknowledgements of point-to-point transfers
+constexpr int kFlagKinds = 3;
+constexpr int kFlagAck = 2;
 
 // fault-injection modes (values of llar_inject_t)
 constexpr int LLAR_INJECT_SKIP_ = 1;
@@ -67,8 +71,11 @@ struct Params {
   size_t l128_lines;                            // L: lines per slot
   char* chainbuf;      size_t chain_stride;     // [2][max_bytes] per rank
   size_t chain_slot_bytes;
-  unsigned long long* flags;                    // [N][Gmax][2] ready/done epochs
+  unsigned long long* flags;                    // [N][Gmax][kFlagKinds] signal words
   int flags_gmax;
+
+  int peer_dst[kMaxRanks];  // point to point: rank r sends to peer_dst[r] (-1: none)
+  int peer_src[kMaxRanks];  // and receives from peer_src[r] (-1: none)
 
   unsigned long long timeout_ns;
   int inject_rank;
@@ -87,6 +94,9 @@ cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaSt
 // 3 AG fixed (one collective per launch)
 cudaError_t launch_segment(int which, int dtype, const Params& p, int threads, cudaStream_t s);
 int max_resident_segment_ctas(int which, int dtype, int nranks, int threads);
+// point-to-point transfers (proto LLAR_PROTO_LL or LLAR_PROTO_SENTINEL)
+cudaError_t launch_p2p(int proto, int dtype, const Params& p, int threads, cudaStream_t s);
+int max_resident_p2p_ctas(int proto, int dtype, int threads);
 // TMA bulk-copy variant of the fixed two-shot (no chain), one CTA per SM
 cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, cudaStream_t s);
 size_t bulk_smem_bytes(int nranks);

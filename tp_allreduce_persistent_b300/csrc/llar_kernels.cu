@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
 // epoch E-1 are done) and, for the two-shot, done[s][c] (owner s wrote
 // segment s, range c, of every output for epoch E).
 __device__ __forceinline__ unsigned long long* flag_ptr(const Params& p, int rank, int cta, int kind) {
-  return p.flags + ((size_t)rank * p.flags_gmax + cta) * 2 + kind;
+  return p.flags + ((size_t)rank * p.flags_gmax + cta) * kFlagKinds + kind;
 }
 
 // Thread 0 waits until flag[q][c][kind] >= want for every q != skip_rank;
@@ -1152,6 +1152,164 @@ __global__ void __launch_bounds__(kMaxThreads) k_ag_fixed(const Params p) {
   finish_launch(p);
 }
 
+// ========================================================= point to point
+// A pipeline-parallel stage hand-off between virtual ranks: rank r sends
+// its buffer to rank peer_dst[r] and receives from peer_src[r] ("Every
+// Microsecond Matters", summary page: the same LL and sentinel signalling,
+// double-buffered). CTA c of every rank covers the same share of the
+// message. A one-directional flow carries no returning data that could
+// act as technique 3's implicit credit, so the receiving CTA publishes an
+// explicit acknowledgement after it has consumed (and, for the sentinel,
+// reset) its share of a transfer; the sending CTA waits for it before it
+// reuses that slot two transfers later. Acknowledgement values are
+// (epoch << 24) + chunk, monotone across launches, in their own flag kind.
+__device__ __forceinline__ u64 ack_value(u64 E, unsigned chunk) { return (E << 24) + chunk; }
+
+// Thread 0 waits until rank q's CTA c acknowledged `want`; CTA-uniform result.
+__device__ __forceinline__ bool wait_ack(const Params& p, int q, int c, u64 want, int me, u64 E) {
+  int fail = 0;
+  if (threadIdx.x == 0) {
+    Waiter wt;
+    while (ld_acquire_u64(flag_ptr(p, q, c, kFlagAck)) < want)
+      if (wt.expired(p)) {
+        report_timeout(p, me, c, E);
+        fail = 1;
+        break;
+      }
+  }
+  return !__syncthreads_or(fail);
+}
+// After a CTA-wide barrier: thread 0 releases the CTA's reads and resets.
+__device__ __forceinline__ void post_ack(const Params& p, int me, int c, u64 value) {
+  if (threadIdx.x == 0) {
+    fence_gpu();
+    st_relaxed_u64(flag_ptr(p, me, c, kFlagAck), value);
+  }
+}
+
+// LL: rank r publishes its words in its own staging (slot E & 1) as in the
+// one-shot; the receiver polls the sender's lines. Slot E & 1 held epoch
+// E - 2, so the sender first waits for the receiver's acknowledgement of it.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
+  const u64 E0 = launch_epoch(p);
+  const int r = blockIdx.x % p.nranks, c = blockIdx.x / p.nranks;
+  // an injected silent rank neither sends nor acknowledges
+  const bool silent = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  const int dst = silent ? -1 : p.peer_dst[r], src = p.peer_src[r];
+  const size_t W = (p.count * Fmt<DT>::kBytes + 7) / 8;
+  const size_t per = (W + p.G - 1) / p.G;
+  const size_t w0 = min(W, (size_t)c * per), w1 = min(W, w0 + per);
+  const size_t slot_stride = p.ll_slot_words * (size_t)kLLLine;
+  char* const mine = p.ll + (size_t)r * p.ll_stride;
+  const char* const from = p.ll + (size_t)(src < 0 ? 0 : src) * p.ll_stride;
+  bool ok = true;
+  for (int e = 0; e < p.iters && ok; ++e) {
+    const u64 E = E0 + (u64)e;
+    const size_t slot = (size_t)(E & 1) * slot_stride;
+    if (dst >= 0) {
+      if (e >= 2) ok = wait_ack(p, dst, c, ack_value(E - 2, 0), r, E);
+      if (ok) {
+        const char* in = rank_input<DT>(p, r, e);
+        for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x)
+          st_relaxed_b128(mine + slot + w * kLLLine, load_word8<DT>(in, w, p.count), E);
+      }
+    }
+    if (src >= 0 && ok) {
+      char* out = rank_output<DT>(p, r, e);
+      bool mine_ok = true;
+      for (size_t w = w0 + threadIdx.x; w < w1 && mine_ok; w += blockDim.x) {
+        Waiter wt;
+        u64 lo, hi;
+        while (true) {
+          ld_relaxed_b128(from + slot + w * kLLLine, lo, hi);
+          if (hi == E) break;
+          if (wt.expired(p)) {
+            report_timeout(p, r, c, E);
+            mine_ok = false;
+            break;
+          }
+        }
+        if (mine_ok) store_word8<DT>(out, w, p.count, lo);
+      }
+      ok = !__syncthreads_or(!mine_ok);
+      if (ok && !silent) post_ack(p, r, c, ack_value(E, 0));
+    }
+  }
+  finish_launch(p);
+}
+
+// Sentinel: the sender pushes raw 16-byte vectors into the receiver's slot
+// [seq & 1][sender][vector] (all-ones when idle); the receiver polls until
+// no element is the all-ones pattern, stores the vector and resets the
+// slot. Messages longer than a chunk go in chunks, seq numbering them
+// within the launch; slot seq & 1 was last used by seq - 2.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_p2p_sentinel(const Params p) {
+  const u64 E0 = launch_epoch(p);
+  const int N = p.nranks;
+  const int r = blockIdx.x % N, c = blockIdx.x / N;
+  const bool silent = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  const int dst = silent ? -1 : p.peer_dst[r], src = p.peer_src[r];
+  const size_t NV = (p.count * Fmt<DT>::kBytes + 15) / 16;
+  const unsigned CV = (unsigned)p.sen_chunk_vecs;
+  const unsigned nchunks = (unsigned)((NV + CV - 1) / CV);
+  const unsigned per = (CV + p.G - 1) / p.G;
+  const unsigned j0 = min(CV, (unsigned)c * per), j1 = min(CV, j0 + per);
+  const size_t src_stride = (size_t)CV * 16;
+  const size_t slot_stride = (size_t)N * src_stride;
+  const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  char* const to = p.sen + (size_t)(dst < 0 ? 0 : dst) * p.sen_stride + (size_t)r * src_stride;
+  char* const box = p.sen + (size_t)r * p.sen_stride + (size_t)(src < 0 ? 0 : src) * src_stride;
+  bool ok = true;
+  for (int e = 0; e < p.iters && ok; ++e) {
+    const u64 E = E0 + (u64)e;
+    const char* in = rank_input<DT>(p, r, e);
+    char* out = rank_output<DT>(p, r, e);
+    for (unsigned k = 0; k < nchunks && ok; ++k) {
+      const size_t seq = (size_t)e * nchunks + k;
+      const size_t slot = (seq & 1) * slot_stride;
+      if (dst >= 0) {
+        if (seq >= 2) {
+          const size_t prev = seq - 2;
+          ok = wait_ack(p, dst, c, ack_value(E0 + prev / nchunks, (unsigned)(prev % nchunks)), r, E);
+        }
+        if (ok)
+          for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+            const size_t v = (size_t)k * CV + j;
+            if (v < NV) st_relaxed_v4(to + slot + (size_t)j * 16, load_vec16<DT>(in, v, p.count, false));
+          }
+      }
+      if (src >= 0 && ok) {
+        bool mine_ok = true;
+        for (unsigned j = j0 + threadIdx.x; j < j1 && mine_ok; j += blockDim.x) {
+          const size_t v = (size_t)k * CV + j;
+          if (v >= NV) continue;
+          char* cell = box + slot + (size_t)j * 16;
+          Waiter wt;
+          uint4 x;
+          while (true) {
+            x = ld_relaxed_v4(cell);
+            if (!has_sentinel<DT>(x)) break;
+            if (wt.expired(p)) {
+              report_timeout(p, r, c, E);
+              mine_ok = false;
+              break;
+            }
+          }
+          if (mine_ok) {
+            st_relaxed_v4(cell, ones);
+            store_vec16<DT>(out, v, p.count, x);
+          }
+        }
+        ok = !__syncthreads_or(!mine_ok);
+        if (ok && !silent) post_ack(p, r, c, ack_value(E, k));
+      }
+    }
+  }
+  finish_launch(p);
+}
+
 // ============================================================ launchers
 // Launch N x G blocks: cooperative when CTAs wait on each other (the
 // runtime refuses a grid that cannot be fully resident), in clusters of N
@@ -1288,6 +1446,26 @@ cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaSt
 
 size_t bulk_smem_bytes(int nranks) { return (size_t)kBulkStages * nranks * kBulkTileBytes + 8 * kBulkStages; }
 size_t bulk_tile_vectors() { return kBulkTileBytes / 16; }
+
+static const void* p2p_kernel(int proto, int dtype) {
+  if (proto == 1)
+    return dtype == 0 ? (const void*)k_p2p_ll<0> : dtype == 1 ? (const void*)k_p2p_ll<1> : (const void*)k_p2p_ll<2>;
+  return dtype == 0 ? (const void*)k_p2p_sentinel<0>
+                    : dtype == 1 ? (const void*)k_p2p_sentinel<1> : (const void*)k_p2p_sentinel<2>;
+}
+cudaError_t launch_p2p(int proto, int dtype, const Params& p, int threads, cudaStream_t s) {
+  return launch_kernel(p2p_kernel(proto, dtype), p, threads, s, true);
+}
+int max_resident_p2p_ctas(int proto, int dtype, int threads) {
+  int per = 0, sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, p2p_kernel(proto, dtype), threads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per * sms;
+}
 
 cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, cudaStream_t s) {
   const void* k = dtype == 0 ? (const void*)k_fixed_twoshot_bulk<0>

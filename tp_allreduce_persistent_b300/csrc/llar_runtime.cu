@@ -267,6 +267,99 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   return LLAR_OK;
 }
 
+// Point-to-point transfers: rank r sends to dst[r] (-1: nothing).
+int run_p2p(const void* const* send, void* const* recv, const int* dst, size_t count, int proto, int iters,
+            size_t send_stride, size_t recv_stride, cudaStream_t stream) {
+  if (!g) return LLAR_ERR_NOT_INIT;
+  Ctx& c = *g;
+  if (!send || !recv || !dst || iters < 1) return LLAR_ERR_INVALID;
+  const size_t e = c.esize;
+  const size_t bytes = count * e;
+  if ((send_stride * e) % 16 || (recv_stride * e) % 16) return LLAR_ERR_INVALID;
+  int src[llar::kMaxRanks];
+  for (int r = 0; r < c.n; ++r) src[r] = -1;
+  for (int r = 0; r < c.n; ++r) {
+    const int d = dst[r];
+    if (d < -1 || d >= c.n || d == r) return LLAR_ERR_INVALID;
+    if (d >= 0) {
+      if (src[d] >= 0) return LLAR_ERR_INVALID;  // a rank receives from one sender at most
+      src[d] = r;
+    }
+  }
+  if (proto == LLAR_PROTO_AUTO) proto = bytes <= (64u << 10) ? LLAR_PROTO_LL : LLAR_PROTO_SENTINEL;
+  if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_SENTINEL) return LLAR_ERR_UNSUPPORTED;
+  if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
+  if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
+  // participating buffers: 16-byte aligned, no receive span overlapping a
+  // send span or another receive span
+  const size_t sspan = (size_t)(iters - 1) * send_stride * e + bytes;
+  const size_t rspan = (size_t)(iters - 1) * recv_stride * e + bytes;
+  for (int r = 0; r < c.n; ++r) {
+    if (dst[r] >= 0 && (!send[r] || ((uintptr_t)send[r] & 15u))) return LLAR_ERR_INVALID;
+    if (src[r] >= 0 && (!recv[r] || ((uintptr_t)recv[r] & 15u))) return LLAR_ERR_INVALID;
+  }
+  for (int r = 0; r < c.n; ++r) {
+    if (src[r] < 0) continue;
+    const uintptr_t o0 = (uintptr_t)recv[r], o1 = o0 + rspan;
+    for (int q = 0; q < c.n; ++q) {
+      if (dst[q] >= 0) {
+        const uintptr_t i0 = (uintptr_t)send[q], i1 = i0 + sspan;
+        if (o0 < i1 && i0 < o1) return LLAR_ERR_INVALID;
+      }
+      if (q != r && src[q] >= 0) {
+        const uintptr_t p0 = (uintptr_t)recv[q], p1 = p0 + rspan;
+        if (o0 < p1 && p0 < o1) return LLAR_ERR_INVALID;
+      }
+    }
+  }
+  if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
+  if (count == 0) return LLAR_OK;
+  Params p;
+  const void* ins[llar::kMaxRanks];
+  void* outs[llar::kMaxRanks];
+  for (int r = 0; r < c.n; ++r) {
+    ins[r] = dst[r] >= 0 ? send[r] : nullptr;
+    outs[r] = src[r] >= 0 ? recv[r] : nullptr;
+  }
+  fill_params(c, p, ins, outs, count);
+  for (int r = 0; r < c.n; ++r) {
+    p.peer_dst[r] = dst[r];
+    p.peer_src[r] = src[r];
+  }
+  p.iters = iters;
+  p.in_stride = send_stride;
+  p.out_stride = recv_stride;
+  // units of CTA work: LL 8-byte words; sentinel 16-byte vectors of a chunk
+  int T;
+  size_t units;
+  if (proto == LLAR_PROTO_LL) {
+    T = 128;
+    units = (bytes + 7) / 8;
+  } else {
+    T = 64;
+    units = std::min(c.chunk_bytes, round_up(bytes, 16)) / 16;
+  }
+  int G = (int)std::max<size_t>(1, (units + T - 1) / T);
+  const int cap = llar::max_resident_p2p_ctas(proto, c.dtype, T);
+  if (cap <= 0) return LLAR_ERR_CUDA;
+  G = std::min(G, std::max(1, cap / c.n));
+  if (g_force_G > 0) G = g_force_G;
+  if (g_force_T > 0) T = g_force_T;
+  if (G * c.n > cap) return LLAR_ERR_OCCUPANCY;
+  G = std::min(G, kFlagsGmax);
+  p.G = G;
+  const cudaError_t err = llar::launch_p2p(proto, c.dtype, p, T, stream);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(err);
+  }
+  g_last_proto = proto;
+  g_last_G = G;
+  g_last_T = T;
+  g_last_iters = iters;
+  return LLAR_OK;
+}
+
 int run(const void* const* in, void* const* out, size_t count, int proto, int iters,
         size_t in_stride, size_t out_stride, float chain_scale, cudaStream_t stream) {
   if (!g) return LLAR_ERR_NOT_INIT;
@@ -371,7 +464,7 @@ int fill_staging(Ctx& c, cudaStream_t s) {
   ok(cudaMemsetAsync(c.base + c.sen_off, 0xFF, c.sen_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.l128_off, 0, c.l128_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.ag_off, 0, c.ag_stride * c.n, s));
-  ok(cudaMemsetAsync(c.base + c.flags_off, 0, (size_t)c.n * kFlagsGmax * 2 * 8, s));
+  ok(cudaMemsetAsync(c.base + c.flags_off, 0, (size_t)c.n * kFlagsGmax * llar::kFlagKinds * 8, s));
   // abort word only: the epoch counter at +128 keeps counting across resets
   ok(cudaMemsetAsync(c.base + c.abort_off, 0, 4, s));
   ok(cudaStreamSynchronize(s));
@@ -427,7 +520,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   c->chain_slot = round_up(c->max_bytes, kAlign);
   region(2 * c->chain_slot, &c->chain_off, &c->chain_stride);
   c->flags_off = off;
-  off += round_up((size_t)n * kFlagsGmax * 2 * 8, kAlign);
+  off += round_up((size_t)n * kFlagsGmax * llar::kFlagKinds * 8, kAlign);
   c->abort_off = off;
   off += kAlign;
   c->total = off;
@@ -491,6 +584,13 @@ int llar_reduce_scatter(const void* const* in, void* const* out, size_t count, i
 int llar_all_gather(const void* const* in, void* const* out, size_t count, int protocol, void* stream) {
   std::lock_guard<std::mutex> lk(g_mu);
   return run_segment(false, in, out, count, protocol, static_cast<cudaStream_t>(stream));
+}
+
+int llar_sendrecv(const void* const* send, void* const* recv, const int* dst, size_t count, int protocol, int iters,
+                  size_t send_stride, size_t recv_stride, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return run_p2p(send, recv, dst, count, protocol, iters, send_stride, recv_stride,
+                 static_cast<cudaStream_t>(stream));
 }
 
 int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int protocol, void* stream) {

@@ -70,6 +70,7 @@ def lib():
         "llar_allreduce_host": (c_int, [c_vp, c_vp, c_size, c_int, c_vp]),
         "llar_reduce_scatter": (c_int, [pp, pp, c_size, c_int, c_vp]),
         "llar_all_gather": (c_int, [pp, pp, c_size, c_int, c_vp]),
+        "llar_sendrecv": (c_int, [pp, pp, ctypes.POINTER(c_int), c_size, c_int, c_int, c_size, c_size, c_vp]),
         "llar_allreduce_noalloc": (c_int, [pp, pp, c_size, c_int, c_int, c_vp]),
         "llar_get_status": (c_int, [ctypes.POINTER(c_int), ctypes.POINTER(c_int), ctypes.POINTER(c_ull)]),
         "llar_reset": (c_int, [c_vp]),
@@ -191,6 +192,18 @@ def llar_all_gather(ins, outs, count, protocol="auto", stream=None):
     _check(lib().llar_all_gather(_ptr_array(ins), _ptr_array(outs), int(count),
                                  _enum(PROTOCOLS, protocol), ctypes.c_void_p(_stream(stream))),
            "llar_all_gather")
+
+
+def llar_sendrecv(sends, recvs, dst, count, protocol="auto", iters=1, send_stride=0, recv_stride=0,
+                  stream=None):
+    """recvs[dst[r]] = sends[r] for every r with dst[r] >= 0 (None: no buffer)."""
+    n = len(dst)
+    d = (ctypes.c_int * n)(*[int(v) for v in dst])
+    _check(lib().llar_sendrecv(_ptr_array([0 if t is None else t for t in sends]),
+                               _ptr_array([0 if t is None else t for t in recvs]), d, int(count),
+                               _enum(PROTOCOLS, protocol), int(iters), int(send_stride), int(recv_stride),
+                               ctypes.c_void_p(_stream(stream))),
+           "llar_sendrecv")
 
 
 def llar_allreduce_host(in_host, out_host, count, protocol="auto", stream=None):
