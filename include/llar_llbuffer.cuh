@@ -181,17 +181,17 @@ __device__ __forceinline__ u64 begin(const llar_llbuffer& b) {
   return *reinterpret_cast<volatile const u64*>(b.epoch) + 1;
 }
 // Every thread of every CTA, once, as the launch's last step: the last CTA
-// to get here (all CTAs have read the counter by then) advances it by n.
+// to get here (all CTAs have read the counter by then: each read completed
+// before its CTA counted itself) advances it by n. The next launch is
+// stream-ordered after this one, so relaxed atomics suffice.
 __device__ __forceinline__ void end(const llar_llbuffer& b, unsigned n) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     const unsigned total = gridDim.x * gridDim.y * gridDim.z;
     if (atomicAdd(b.done_count, 1u) == total - 1) {
-      atomicExch(b.done_count, 0u);
+      *reinterpret_cast<volatile unsigned*>(b.done_count) = 0u;
       volatile u64* ep = b.epoch;
       *ep = *ep + (u64)n;
-      __threadfence();
     }
   }
 }

@@ -84,23 +84,30 @@ __device__ __forceinline__ int cta_of_block(const Params& p) { return blockIdx.x
 // replayed still gets fresh epochs: every CTA reads the counter when it
 // starts (iteration e of the launch uses counter + 1 + e), and the last CTA
 // to finish, which knows that every CTA has read it, advances it by the
-// launch's iteration count.
+// launch's iteration count. A CTA's read has completed (its value is in
+// use) before the CTA counts itself finished, and the next launch is
+// stream-ordered after this one, so relaxed atomics suffice: no fence.
+// Measured per launch on B300 (128 CTAs, cooperative, graph replay): the
+// fenced version cost 1.7 us over a bare launch, the relaxed one 1.0 us.
 __device__ __forceinline__ u64 launch_epoch(const Params& p) {
   return *reinterpret_cast<volatile const u64*>(p.epoch_dev) + 1;
 }
-__device__ __forceinline__ void finish_launch(const Params& p) {
+// `counted`: whether this CTA takes part in the count; `participants`: how
+// many do. Every CTA may take part; a kernel in which rank 0's CTA c
+// consumes, in its last iteration, data that every CTA of column c produced
+// after reading the counter may count rank 0's CTAs alone (G atomics on
+// the counter word instead of N x G).
+__device__ __forceinline__ void finish_launch(const Params& p, bool counted, unsigned participants) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(p.done_count, 1u);
-    if (prev == gridDim.x - 1) {
-      atomicExch(p.done_count, 0u);
+  if (threadIdx.x == 0 && counted) {
+    if (atomicAdd(p.done_count, 1u) == participants - 1) {
+      *reinterpret_cast<volatile unsigned*>(p.done_count) = 0u;
       volatile u64* ep = p.epoch_dev;
       *ep = *ep + (u64)p.iters;
-      __threadfence();
     }
   }
 }
+__device__ __forceinline__ void finish_launch(const Params& p) { finish_launch(p, true, gridDim.x); }
 
 // One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
 // the thread pushes its unit of my data to every peer, polls the unit every
@@ -261,7 +268,10 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
       store_word8<DT>(out, w, p.count, y);
     }
   }
-  finish_launch(p);
+  // every thread of rank 0's CTA c read, in the last iteration, a line that
+  // the same thread of each peer CTA c published after reading the counter
+  // (peer threads without words do nothing with it)
+  finish_launch(p, r == 0, (unsigned)p.G);
 }
 
 // ====================================================== sentinel one-shot

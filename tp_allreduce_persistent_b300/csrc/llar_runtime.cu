@@ -61,7 +61,7 @@ Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
 int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0;
-constexpr size_t kBulkMinBytes = 1u << 20;  // per rank: TMA bulk path from 1 MiB
+size_t g_bulk_min_bytes = 1u << 20;  // per rank: TMA bulk path from here (LLAR_BULK_MIN_BYTES)
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
@@ -434,7 +434,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     case LLAR_PROTO_LL128_ATOMIC: err = llar::launch_ll128(c.dtype, p, T, stream); break;
     case LLAR_PROTO_FIXED_ONESHOT: err = llar::launch_fixed_oneshot(c.dtype, p, T, stream); break;
     default:
-      if (!chain && g_bulk && bytes >= kBulkMinBytes && g_force_G == 0) {
+      if (!chain && g_bulk && bytes >= g_bulk_min_bytes && g_force_G == 0) {
         // as many CTAs as the ring's shared memory lets each SM hold
         const int per_sm = std::max(1, (int)((227u << 10) / llar::bulk_smem_bytes(c.n)));
         p.G = std::max(1, per_sm * c.sms / c.n);
@@ -495,6 +495,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_cluster = (int)env_size("LLAR_CLUSTER", (size_t)g_cluster);
   g_log = (int)env_size("LLAR_LOG", (size_t)g_log);
   g_bulk = (int)env_size("LLAR_BULK", (size_t)g_bulk);
+  g_bulk_min_bytes = env_size("LLAR_BULK_MIN_BYTES", g_bulk_min_bytes);
   g_spread = (int)env_size("LLAR_SPREAD_SMEM", (size_t)g_spread);
 
   cudaError_t err = cudaGetDevice(&c->dev);
