@@ -179,7 +179,7 @@ void llar_set_timeout_ns(unsigned long long ns);
 int llar_set_launch(int ctas_per_rank, int threads);
 
 /* Sentinel chunk size in bytes per rank (multiple of 16, at most 64 KiB;
- * default 8 KiB): each call moves ceil(bytes / chunk) chunks through the
+ * default 64 KiB): each call moves ceil(bytes / chunk) chunks through the
  * two staging slots of every peer (technique 3). */
 int llar_set_sentinel_chunk(size_t bytes);
 
@@ -220,7 +220,13 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
                 size_t* line_bytes, size_t* payload_elems_per_line,
                 size_t* staging_bytes_per_rank);
 
-/* The protocol LLAR_PROTO_AUTO picks for this size (host-only). */
+/* The protocol LLAR_PROTO_AUTO picks for this rank count and size
+ * (host-only). Measured per rank count on a B300 (one call per launch):
+ * LL up to 256 KiB (2 ranks), 128 KiB (3-4), 64 KiB (5), 32 KiB (6-8);
+ * then the direct-read one-shot up to 1 MiB (2-3), 512 KiB (4), 256 KiB
+ * (5); then the direct-read two-shot, which streams through shared memory
+ * with TMA bulk copies from 1 MiB (3-4), 512 KiB (5) or 32 KiB (6-8), and
+ * never for 2 ranks. LLAR_PROTO (environment) forces a protocol. */
 int llar_select_protocol(int nranks, int dtype, size_t count);
 
 /* Epoch the next launch will use for its first AllReduce; strictly

@@ -177,8 +177,15 @@ static __device__ __noinline__ void fail(const llar_llbuffer& b, int rank, u64 E
 __device__ __forceinline__ bool aborted(const llar_llbuffer& b) { return ld_relaxed_u32(b.abort_word) != 0; }
 
 // ---------------------------------------------------------------- epochs
+// When the kernel was launched as a programmatic dependent of the previous
+// kernel in its stream, begin() first waits for that kernel to complete
+// (griddepcontrol.wait; a no-op otherwise), then lets the next launch be
+// scheduled early.
 __device__ __forceinline__ u64 begin(const llar_llbuffer& b) {
-  return *reinterpret_cast<volatile const u64*>(b.epoch) + 1;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const u64 e = *reinterpret_cast<volatile const u64*>(b.epoch) + 1;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  return e;
 }
 // Every thread of every CTA, once, as the launch's last step: the last CTA
 // to get here (all CTAs have read the counter by then: each read completed

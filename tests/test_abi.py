@@ -51,6 +51,24 @@ def test_layout_constants(dtype):
     assert lb == 16 and pl * e == 16 and st == 2 * 8 * 8192
 
 
+@pytest.mark.parametrize("n", range(2, 9))
+def test_protocol_selection_per_rank_count(n):
+    kib = 512  # bf16 elements per KiB
+    want = {2: (256, 1024), 3: (128, 1024), 4: (128, 512), 5: (64, 256), 6: (32, 32), 7: (32, 32), 8: (32, 32)}[n]
+    ll_max, one_max = want
+    order = ["ll", "fixed_oneshot", "fixed_twoshot"]
+    last = 0
+    for k in (2, 4, 8, 16, 32, 33, 64, 65, 128, 129, 256, 257, 512, 513, 1024, 1025, 4096):
+        p = llar.llar_select_protocol(n, "bf16", k * kib)
+        expect = "ll" if k <= ll_max else ("fixed_oneshot" if one_max is None or k <= one_max else "fixed_twoshot")
+        assert p == expect, (n, k, p)
+        assert order.index(p) >= last
+        last = order.index(p)
+    # the rule is in bytes: fp32 reaches each threshold at half the elements
+    assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4) == "ll"
+    assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4 + 1) != "ll"
+
+
 def test_protocol_selection_is_monotone_in_size():
     order = ["ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"]
     last = 0

@@ -150,3 +150,19 @@ def test_chain_ll128_stepwise(dtype):
             ok, err, rel = orc.compare_atomic(got[e], orc.allreduce(cur, dtype), cur, dtype)
             assert ok, (e, err, rel)
             cur = orc.chain_next(got[e], scale, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("n", [5, 6, 7, 8])
+def test_two_shot_tma_path_at_small_sizes(n, dtype):
+    # 6-8 ranks stream the two-shot through shared memory with TMA bulk copies
+    # from 32 KiB per rank, 5 ranks from 512 KiB: ragged and tile-crossing sizes
+    e = inputs.ELEM_BYTES[dtype]
+    with context(n, dtype, 2 << 20):
+        for nbytes in (32 << 10, (48 << 10) + 6, 64 << 10, (200 << 10) + 2, 512 << 10, (1 << 20) + 14):
+            count = nbytes // e
+            x = inputs.normal(n, count, dtype, seed=count + n)
+            got = allreduce(x, dtype, "fixed_twoshot")
+            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype)), count
+            got_auto = allreduce(x, dtype, "auto")
+            assert np.array_equal(got_auto, orc.allreduce(inputs.bits_of(x), dtype)), count

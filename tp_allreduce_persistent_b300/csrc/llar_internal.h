@@ -53,6 +53,7 @@ struct Params {
   int G;                      // CTAs per rank
   int clustered;              // launch in clusters of nranks blocks (one CTA per rank, same range)
   int spread_smem;            // dynamic shared memory reserved only to keep one CTA per SM
+  int pdl;                    // launch as a programmatic dependent of the previous kernel
   int iters;
   int chain;                  // 1: next input = RNE(chain_scale * output)
   float chain_scale;

@@ -89,8 +89,16 @@ __device__ __forceinline__ int cta_of_block(const Params& p) { return blockIdx.x
 // stream-ordered after this one, so relaxed atomics suffice: no fence.
 // Measured per launch on B300 (128 CTAs, cooperative, graph replay): the
 // fenced version cost 1.7 us over a bare launch, the relaxed one 1.0 us.
+// A launch made as a programmatic dependent of the previous kernel in the
+// stream (p.pdl) may be scheduled before that kernel ends; griddepcontrol
+// .wait holds it until the previous kernel has completed and its memory
+// is visible (a no-op otherwise), and launch_dependents lets the next
+// launch be scheduled early in turn.
 __device__ __forceinline__ u64 launch_epoch(const Params& p) {
-  return *reinterpret_cast<volatile const u64*>(p.epoch_dev) + 1;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const u64 e = *reinterpret_cast<volatile const u64*>(p.epoch_dev) + 1;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  return e;
 }
 // `counted`: whether this CTA takes part in the count; `participants`: how
 // many do. Every CTA may take part; a kernel in which rank 0's CTA c
@@ -294,9 +302,12 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
   const bool full = (p.count % PER16) == 0;  // no partial vector at the end
   const unsigned CV = (unsigned)p.sen_chunk_vecs;
   const unsigned nchunks = (NV + CV - 1) / CV;
-  const unsigned per = (CV + p.G - 1) / p.G;
-  const unsigned j0 = min(CV, (unsigned)c * per);
-  const unsigned j1 = min(CV, j0 + per);
+  // the CTAs split the part of a chunk the message uses (a message shorter
+  // than the chunk would otherwise land on the first CTAs only)
+  const unsigned CU = min(CV, NV);
+  const unsigned per = (CU + p.G - 1) / p.G;
+  const unsigned j0 = min(CU, (unsigned)c * per);
+  const unsigned j1 = min(CU, j0 + per);
   const size_t src_stride = (size_t)CV * 16;
   const size_t slot_stride = (size_t)N * src_stride;
   const bool injected = INJ && (p.inject_rank == r);
@@ -394,7 +405,9 @@ template <int DT, int N, bool CHAIN, bool INJ>
 __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_sentinel<DT, N, CHAIN, INJ>(p, epoch0);
-  finish_launch(p);
+  // rank 0's thread j took, in the last chunk it handled, the vector that
+  // thread j of each peer CTA pushed after reading the counter
+  finish_launch(p, rank_of_block(p) == 0, (unsigned)p.G);
 }
 
 // ======================================================= LL128 two-shot
@@ -618,7 +631,11 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_ll128<DT>(p, epoch0);
-  finish_launch(p);
+  // rank 0's CTA c waited for every contribution to its own lines and for
+  // every other owner's AllGather lines of its range, which each owner sent
+  // only after all contributions to them: every working thread of column c
+  // had read the counter
+  finish_launch(p, rank_of_block(p) == 0, (unsigned)p.G);
 }
 
 // ==================================================== fixed-order paths
@@ -1264,8 +1281,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_sentinel(const Params p) {
   const size_t NV = (p.count * Fmt<DT>::kBytes + 15) / 16;
   const unsigned CV = (unsigned)p.sen_chunk_vecs;
   const unsigned nchunks = (unsigned)((NV + CV - 1) / CV);
-  const unsigned per = (CV + p.G - 1) / p.G;
-  const unsigned j0 = min(CV, (unsigned)c * per), j1 = min(CV, j0 + per);
+  const unsigned CU = (unsigned)min((size_t)CV, NV);  // vectors of a chunk the message uses
+  const unsigned per = (CU + p.G - 1) / p.G;
+  const unsigned j0 = min(CU, (unsigned)c * per), j1 = min(CU, j0 + per);
   const size_t src_stride = (size_t)CV * 16;
   const size_t slot_stride = (size_t)N * src_stride;
   const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
@@ -1338,6 +1356,11 @@ static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream
     at[na].val.cooperative = 1;
     ++na;
   }
+  if (p.pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if (p.clustered) {
     at[na].id = cudaLaunchAttributeClusterDimension;
     at[na].val.clusterDim.x = p.nranks;
@@ -1354,7 +1377,7 @@ static cudaError_t launch_kernel(const void* k, const Params& p, int threads, cu
     const cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.spread_smem);
     if (err != cudaSuccess) return err;
   }
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   cudaLaunchConfig_t cfg = launch_config(p, threads, s, coop, at);
   void* args[] = {const_cast<Params*>(&p)};
   return cudaLaunchKernelExC(&cfg, k, args);
@@ -1483,7 +1506,7 @@ cudaError_t launch_fixed_twoshot_bulk(int dtype, const Params& p, int threads, c
   const int smem = (int)bulk_smem_bytes(p.nranks);
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];  // cooperative, programmatic dependency, cluster
   cudaLaunchConfig_t cfg = launch_config(p, threads, s, false, at);
   cfg.dynamicSmemBytes = smem;
   void* args[] = {const_cast<Params*>(&p)};
@@ -1516,7 +1539,7 @@ int max_resident_ctas(int proto, int dtype, int nranks, int threads, bool cluste
       cudaGetLastError();
       return 0;
     }
-    cudaLaunchAttribute at[2];
+    cudaLaunchAttribute at[3];  // cooperative, programmatic dependency, cluster
     cudaLaunchConfig_t cfg = launch_config(p, threads, 0, false, at);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess) {

@@ -433,17 +433,21 @@ int sm_count() {
   return sms;
 }
 
+// Cooperative (CTAs wait on one another), and a programmatic dependent of
+// the previous kernel in the stream: llb::begin() waits for it.
 cudaError_t launch_coop(const void* kernel, int blocks, int threads, size_t smem, cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeCooperative;
   at[0].val.cooperative = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 

@@ -20,7 +20,7 @@ using llar::Params;
 constexpr size_t kAlign = 256;
 constexpr size_t kDefaultLLCap = 1u << 20;      // LL messages up to 1 MiB per rank
 constexpr size_t kDefaultLL128Cap = 64u << 20;  // LL128 messages up to 64 MiB per rank
-constexpr size_t kDefaultChunk = 8u << 10;      // sentinel chunk: 8 KiB per rank
+constexpr size_t kDefaultChunk = 64u << 10;     // sentinel chunk per rank: every chunk costs a round trip and a fence
 constexpr size_t kMaxChunk = 64u << 10;         // largest sentinel chunk
 constexpr int kFlagsGmax = 1024;                // CTAs per rank the chain flags can address
 
@@ -60,8 +60,8 @@ std::mutex g_mu;
 Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
-int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0;
-size_t g_bulk_min_bytes = 1u << 20;  // per rank: TMA bulk path from here (LLAR_BULK_MIN_BYTES)
+int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0, g_pdl = 1;  // LLAR_PDL=0: plain stream order
+size_t g_bulk_min_bytes = 0;  // LLAR_BULK_MIN_BYTES: TMA two-shot threshold for every N (0: per N)
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
 
@@ -87,6 +87,29 @@ size_t ll128_lines_for(size_t count, int n, int dtype) {
 bool valid_dtype(int d) { return d == LLAR_F32 || d == LLAR_F16 || d == LLAR_BF16; }
 bool valid_proto(int p) { return p >= LLAR_PROTO_AUTO && p <= LLAR_PROTO_FIXED_TWOSHOT; }
 
+// AUTO, per rank count. Measured on a B300 (bf16, one call per launch,
+// replayed from a CUDA graph, 2 KiB .. 4 MiB per rank): LL is fastest up
+// to ll_max, the direct-read one-shot up to oneshot_max, the direct-read
+// two-shot above, streamed through shared memory with TMA bulk copies
+// from bulk_min (with 6 or more ranks already from 32 KiB: 3.3 us against
+// 3.5-6.2 us for the other paths at 64 KiB).
+struct AutoRule {
+  size_t ll_max, oneshot_max, bulk_min;
+};
+AutoRule auto_rule(int n) {
+  constexpr size_t K = 1024, M = 1024 * 1024, kNever = ~size_t(0);
+  switch (n) {
+    case 2: return {256 * K, 1 * M, kNever};
+    case 3: return {128 * K, 1 * M, 1 * M};
+    case 4: return {128 * K, 512 * K, 1 * M};
+    case 5: return {64 * K, 256 * K, 512 * K};
+    default: return {32 * K, 32 * K, 32 * K};
+  }
+}
+size_t bulk_min_bytes(int n) {
+  return g_bulk_min_bytes ? g_bulk_min_bytes : auto_rule(n).bulk_min;
+}
+
 int select_protocol(int n, int dtype, size_t count) {
   const char* force = std::getenv("LLAR_PROTO");
   if (force && *force) {
@@ -94,12 +117,9 @@ int select_protocol(int n, int dtype, size_t count) {
     if (f >= LLAR_PROTO_LL && f <= LLAR_PROTO_FIXED_TWOSHOT) return f;
   }
   const size_t bytes = count * elem_bytes(dtype);
-  (void)n;
-  // measured on a B300 with 8 ranks (persistent per-AllReduce time): LL is
-  // fastest up to 64 KiB per rank, direct-read one-shot from there to
-  // 256 KiB, direct-read two-shot beyond
-  if (bytes <= (64u << 10)) return LLAR_PROTO_LL;
-  if (bytes <= (256u << 10)) return LLAR_PROTO_FIXED_ONESHOT;
+  const AutoRule rule = auto_rule(n);
+  if (bytes <= rule.ll_max) return LLAR_PROTO_LL;
+  if (bytes <= rule.oneshot_max) return LLAR_PROTO_FIXED_ONESHOT;
   return LLAR_PROTO_FIXED_TWOSHOT;
 }
 
@@ -125,10 +145,12 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
     g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)cap);
   } else if (proto == LLAR_PROTO_SENTINEL) {
     // every vector costs N-1 pushes, polls and resets plus a fence per
-    // chunk: spread the chunk thinly over as many SMs as possible
-    t = 64;
-    const size_t want = (units + t - 1) / t;
-    g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)std::max(1, 2 * c.sms / n));
+    // chunk: spread the chunk thinly over as many SMs as possible (measured,
+    // 8 ranks x 2 KiB: 2 CTAs of 64 threads per rank 4.1 us, 16 of 32
+    // threads 2.9 us)
+    t = units <= 512 ? 32 : 64;
+    const size_t want = std::max<size_t>((units + t - 1) / t, 16);
+    g = (int)std::min<size_t>(want, (size_t)std::max(1, 2 * c.sms / n));
     if (want > (size_t)g) t = (int)std::min<size_t>(llar::kMaxThreads, round_up((units + g - 1) / g, 32));
   } else {
     const size_t want = (units + t - 1) / t;
@@ -212,6 +234,7 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
   p.inject_mode = g_inject_mode;
   p.abort_flag = reinterpret_cast<unsigned*>(c.base + c.abort_off);
   p.status = c.status_dev;
+  p.pdl = g_pdl;
 }
 
 // ReduceScatter (rs) or AllGather over segments of a count-element vector.
@@ -434,7 +457,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     case LLAR_PROTO_LL128_ATOMIC: err = llar::launch_ll128(c.dtype, p, T, stream); break;
     case LLAR_PROTO_FIXED_ONESHOT: err = llar::launch_fixed_oneshot(c.dtype, p, T, stream); break;
     default:
-      if (!chain && g_bulk && bytes >= g_bulk_min_bytes && g_force_G == 0) {
+      if (!chain && g_bulk && bytes >= bulk_min_bytes(c.n) && g_force_G == 0) {
         // as many CTAs as the ring's shared memory lets each SM hold
         const int per_sm = std::max(1, (int)((227u << 10) / llar::bulk_smem_bytes(c.n)));
         p.G = std::max(1, per_sm * c.sms / c.n);
@@ -495,6 +518,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_cluster = (int)env_size("LLAR_CLUSTER", (size_t)g_cluster);
   g_log = (int)env_size("LLAR_LOG", (size_t)g_log);
   g_bulk = (int)env_size("LLAR_BULK", (size_t)g_bulk);
+  g_pdl = (int)env_size("LLAR_PDL", (size_t)g_pdl);
   g_bulk_min_bytes = env_size("LLAR_BULK_MIN_BYTES", g_bulk_min_bytes);
   g_spread = (int)env_size("LLAR_SPREAD_SMEM", (size_t)g_spread);
 
