@@ -362,8 +362,8 @@ def configs_leg(llar, torch, dev, stream):
 
     out["single_call_graph_8ranks_16KiB_bf16_us"] = {
         "allreduce": {p: graph_call_us("allreduce", p) for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")},
-        "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "fixed_oneshot")},
-        "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "fixed_oneshot")},
+        "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "sentinel", "ll128", "fixed_oneshot")},
+        "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "sentinel", "fixed_oneshot")},
     }
     # point-to-point hand-off along a ring of 8 ranks (every rank sends 16 KiB
     # bf16 to the next), back-to-back transfers in one launch

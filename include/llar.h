@@ -117,15 +117,22 @@ int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
  * in[r]: count elements; out[r]: the S (or fewer) elements of segment r,
  * = sum over q of in[q][segment r], added in rank order in float32 and
  * rounded once. protocol: LLAR_PROTO_LL (flag-in-data lines),
- * LLAR_PROTO_FIXED_ONESHOT (direct reads) or LLAR_PROTO_AUTO; others give
- * LLAR_ERR_UNSUPPORTED. One collective per launch. */
+ * LLAR_PROTO_SENTINEL (raw vectors into all-ones slots; a segment must fit
+ * one sentinel chunk, else LLAR_ERR_TOO_LARGE), LLAR_PROTO_FIXED_ONESHOT
+ * (direct reads), LLAR_PROTO_LL128_ATOMIC (technique 4's atomic
+ * reductions into 128-byte lines with a count flag: element-type
+ * additions in arrival order, within (N-1) ulp of the sum of |x|) or
+ * LLAR_PROTO_AUTO; others give LLAR_ERR_UNSUPPORTED. One collective per
+ * launch. */
 int llar_reduce_scatter(const void* const* in, void* const* out, size_t count,
                         int protocol, void* stream);
 
 /* AllGather, the second half of the two-shot AllReduce (same table,
  * All-Gather row: each rank collects every rank's segment). in[r]: segment
  * r of a count-element vector (segments as for llar_reduce_scatter);
- * out[r]: all count elements, segment q at offset q*S. Same protocols. */
+ * out[r]: all count elements, segment q at offset q*S. Protocols as for
+ * llar_reduce_scatter except LLAR_PROTO_LL128_ATOMIC (nothing is added in
+ * an AllGather: LLAR_ERR_UNSUPPORTED). */
 int llar_all_gather(const void* const* in, void* const* out, size_t count,
                     int protocol, void* stream);
 

@@ -1,8 +1,12 @@
 """ReduceScatter and AllGather through the C ABI against the oracle.
 
-Both are fixed-order (rank-order float32 sums, one rounding; copies are
-copies), so results must match bit for bit, including ragged and empty
-segments. AllGather(ReduceScatter(x)) must equal AllReduce(x).
+LL, sentinel and direct-read variants are fixed-order (rank-order float32
+sums, one rounding; copies are copies), so results must match bit for bit,
+including ragged and empty segments. The LL128 ReduceScatter adds with
+atomics in the element type: within (N-1) ulp of sum |x|, exact on
+integers. AllGather(ReduceScatter(x)) must equal AllReduce(x). Sentinel
+variants move a segment in one chunk (larger segments are refused) and
+leave their slots all-ones; LL128 leaves its lines zero.
 """
 
 import numpy as np
@@ -23,32 +27,65 @@ def _seg_len(count, n):
     return -(-count // n) if count else 0
 
 
-@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot"])
+def _fits(proto, count, n, dtype):
+    # sentinel segments travel in one 64 KiB chunk
+    return proto != "sentinel" or -(-_seg_len(count, n) * inputs.ELEM_BYTES[dtype] // 16) * 16 <= 65536
+
+
+@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot", "sentinel", "ll128"])
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("n", [2, 3, 5, 8])
 def test_reduce_scatter(proto, dtype, n):
     with context(n, dtype, 1 << 20):
         for count in COUNTS:
-            x = inputs.normal(n, count, dtype, seed=count + n)
+            x = inputs.normal(n, count, dtype, seed=count + n, exclude_sentinel=True)
             ins = device_inputs(x)
             seg = _seg_len(count, n)
             outs = filled_outputs(n, max(seg, 1), dtype)
+            if not _fits(proto, count, n, dtype):
+                with pytest.raises(llar.LlarError) as ei:
+                    llar.llar_reduce_scatter(ins, outs, count, proto)
+                assert ei.value.code == llar.ERR_TOO_LARGE
+                continue
             llar.llar_reduce_scatter(ins, outs, count, proto)
             torch.cuda.synchronize()
             assert llar.llar_get_status()[0] == llar.OK
-            want = orc.reduce_scatter(inputs.bits_of(x), dtype)
+            xb = inputs.bits_of(x)
+            want = orc.reduce_scatter(xb, dtype)
             for s in range(n):
                 got = inputs.bits_of(outs[s])[: len(want[s])]
-                assert np.array_equal(got, want[s]), (count, s)
+                if proto == "ll128":
+                    lo, hi = orc.shard_bounds(count, n, s)
+                    ok, err, rel = orc.compare_atomic(got[None], want[s][None], xb[:, lo:hi], dtype)
+                    assert ok, (count, s, err, rel)
+                else:
+                    assert np.array_equal(got, want[s]), (count, s)
 
 
-@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot"])
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_reduce_scatter_ll128_integers_exact(n):
+    for dtype, lo, hi in (("fp32", -64, 64), ("fp16", -64, 64), ("bf16", -32, 32)):
+        with context(n, dtype, 1 << 20):
+            for count in (100, 4097, 65539):
+                x = inputs.integers(n, count, dtype, seed=count, lo=lo, hi=hi)
+                ins = device_inputs(x)
+                outs = filled_outputs(n, _seg_len(count, n), dtype)
+                llar.llar_reduce_scatter(ins, outs, count, "ll128")
+                torch.cuda.synchronize()
+                want = orc.reduce_scatter(inputs.bits_of(x), dtype)
+                for s in range(n):
+                    assert np.array_equal(inputs.bits_of(outs[s])[: len(want[s])], want[s]), (dtype, count, s)
+
+
+@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot", "sentinel"])
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("n", [2, 3, 5, 8])
 def test_all_gather(proto, dtype, n):
     with context(n, dtype, 1 << 20):
         for count in COUNTS:
-            full = inputs.normal(1, count, dtype, seed=count * 3 + n)[0]
+            if not _fits(proto, count, n, dtype):
+                continue
+            full = inputs.normal(1, count, dtype, seed=count * 3 + n, exclude_sentinel=True)[0]
             segs = [full[lo:hi] for lo, hi in (orc.shard_bounds(count, n, s) for s in range(n))]
             ins = []
             for sg in segs:
@@ -64,28 +101,55 @@ def test_all_gather(proto, dtype, n):
             assert np.array_equal(got, want), count
 
 
-@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot"])
-def test_all_gather_of_reduce_scatter_is_allreduce(proto):
+@pytest.mark.parametrize("rs,ag", [("ll", "ll"), ("fixed_oneshot", "fixed_oneshot"), ("sentinel", "sentinel"),
+                                   ("ll128", "ll"), ("sentinel", "ll"), ("ll", "sentinel")])
+def test_all_gather_of_reduce_scatter_is_allreduce(rs, ag):
     n, dtype = 8, "bf16"
     with context(n, dtype, 1 << 20):
         for count in (8192, 8195):
-            x = inputs.normal(n, count, dtype, seed=count, scale=0.02)
+            x = inputs.normal(n, count, dtype, seed=count, scale=0.02, exclude_sentinel=True)
             ins = device_inputs(x)
             seg = _seg_len(count, n)
             mid = filled_outputs(n, seg, dtype)
             outs = filled_outputs(n, count, dtype)
-            llar.llar_reduce_scatter(ins, mid, count, proto)
-            llar.llar_all_gather(mid, outs, count, proto)
+            llar.llar_reduce_scatter(ins, mid, count, rs)
+            llar.llar_all_gather(mid, outs, count, ag)
             torch.cuda.synchronize()
             got = np.stack([inputs.bits_of(o) for o in outs])
-            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
+            xb = inputs.bits_of(x)
+            if rs == "ll128":
+                assert orc.compare_atomic(got, orc.allreduce(xb, dtype), xb, dtype)[0]
+            else:
+                assert np.array_equal(got, orc.allreduce(xb, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_segment_staging_state_after_use(dtype):
+    from test_gpu_protocol import staging_bytes
+    n = 8
+    with context(n, dtype, 1 << 20):
+        for count in (1000, 8195, 32768):
+            x = inputs.normal(n, count, dtype, seed=count, exclude_sentinel=True)
+            ins = device_inputs(x)
+            seg = _seg_len(count, n)
+            llar.llar_reduce_scatter(ins, filled_outputs(n, seg, dtype), count, "sentinel")
+            segs = [t[:seg].contiguous() for t in ins]
+            llar.llar_all_gather(segs, filled_outputs(n, count, dtype), count, "sentinel")
+            torch.cuda.synchronize()
+            for buf in staging_bytes("sentinel", n):
+                assert np.all(buf == 0xFF)
+            llar.llar_reduce_scatter(ins, filled_outputs(n, seg, dtype), count, "ll128")
+            torch.cuda.synchronize()
+            for buf in staging_bytes("ll128", n):
+                assert np.all(buf == 0)
 
 
 def test_segment_collectives_reject_other_protocols():
     with context(4, "fp32", 1 << 12):
         ins = device_inputs(inputs.normal(4, 64, "fp32", seed=1))
         outs = filled_outputs(4, 64, "fp32")
-        for proto in ("sentinel", "ll128", "fixed_twoshot"):
+        for fn, proto in ((llar.llar_reduce_scatter, "fixed_twoshot"), (llar.llar_all_gather, "fixed_twoshot"),
+                          (llar.llar_all_gather, "ll128")):
             with pytest.raises(llar.LlarError) as ei:
-                llar.llar_reduce_scatter(ins, outs, 64, proto)
+                fn(ins, outs, 64, proto)
             assert ei.value.code == llar.ERR_UNSUPPORTED

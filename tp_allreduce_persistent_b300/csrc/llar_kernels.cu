@@ -1154,6 +1154,262 @@ __device__ __forceinline__ void body_ag_fixed(const Params& p, const u64 E) {
   }
 }
 
+// Element i of segment s of a rank buffer, as raw bits (0 past the end).
+template <int DT>
+__device__ __forceinline__ unsigned seg_elem(const char* base, size_t lo, size_t len, size_t i) {
+  return i < len ? Fmt<DT>::load(base, lo + i) : 0u;
+}
+// 16-byte vector j of a segment [lo, lo + len) of a buffer: elements
+// [j * PER16, (j + 1) * PER16), zero past the end; one vector load when the
+// segment starts on a 16-byte boundary and the vector is whole.
+template <int DT>
+__device__ __forceinline__ uint4 seg_vec(const char* base, size_t lo, size_t len, size_t j) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  const size_t first = j * PER16;
+  if ((lo * Fmt<DT>::kBytes) % 16 == 0 && first + PER16 <= len)
+    return ld_stream_v4(base + (lo + first) * Fmt<DT>::kBytes);
+  unsigned w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int k = 0; k < PER16; ++k) {
+    const unsigned b = seg_elem<DT>(base, lo, len, first + k);
+    const int word = (k * Fmt<DT>::kBytes) / 4;
+    w[word] = Fmt<DT>::kBytes == 4 ? b : word_set<DT>(w[word], k & 1, b);
+  }
+  return u4(w);
+}
+template <int DT>
+__device__ __forceinline__ void seg_store(char* base, size_t lo, size_t len, size_t j, uint4 v) {
+  constexpr int PER16 = 16 / Fmt<DT>::kBytes;
+  const size_t first = j * PER16;
+  if ((lo * Fmt<DT>::kBytes) % 16 == 0 && first + PER16 <= len) {
+    st_v4(base + (lo + first) * Fmt<DT>::kBytes, v);
+    return;
+  }
+  const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < PER16; ++k)
+    if (first + k < len)
+      Fmt<DT>::store(base, lo + first + k, word_elem<DT>(w[(k * Fmt<DT>::kBytes) / 4], Fmt<DT>::kBytes == 4 ? 0 : (k & 1)));
+}
+
+// ReduceScatter over LL128 lines (technique 4's first half): every rank
+// adds its part of segment s into owner s's lines with vector reductions
+// in the element type, then, after a fence, counts itself on each line;
+// owner r waits for count N, writes its segment and zeroes the lines.
+// Atomic: the order of the additions is not fixed.
+template <int DT>
+__device__ __forceinline__ void body_rs_ll128(const Params& p, const u64 E) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int V = 16 / EB;    // elements per lane
+  constexpr int P = 128 / EB - 1;
+  const int N = p.nranks;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t seg = (count + N - 1) / N;
+  const size_t L = (seg + P - 1) / P;
+  const size_t Lc = (L + p.G - 1) / p.G;
+  const size_t l0 = min(L, (size_t)c * Lc);
+  const size_t nl = min(L, l0 + Lc) - l0;
+  const size_t items = (size_t)N * nl * kLL128Lanes;
+  const size_t T = blockDim.x;
+  const int slot = (int)(E & 1);
+  const size_t line_slot = p.l128_lines * (size_t)kLL128Line;
+  const unsigned one_bits = Fmt<DT>::from_f(1.0f);
+  const unsigned n_bits = Fmt<DT>::from_f((float)N);
+  const unsigned flag_mask = (EB == 4) ? 0xFFFFFFFFu : 0xFFFFu;
+  const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  const char* src = p.in[r];
+  if (!skip)
+    for (size_t i = threadIdx.x; i < items; i += T) {
+      const int s = (int)(i / (nl * kLL128Lanes));
+      const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+      const size_t l = l0 + rem / kLL128Lanes;
+      const int j = (int)(rem % kLL128Lanes);
+      size_t lo, hi;
+      segment_of(count, N, s, lo, hi);
+      unsigned w[4] = {0u, 0u, 0u, 0u};
+      bool any = false;
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int pos = j * V + k;
+        const size_t sl = l * P + (size_t)pos - 1;
+        if (pos >= 1 && sl < hi - lo) {
+          const unsigned b = Fmt<DT>::load(src, lo + sl);
+          const int word = (k * EB) / 4;
+          w[word] = EB == 4 ? b : word_set<DT>(w[word], k & 1, b);
+          any = true;
+        }
+      }
+      if (any) red_add_v4<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line + j * 16, w);
+    }
+  __syncwarp();
+  fence_gpu();  // every data reduction of this warp before its counts
+  if (!skip)
+    for (size_t i = threadIdx.x; i < items; i += T) {
+      if ((i % kLL128Lanes) != 0) continue;
+      const int s = (int)(i / (nl * kLL128Lanes));
+      const size_t l = l0 + (i - (size_t)s * nl * kLL128Lanes) / kLL128Lanes;
+      red_add_flag<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line, one_bits);
+    }
+  // owner r: my lines [l0, l0 + nl), 8 lanes each
+  size_t lo, hi;
+  segment_of(count, N, r, lo, hi);
+  char* const my_lines = p.l128 + (size_t)r * p.l128_stride + slot * line_slot;
+  bool failed = false;
+  const size_t mine = nl * kLL128Lanes;
+  for (size_t base = 0; base < mine; base += T) {  // warp-uniform trip count
+    const size_t i = base + threadIdx.x;
+    const bool active = i < mine;
+    const size_t l = l0 + i / kLL128Lanes;
+    const int j = (int)(i % kLL128Lanes);
+    char* line = my_lines + l * kLL128Line;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (active && !failed) {
+      Waiter wt;
+      while ((ld_acquire_u32(line) & flag_mask) != n_bits)
+        if (wt.expired(p)) {
+          report_timeout(p, r, c, E);
+          failed = true;
+          break;
+        }
+      if (!failed) v = ld_relaxed_v4(line + j * 16);
+    }
+    __syncwarp();  // all lanes of the line have read before any zeroing
+    if (active && !failed) {
+      st_relaxed_v4(line + j * 16, make_uint4(0, 0, 0, 0));
+      const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int pos = j * V + k;
+        const size_t sl = l * P + (size_t)pos - 1;
+        if (pos >= 1 && sl < hi - lo) Fmt<DT>::store(p.out[r], sl, word_elem<DT>(w[(k * EB) / 4], EB == 4 ? 0 : (k & 1)));
+      }
+    }
+  }
+}
+
+// ReduceScatter and AllGather over sentinel slots, one chunk per launch
+// (the host checks that a segment fits a chunk; the launch boundary orders
+// slot reuse): vector j of a segment travels raw into the receiver's slot
+// [0][sender][j], which holds the all-ones pattern until it lands; the
+// receiver polls until no element is the pattern, then writes the pattern
+// back.
+template <int DT, int N>
+__device__ __forceinline__ bool sen_take(const Params& p, char* cell, int r, int c, u64 E, uint4& x) {
+  Waiter wt;
+  while (true) {
+    x = ld_relaxed_v4(cell);
+    if (!has_sentinel<DT>(x)) break;
+    if (wt.expired(p)) {
+      report_timeout(p, r, c, E);
+      return false;
+    }
+  }
+  st_relaxed_v4(cell, make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu));
+  return true;
+}
+
+template <int DT, int N>
+__device__ __forceinline__ void body_rs_sentinel(const Params& p, const u64 E) {
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t S = (count + N - 1) / N;
+  const size_t VS = (S * Fmt<DT>::kBytes + 15) / 16;  // vectors of the longest segment
+  const size_t per = (VS + p.G - 1) / p.G;
+  const size_t j0 = min(VS, (size_t)c * per), j1 = min(VS, j0 + per);
+  const size_t src_stride = (size_t)p.sen_chunk_vecs * 16;
+  const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    if (!skip)
+#pragma unroll
+      for (int s = 0; s < N; ++s) {
+        if (s == r) continue;
+        size_t lo, hi;
+        segment_of(count, N, s, lo, hi);
+        if (j * 16 >= (hi - lo) * Fmt<DT>::kBytes) continue;
+        st_relaxed_v4(p.sen + (size_t)s * p.sen_stride + (size_t)r * src_stride + j * 16,
+                      seg_vec<DT>(p.in[r], lo, hi - lo, j));
+      }
+  }
+  size_t lo, hi;
+  segment_of(count, N, r, lo, hi);
+  const size_t len = hi - lo;
+  for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    if (j * 16 >= len * Fmt<DT>::kBytes) break;
+    float acc[16 / Fmt<DT>::kBytes];
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      uint4 x;
+      if (q == r) x = seg_vec<DT>(p.in[r], lo, len, j);
+      else if (!sen_take<DT, N>(p, p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride + j * 16, r, c, E, x))
+        return;
+      const unsigned w4[4] = {x.x, x.y, x.z, x.w};
+      acc_words<DT, 4>(acc, w4, q == 0);
+    }
+    unsigned y[4];
+    round_words<DT, 4>(acc, y);
+    seg_store<DT>(p.out[r], 0, len, j, u4(y));
+  }
+}
+
+template <int DT, int N>
+__device__ __forceinline__ void body_ag_sentinel(const Params& p, const u64 E) {
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t S = (count + N - 1) / N;
+  const size_t VS = (S * Fmt<DT>::kBytes + 15) / 16;
+  const size_t per = (VS + p.G - 1) / p.G;
+  const size_t j0 = min(VS, (size_t)c * per), j1 = min(VS, j0 + per);
+  const size_t src_stride = (size_t)p.sen_chunk_vecs * 16;
+  const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
+  size_t lo, hi;
+  segment_of(count, N, r, lo, hi);
+  const size_t len = hi - lo;
+  for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    if (j * 16 >= len * Fmt<DT>::kBytes) break;
+    const uint4 x = seg_vec<DT>(p.in[r], 0, len, j);
+    if (!skip)
+#pragma unroll
+      for (int q = 0; q < N; ++q)
+        if (q != r) st_relaxed_v4(p.sen + (size_t)q * p.sen_stride + (size_t)r * src_stride + j * 16, x);
+    seg_store<DT>(p.out[r], lo, len, j, x);
+  }
+  for (size_t j = j0 + threadIdx.x; j < j1; j += blockDim.x)
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      if (q == r) continue;
+      size_t qlo, qhi;
+      segment_of(count, N, q, qlo, qhi);
+      if (j * 16 >= (qhi - qlo) * Fmt<DT>::kBytes) continue;
+      uint4 x;
+      if (!sen_take<DT, N>(p, p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride + j * 16, r, c, E, x))
+        return;
+      seg_store<DT>(p.out[r], qlo, qhi - qlo, j, x);
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_rs_ll128(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_rs_ll128<DT>(p, epoch0);
+  finish_launch(p);
+}
+template <int DT, int N>
+__global__ void __launch_bounds__(kMaxThreads) k_rs_sentinel(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_rs_sentinel<DT, N>(p, epoch0);
+  finish_launch(p);
+}
+template <int DT, int N>
+__global__ void __launch_bounds__(kMaxThreads) k_ag_sentinel(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  body_ag_sentinel<DT, N>(p, epoch0);
+  finish_launch(p);
+}
+
 template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_rs_ll(const Params p) {
   const u64 epoch0 = launch_epoch(p);
@@ -1432,12 +1688,18 @@ static cudaError_t launch_one_shot(int proto, int dtype, const Params& p, int th
 }
 template <int DT>
 static const void* segment_kernel(int which, int n) {
-  // which: 0 = ReduceScatter LL, 1 = AllGather LL, 2 = ReduceScatter fixed, 3 = AllGather fixed
+  // which: 0 = ReduceScatter LL, 1 = AllGather LL, 2 = ReduceScatter fixed,
+  // 3 = AllGather fixed, 4 = ReduceScatter LL128, 5 = ReduceScatter
+  // sentinel, 6 = AllGather sentinel
   if (which == 2) return (const void*)k_rs_fixed<DT>;
   if (which == 3) return (const void*)k_ag_fixed<DT>;
+  if (which == 4) return (const void*)k_rs_ll128<DT>;
   switch (n) {
-#define LLAR_SEG_CASE(NN) \
-    case NN: return which == 0 ? (const void*)k_rs_ll<DT, NN> : (const void*)k_ag_ll<DT, NN>;
+#define LLAR_SEG_CASE(NN)                                                                       \
+    case NN:                                                                                    \
+      return which == 0   ? (const void*)k_rs_ll<DT, NN>                                        \
+             : which == 1 ? (const void*)k_ag_ll<DT, NN>                                        \
+             : which == 5 ? (const void*)k_rs_sentinel<DT, NN> : (const void*)k_ag_sentinel<DT, NN>;
     LLAR_SEG_CASE(2) LLAR_SEG_CASE(3) LLAR_SEG_CASE(4) LLAR_SEG_CASE(5)
     LLAR_SEG_CASE(6) LLAR_SEG_CASE(7) LLAR_SEG_CASE(8)
 #undef LLAR_SEG_CASE
@@ -1450,7 +1712,7 @@ const void* segment_kernel_for(int which, int dtype, int n) {
 cudaError_t launch_segment(int which, int dtype, const Params& p, int threads, cudaStream_t s) {
   const void* k = segment_kernel_for(which, dtype, p.nranks);
   if (!k) return cudaErrorInvalidValue;
-  return launch_kernel(k, p, threads, s, which < 2);
+  return launch_kernel(k, p, threads, s, which != 2 && which != 3);  // the direct-read ones never wait
 }
 int max_resident_segment_ctas(int which, int dtype, int nranks, int threads) {
   const void* k = segment_kernel_for(which, dtype, nranks);

@@ -245,9 +245,16 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   const size_t bytes = count * e;
   const size_t seg_bytes = (count + c.n - 1) / c.n * e;
   if (proto == LLAR_PROTO_AUTO) proto = bytes <= (64u << 10) ? LLAR_PROTO_LL : LLAR_PROTO_FIXED_ONESHOT;
-  if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_FIXED_ONESHOT) return LLAR_ERR_UNSUPPORTED;
+  // AllGather adds nothing, so the atomic LL128 protocol has no AllGather
+  // of its own (its second half is LL)
+  const bool ok_proto = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_FIXED_ONESHOT ||
+                        proto == LLAR_PROTO_SENTINEL || (rs && proto == LLAR_PROTO_LL128_ATOMIC);
+  if (!ok_proto) return LLAR_ERR_UNSUPPORTED;
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
+  if (proto == LLAR_PROTO_LL128_ATOMIC && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
+  // the sentinel variants move every segment in one chunk
+  if (proto == LLAR_PROTO_SENTINEL && round_up(seg_bytes, 16) > c.chunk_bytes) return LLAR_ERR_TOO_LARGE;
   size_t full[llar::kMaxRanks], seg[llar::kMaxRanks];
   for (int r = 0; r < c.n; ++r) {
     const size_t per = (count + c.n - 1) / c.n;
@@ -261,18 +268,30 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   if (count == 0) return LLAR_OK;
   Params p;
   fill_params(c, p, in, out, count);
-  const int which = rs ? (proto == LLAR_PROTO_LL ? 0 : 2) : (proto == LLAR_PROTO_LL ? 1 : 3);
+  int which;
+  switch (proto) {
+    case LLAR_PROTO_LL: which = rs ? 0 : 1; break;
+    case LLAR_PROTO_LL128_ATOMIC: which = 4; break;
+    case LLAR_PROTO_SENTINEL: which = rs ? 5 : 6; break;
+    default: which = rs ? 2 : 3; break;
+  }
   int T = proto == LLAR_PROTO_LL ? 128 : 256;
   size_t units;
   if (proto == LLAR_PROTO_LL) {
     const size_t words = (bytes + 7) / 8, seg_words = (seg_bytes + 7) / 8;
     units = rs ? std::max(words, seg_words) : seg_words * c.n;
+  } else if (proto == LLAR_PROTO_LL128_ATOMIC) {
+    units = ll128_lines_for(count, c.n, c.dtype) * c.n * llar::kLL128Lanes;  // (segment, line, lane) items
+  } else if (proto == LLAR_PROTO_SENTINEL) {
+    units = round_up(seg_bytes, 16) / 16;  // one thread per vector of a segment, thin CTAs
+    T = units <= 512 ? 32 : 64;
   } else {
     units = rs ? seg_bytes / e : count;
   }
   int G = (int)std::max<size_t>(1, (units + T - 1) / T);
-  const int cap = proto == LLAR_PROTO_LL ? llar::max_resident_segment_ctas(which, c.dtype, c.n, T)
-                                         : 4 * c.sms;
+  if (proto == LLAR_PROTO_SENTINEL) G = std::max(G, 16);
+  const bool waits = proto != LLAR_PROTO_FIXED_ONESHOT;
+  const int cap = waits ? llar::max_resident_segment_ctas(which, c.dtype, c.n, T) : 4 * c.sms;
   if (cap <= 0) return LLAR_ERR_CUDA;
   G = std::min(G, std::max(1, cap / c.n));
   if (g_force_G > 0) G = g_force_G;
