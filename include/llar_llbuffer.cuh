@@ -108,9 +108,10 @@ template <> struct Elem<__half> {
     asm volatile("red.relaxed.gpu.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};"
                  :: "l"(a), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w) : "memory");
   }
+  // {1, -0} on the flag's 32-bit word: -0 leaves the next element as it is
   __device__ static __forceinline__ void red_one(void* a) {
-    const unsigned short one = 0x3C00;
-    asm volatile("red.relaxed.gpu.global.add.noftz.f16 [%0], %1;" :: "l"(a), "h"(one) : "memory");
+    const unsigned pair = 0x3C00u | (0x8000u << 16);
+    asm volatile("red.relaxed.gpu.global.add.noftz.f16x2 [%0], %1;" :: "l"(a), "r"(pair) : "memory");
   }
 };
 template <> struct Elem<__nv_bfloat16> {
@@ -125,8 +126,8 @@ template <> struct Elem<__nv_bfloat16> {
                  :: "l"(a), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w) : "memory");
   }
   __device__ static __forceinline__ void red_one(void* a) {
-    const unsigned short one = 0x3F80;
-    asm volatile("red.relaxed.gpu.global.add.noftz.bf16 [%0], %1;" :: "l"(a), "h"(one) : "memory");
+    const unsigned pair = 0x3F80u | (0x8000u << 16);
+    asm volatile("red.relaxed.gpu.global.add.noftz.bf16x2 [%0], %1;" :: "l"(a), "r"(pair) : "memory");
   }
 };
 

@@ -68,7 +68,7 @@ struct Params {
   char* sen;           size_t sen_stride;       // [2][N][CV][16]
   int sen_chunk_vecs;                           // CV: 16-byte vectors per chunk
   char* l128;          size_t l128_stride;      // [2][L][128]
-  char* l128ag;        size_t l128ag_stride;    // [2][N][L][256]
+  char* l128ag;        size_t l128ag_stride;    // [2][L][256]: the owner's published AllGather lines
   size_t l128_lines;                            // L: lines per slot
   char* chainbuf;      size_t chain_stride;     // [2][max_bytes] per rank
   size_t chain_slot_bytes;

@@ -560,7 +560,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   region(2 * (size_t)n * kMaxChunk, &c->sen_off, &c->sen_stride);
   c->l128_lines = ll128_lines_for(c->ll128_cap / c->esize, n, dtype);
   region(2 * c->l128_lines * llar::kLL128Line, &c->l128_off, &c->l128_stride);
-  region(2 * (size_t)n * c->l128_lines * llar::kAgLineBytes, &c->ag_off, &c->ag_stride);
+  region(2 * c->l128_lines * llar::kAgLineBytes, &c->ag_off, &c->ag_stride);
   c->chain_slot = round_up(c->max_bytes, kAlign);
   region(2 * c->chain_slot, &c->chain_off, &c->chain_stride);
   c->flags_off = off;
