@@ -491,6 +491,30 @@ def llbuffer_rows(llar, torch, dev, stream):
     return res
 
 
+def per_config_roofline(per_config, sol_us, hbm_gbs):
+    """Each row against its roofline: latency rows (microseconds per
+    operation) as speed of light / time, with the speed of light measured in
+    this run (2 x L2 round trip + one write: a per-operation floor whatever
+    the size); bandwidth rows as GB/s / the measured HBM copy bandwidth."""
+    def lat(v):
+        if isinstance(v, dict):
+            return {k: lat(x) for k, x in v.items()}
+        return round(sol_us / v, 4) if isinstance(v, (int, float)) and v > 0 else None
+
+    out = {"definition": "latency rows: sol_us / us (above 1 where back-to-back operations of one "
+                         "persistent launch overlap: the next one's lines leave before this one's "
+                         "reduction); bandwidth rows: GB/s / measured hbm_gbs",
+           "sol_us": round(sol_us, 4), "hbm_gbs": hbm_gbs}
+    for key, val in per_config.items():
+        if key.endswith("_us"):
+            out[key] = lat(val)
+        elif key == "C5_sweep_8ranks_bf16_fixed_twoshot":
+            out[key] = {k: round(v["GB/s"] / hbm_gbs, 4) for k, v in val.items()}
+        elif key.startswith("fused_linear"):
+            out[key] = {k: v["fused_frac_of_measured_hbm"] for k, v in val.items()}
+    return out
+
+
 def run_ours(args, world, rank, local, pg):
     import torch
     from tp_allreduce_persistent_b300 import inputs, llar
@@ -578,6 +602,7 @@ def run_ours(args, world, rank, local, pg):
     res["config"] = config
     if per_config is not None:
         res["per_config"] = per_config
+        res["per_config_roofline"] = per_config_roofline(per_config, sol_us, hbm_peak)
     return res
 
 
