@@ -258,6 +258,42 @@ __device__ __forceinline__ float elem_f(const T* p, size_t i) {
   return llb::Elem<T>::to_f(reinterpret_cast<const unsigned short*>(p)[i]);
 }
 
+// float32 values of elements (2i, 2i + 1) of a packed group of words, as
+// one 64-bit pair (element 2i in the low half)
+template <typename T>
+__device__ __forceinline__ u64 pair_of(const unsigned* v, int i) {
+  if (llb::Elem<T>::kBytes == 4) return (u64)v[2 * i] | ((u64)v[2 * i + 1] << 32);
+  const unsigned w = v[i];
+  const float lo = llb::Elem<T>::to_f(w & 0xFFFFu), hi = llb::Elem<T>::to_f(w >> 16);
+  return (u64)__float_as_uint(lo) | ((u64)__float_as_uint(hi) << 32);
+}
+// the MT activations of one k from shared memory, in 16-, 8-, 4- or 2-byte loads
+template <int XROW>
+__device__ __forceinline__ void load_xrow(const unsigned char* p, unsigned (&w)[(XROW + 3) / 4]) {
+  if (XROW >= 16) {
+#pragma unroll
+    for (int i = 0; i < XROW / 16; ++i) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+  } else if (XROW == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else if (XROW == 4) {
+    w[0] = *reinterpret_cast<const unsigned*>(p);
+  } else {
+    w[0] = *reinterpret_cast<const unsigned short*>(p);
+  }
+}
+// acc (two float32 lanes) += x * w lane by lane, one rounding per lane
+__device__ __forceinline__ void fma2(u64& acc, u64 x, u64 w) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(w));
+}
+
 template <int LW>
 __device__ __forceinline__ void load_lane(const char* p, unsigned (&v)[LW / 4]) {
   if (LW == 16) {
@@ -274,7 +310,7 @@ __device__ __forceinline__ void load_lane(const char* p, unsigned (&v)[LW / 4]) 
 }
 
 template <typename T, int MT, int LW, bool FUSE>
-__global__ void __launch_bounds__(kLinearThreads) kb_linear(const llar_llbuffer b, const LinearArgs a, int G) {
+__global__ void __launch_bounds__(kLinearThreads, 2) kb_linear(const llar_llbuffer b, const LinearArgs a, int G) {
   constexpr int EB = llb::Elem<T>::kBytes;
   constexpr int VEC = LW / EB;       // columns per lane
   constexpr int COLS = 32 * VEC;     // columns per tile
@@ -287,13 +323,23 @@ __global__ void __launch_bounds__(kLinearThreads) kb_linear(const llar_llbuffer 
   const int rank = (int)(blockIdx.x % n), cta = (int)(blockIdx.x / n);
   const int M = a.m, K = a.k, H = a.h;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  T* xs = reinterpret_cast<T*>(smem);
-  const size_t xbytes = ((size_t)M * K * EB + 15) & ~size_t(15);
+  // x staged transposed, [k][MT] with rows M..MT-1 zero: the activations
+  // of one k for every row come in one or two vector loads
+  unsigned char* xs = smem;
+  constexpr int XROW = MT * EB;  // bytes per k
+  const size_t xbytes = ((size_t)K * XROW + 15) & ~size_t(15);
   float* part = reinterpret_cast<float*>(smem + xbytes);  // [warp][m][COLS]
   const T* x = reinterpret_cast<const T*>(a.x[rank]);
   const char* w = a.w[rank];
   char* out = a.out[rank];
-  for (size_t i = threadIdx.x; i < (size_t)M * K; i += blockDim.x) xs[i] = x[i];
+  for (size_t i = threadIdx.x; i < (size_t)K * MT; i += blockDim.x) {
+    const size_t kk = i / MT, m = i % MT;
+    const unsigned b = m < (size_t)M ? (EB == 4 ? reinterpret_cast<const unsigned*>(x)[m * K + kk]
+                                                : reinterpret_cast<const unsigned short*>(x)[m * K + kk])
+                                     : 0u;
+    if (EB == 4) reinterpret_cast<unsigned*>(xs)[i] = b;
+    else reinterpret_cast<unsigned short*>(xs)[i] = (unsigned short)b;
+  }
   __syncthreads();
   const int tiles = (H + COLS - 1) / COLS;
   const int words_per_row = H / (8 / EB);
@@ -304,21 +350,29 @@ __global__ void __launch_bounds__(kLinearThreads) kb_linear(const llar_llbuffer 
   // ---- phase 1: GEMV of every tile of this CTA
   for (int t = cta; t < tiles; t += G) {
     const int col = t * COLS + lane * VEC;  // first column of my lane
-    float acc[MT][VEC];
+    // accumulators in float32 pairs (columns i, i + 1), updated with the
+    // packed two-lane fused multiply-add: each lane rounds once, exactly as
+    // a scalar fmaf, at half the instructions
+    u64 acc[MT][VEC / 2];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) acc[m][i] = 0.0f;
+      for (int i = 0; i < VEC / 2; ++i) acc[m][i] = 0ull;
     if (col < H) {
       const char* wp = w + (size_t)col * EB;
       auto fma_row = [&](const unsigned (&v)[LW / 4], int kk) {
+        u64 wpair[VEC / 2];  // float32 values of columns (2i, 2i + 1)
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) wpair[i] = pair_of<T>(v, i);
+        unsigned xw[(XROW + 3) / 4];
+        load_xrow<XROW>(xs + (size_t)kk * XROW, xw);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           if (m < M) {
-            const float xv = elem_f<T>(xs, (size_t)m * K + kk);
+            const unsigned xb = __float_as_uint(llb::Elem<T>::to_f(llb::elem_get<T>(xw, m)));
+            const u64 xx = ((u64)xb << 32) | xb;
 #pragma unroll
-            for (int i = 0; i < VEC; ++i)
-              acc[m][i] = __fmaf_rn(xv, llb::Elem<T>::to_f(llb::elem_get<T>(v, i)), acc[m][i]);
+            for (int i = 0; i < VEC / 2; ++i) fma2(acc[m][i], xx, wpair[i]);
           }
         }
       };
@@ -340,7 +394,11 @@ __global__ void __launch_bounds__(kLinearThreads) kb_linear(const llar_llbuffer 
     for (int m = 0; m < MT; ++m)
       if (m < M)
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) part[((size_t)warp * M + m) * COLS + lane * VEC + i] = acc[m][i];
+        for (int i = 0; i < VEC / 2; ++i) {
+          float* d = &part[((size_t)warp * M + m) * COLS + lane * VEC + 2 * i];
+          d[0] = __uint_as_float((unsigned)acc[m][i]);
+          d[1] = __uint_as_float((unsigned)(acc[m][i] >> 32));
+        }
     __syncthreads();
     // (row, word) pairs of the tile: slices in warp order, round, publish
     for (int p = threadIdx.x; p < M * 32 * WPL; p += blockDim.x) {
@@ -491,7 +549,7 @@ const void* linear_kernel(int m) {
   if (m <= 1) return (const void*)kb_linear<T, 1, 16, FUSE>;
   if (m <= 2) return (const void*)kb_linear<T, 2, 16, FUSE>;
   if (m <= 4) return (const void*)kb_linear<T, 4, 16, FUSE>;
-  if (m <= 8) return (const void*)kb_linear<T, 8, 8, FUSE>;
+  if (m <= 8) return (const void*)kb_linear<T, 8, 16, FUSE>;
   return (const void*)kb_linear<T, 16, 8, FUSE>;
 }
 template <bool FUSE>
@@ -500,7 +558,8 @@ const void* linear_kernel_for(int dtype, int m) {
   if (dtype == LLAR_F16) return linear_kernel<__half, FUSE>(m);
   return linear_kernel<__nv_bfloat16, FUSE>(m);
 }
-int linear_lane_bytes(int m) { return m <= 4 ? 16 : 8; }
+int linear_lane_bytes(int m) { return m <= 8 ? 16 : 8; }
+int linear_rows(int m) { return m <= 1 ? 1 : m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16; }
 
 int linear_launch(const llar_llbuffer* b, const void* const* x, const void* const* w, void* const* out, int n,
                   int m, int k, int h, int dtype, bool fuse, void* stream) {
@@ -531,7 +590,8 @@ int linear_launch(const llar_llbuffer* b, const void* const* x, const void* cons
   a.h = h;
   const int cols = 32 * linear_lane_bytes(m) / (int)e;
   const int tiles = (h + cols - 1) / cols;
-  const size_t smem = ((xbytes + 15) & ~size_t(15)) + (size_t)kLinearWarps * m * cols * 4;
+  const size_t smem = (((size_t)k * linear_rows(m) * e + 15) & ~size_t(15)) + (size_t)kLinearWarps * m * cols * 4;
+  if (smem > (227u << 10)) return LLAR_ERR_TOO_LARGE;  // not reached within the documented limits
   const void* kern = fuse ? linear_kernel_for<true>(dtype, m) : linear_kernel_for<false>(dtype, m);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return cuda_status(err);
