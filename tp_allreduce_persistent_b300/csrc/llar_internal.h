@@ -16,7 +16,7 @@ constexpr int kMaxThreads = 512;   // threads per CTA, upper bound of every kern
 constexpr int kLL128Line = 128;    // bytes per LL128 line
 constexpr int kLL128Lanes = 8;     // 16-byte lanes (threads) per line
 constexpr int kLLLine = 16;        // bytes per LL line: 8 data + 8 flag
-constexpr int kAgLineBytes = 256;  // one LL128 line re-sent as 16 LL lines
+constexpr int kAgLineBytes = 256;  // one LL128 line published again as 16 LL lines
 // per (rank, CTA) signal words: 0 ready and 1 done epochs of the fixed-order
 // chains, 2 consumption acknowledgements of point-to-point transfers
 constexpr int kFlagKinds = 3;

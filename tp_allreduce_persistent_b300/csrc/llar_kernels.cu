@@ -118,11 +118,12 @@ __device__ __forceinline__ void finish_launch(const Params& p, bool counted, uns
 __device__ __forceinline__ void finish_launch(const Params& p) { finish_launch(p, true, gridDim.x); }
 
 // One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
-// the thread pushes its unit of my data to every peer, polls the unit every
-// peer sent, adds the N values in rank order and stores the result. The
+// the thread sends its unit of my data (LL: publishes it once in my own
+// staging; sentinel: pushes it into every peer's slot), polls the unit of
+// every peer, adds the N values in rank order and stores the result. The
 // kernels are instantiated per N, so the peer loops unroll without guards.
-// Staging is [slot][source][unit]: a warp's store to one peer, and a warp's
-// poll of one source, cover 32 consecutive units.
+// A warp's store, and a warp's poll of one source, cover 32 consecutive
+// units.
 
 // float32 values of the elements of a 32-bit word
 template <int DT>
@@ -417,8 +418,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
 // rank adds its data of segment s into owner s's line with vector
 // reductions in the element type; after a fence, lane 0 adds 1 to the
 // flag. When the owner's flag reads N, every contribution is in. The owner
-// re-sends its reduced lines to every peer as LL lines (AllGather) and
-// zeroes its lines for their next use (epoch + 2).
+// publishes its reduced lines once, as LL lines in its own staging, which
+// every peer polls (AllGather), and zeroes its lines for their next use
+// (epoch + 2).
 template <int DT>
 __device__ __forceinline__ void red_add_v4(void* a, const unsigned* w) {
   if (DT == 0)
