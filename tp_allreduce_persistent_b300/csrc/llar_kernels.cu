@@ -1494,6 +1494,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
   char* const mine = p.ll + (size_t)r * p.ll_stride;
   const char* const from = p.ll + (size_t)(src < 0 ? 0 : src) * p.ll_stride;
   bool ok = true;
+  u64 unacked = 0;  // epoch received but not yet acknowledged (0: none)
   for (int e = 0; e < p.iters && ok; ++e) {
     const u64 E = E0 + (u64)e;
     const size_t slot = (size_t)(E & 1) * slot_stride;
@@ -1504,6 +1505,13 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
         for (size_t w = w0 + threadIdx.x; w < w1; w += blockDim.x)
           st_relaxed_b128(mine + slot + w * kLLLine, load_word8<DT>(in, w, p.count), E);
       }
+    }
+    // the previous transfer's acknowledgement goes out after this one's
+    // send (its sender needs it only before sending the next transfer):
+    // thread 0's fence is then off the path from receiving to sending
+    if (unacked && ok) {
+      post_ack(p, r, c, ack_value(unacked, 0));
+      unacked = 0;
     }
     if (src >= 0 && ok) {
       char* out = rank_output<DT>(p, r, e);
@@ -1523,7 +1531,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
         if (mine_ok) store_word8<DT>(out, w, p.count, lo);
       }
       ok = !__syncthreads_or(!mine_ok);
-      if (ok && !silent) post_ack(p, r, c, ack_value(E, 0));
+      if (ok && !silent) unacked = E;
     }
   }
   finish_launch(p);
