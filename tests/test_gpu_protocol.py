@@ -212,3 +212,20 @@ def test_sol_probe_is_consistent():
         d = llar.llar_sol_probe_detail()
         assert len(d["chase_ns"]) >= 100 and all(v > 0 for v in d["rt_ns"])
         assert all(a != b for a, b in zip(d["smid_a"], d["smid_b"]))
+
+
+@pytest.mark.parametrize("n,dtype,count,chunk,iters", [(5, "fp16", 118700, 65536, 17),
+                                                      (8, "bf16", 3 * 4096 + 100, 8192, 50),
+                                                      (3, "fp32", 2 * 2048 + 1, 8192, 9)])
+def test_sentinel_partial_last_chunk_across_iterations(n, dtype, count, chunk, iters):
+    # vectors beyond a partial last chunk miss that chunk's exchange, so the
+    # next iteration's first push must wait for the peer's reset itself
+    with context(n, dtype, 1 << 20):
+        llar.llar_set_sentinel_chunk(chunk)
+        x = inputs.normal(n, count, dtype, seed=count, iters=iters, exclude_sentinel=True)
+        got = allreduce_iters(x, dtype, "sentinel", iters)
+        xb = inputs.bits_of(x)
+        for e in range(iters):
+            assert np.array_equal(got[e], orc.allreduce(xb[e], dtype)), e
+        for buf in staging_bytes("sentinel", n):
+            assert np.all(buf == 0xFF)

@@ -210,6 +210,8 @@ __device__ __forceinline__ void chain_words(const unsigned* y, unsigned* nx, flo
   }
 }
 
+__device__ __forceinline__ bool is_all_ones(uint4 v) { return (v.x & v.y & v.z & v.w) == 0xFFFFFFFFu; }
+
 // True if any element of the 16-byte vector is the sentinel pattern.
 template <int DT>
 __device__ __forceinline__ bool has_sentinel(uint4 v) {

@@ -333,6 +333,9 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
       const size_t slot_off = (size_t)(seq & 1) * slot_stride;
       if (seq > 0) fence_gpu();  // my resets of the previous chunk before this chunk's pushes
       if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+      // the chunk before this one; a vector index beyond a partial last
+      // chunk took no part in it, so this push has no credit from it
+      const unsigned kprev = k > 0 ? k - 1 : nchunks - 1;
       if (!skip) {
         for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
           const unsigned v = k * CV + j;
@@ -341,9 +344,24 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
                           : (full || v + 1 < NV) ? (CHAIN ? ld_cg_v4(src + (size_t)v * 16)
                                                           : ld_stream_v4(src + (size_t)v * 16))
                                                  : load_vec16<DT>(src, v, p.count, !CHAIN);
+          const bool no_credit = seq >= 2 && kprev * CV + j >= NV;
 #pragma unroll
-          for (int q = 0; q < N; ++q)
-            if (q != r) st_relaxed_v4(to[q] + slot_off + (size_t)j * 16, x);
+          for (int q = 0; q < N; ++q) {
+            if (q == r) continue;
+            char* cell = to[q] + slot_off + (size_t)j * 16;
+            if (no_credit) {
+              // wait until peer q has consumed and reset my last vector in
+              // this slot: after my own earlier write to the cell, reading
+              // the all-ones pattern there can only be q's reset
+              Waiter wt;
+              while (!is_all_ones(ld_relaxed_v4(cell)))
+                if (wt.expired(p)) {
+                  report_timeout(p, r, c, E);
+                  return;  // as the polls below: no barrier inside this body
+                }
+            }
+            st_relaxed_v4(cell, x);
+          }
         }
       }
       for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
