@@ -42,16 +42,25 @@ def check(got, xb, dtype, proto):
         assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("case", draw_cases(2026, 60))
+@pytest.mark.parametrize("case", draw_cases(2026, 60) + draw_cases(99, 60))
 def test_random_allreduce(case):
     n, dtype, count, proto, kind, seed = case
     e = inputs.ELEM_BYTES[dtype]
+    rng = np.random.default_rng(seed)
     with context(n, dtype, max(count * e, 16) * 2 + 4096):
+        # a random sentinel chunk, and now and then a forced launch shape
+        llar.llar_set_sentinel_chunk(16 * int(rng.integers(1, 4097)))
+        if rng.random() < 0.3:
+            llar.llar_set_launch(int(rng.integers(1, 33)), 32 * int(rng.integers(1, 17)))
         x = inputs.normal(n, max(count, 1), dtype, seed=seed, exclude_sentinel=True)[:, :count]
         if kind == 0:  # one call
             ins = device_inputs(x.contiguous()) if count else [torch.zeros(8, device="cuda") for _ in range(n)]
             outs = filled_outputs(n, max(count, 1), dtype)
-            llar.llar_allreduce(ins, outs, count, proto)
+            try:
+                llar.llar_allreduce(ins, outs, count, proto)
+            except llar.LlarError as ex:  # a forced shape that cannot be co-resident
+                assert ex.code == llar.ERR_OCCUPANCY
+                return
             torch.cuda.synchronize()
             assert llar.llar_get_status()[0] == llar.OK
             if count:
@@ -77,7 +86,11 @@ def test_random_allreduce(case):
                     ins.append(buf)
                 in_stride = stride
             outs = filled_outputs(n, iters * stride, dtype)
-            llar.llar_allreduce_iters(ins, outs, count, proto, iters, in_stride, stride, chain)
+            try:
+                llar.llar_allreduce_iters(ins, outs, count, proto, iters, in_stride, stride, chain)
+            except llar.LlarError as ex:
+                assert ex.code == llar.ERR_OCCUPANCY
+                return
             torch.cuda.synchronize()
             assert llar.llar_get_status()[0] == llar.OK
             got = np.stack([inputs.bits_of(o).reshape(iters, stride)[:, :count] for o in outs], axis=1)
@@ -148,3 +161,86 @@ def test_random_segments_and_p2p(case):
             fill = np.full(xb.shape, FILL[dtype], dtype=xb.dtype)
             assert np.array_equal(np.stack([inputs.bits_of(o) for o in recvs]), p2p.sendrecv(xb, dst, fill))
         assert llar.llar_get_status()[0] == llar.OK
+
+
+@pytest.mark.parametrize("case", draw_cases(314, 40))
+def test_random_llbuffer_allreduce(case):
+    n, dtype, count, proto, kind, seed = case
+    proto = {"auto": "ll", "fixed_oneshot": "ll", "fixed_twoshot": "sentinel"}.get(proto, proto)
+    e = inputs.ELEM_BYTES[dtype]
+    count = max(count, 1)
+    iters = [1, 2, 9, 40][kind]
+    with llar.LLBuffer(n, count * e) as buf:
+        x = inputs.normal(n, count, dtype, seed=seed, exclude_sentinel=True)
+        ins = device_inputs(x)
+        outs = filled_outputs(n, count, dtype)
+        buf.allreduce(ins, outs, count, dtype, proto, iters)
+        torch.cuda.synchronize()
+        assert buf.status()[0] == llar.OK
+        check(np.stack([inputs.bits_of(o) for o in outs]), inputs.bits_of(x), dtype, proto)
+
+
+def draw_linear(seed, k):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(k):
+        out.append((int(rng.integers(2, 9)), int(rng.integers(1, 17)), int(rng.integers(1, 300)),
+                    8 * int(rng.integers(1, 66)), ["fp32", "fp16", "bf16"][int(rng.integers(0, 3))],
+                    int(rng.integers(0, 1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("case", draw_linear(2718, 30))
+def test_random_fused_linear(case):
+    from oracle import linear as olin
+    n, m, k, h, dtype, seed = case
+    x, w = inputs.linear_layer(n, m, k, h, dtype, seed=seed)
+    xs = [x[r].contiguous().cuda() for r in range(n)]
+    ws = [w[r].contiguous().cuda() for r in range(n)]
+    with llar.LLBuffer(n, m * h * inputs.ELEM_BYTES[dtype]) as buf:
+        outs = filled_outputs(n, m * h, dtype)
+        buf.fused_linear_allreduce(xs, ws, outs, m, k, h, dtype)
+        parts = filled_outputs(n, m * h, dtype)
+        llar.llar_linear_partials(xs, ws, parts, m, k, h, dtype)
+        outs2 = filled_outputs(n, m * h, dtype)
+        buf.allreduce(parts, outs2, m * h, dtype, "ll")
+        torch.cuda.synchronize()
+        assert buf.status()[0] == llar.OK
+    got = np.stack([inputs.bits_of(o).reshape(m, h) for o in outs])
+    ok, rel = olin.compare_linear(got, inputs.bits_of(x), inputs.bits_of(w), dtype)
+    assert ok, rel
+    assert np.array_equal(got, np.stack([inputs.bits_of(o).reshape(m, h) for o in outs2]))
+
+
+@pytest.mark.parametrize("case", draw_cases(4242, 30))
+def test_random_p2p_back_to_back(case):
+    n, dtype, count, proto, kind, seed = case
+    rng = np.random.default_rng(seed)
+    count = max(count, 1)
+    e = inputs.ELEM_BYTES[dtype]
+    p = "sentinel" if proto in ("sentinel", "ll128", "fixed_twoshot") else "ll"
+    if p == "ll" and count * e > (1 << 20):
+        p = "sentinel"
+    iters = int(rng.integers(2, 12))
+    perm = list(rng.permutation(n))
+    dst = [int(perm[(perm.index(r) + 1) % n]) for r in range(n)]
+    if rng.integers(0, 2):
+        dst[int(rng.integers(0, n))] = -1
+    stride = -(-count * e // 16) * 16 // e
+    with context(n, dtype, count * e + 4096):
+        llar.llar_set_sentinel_chunk(16 * int(rng.integers(1, 4097)))
+        x = inputs.normal(n, count, dtype, seed=seed, iters=iters, exclude_sentinel=True)
+        sends = []
+        for r in range(n):
+            buf = torch.zeros(iters * stride, dtype=inputs.TORCH_DTYPE[dtype], device="cuda")
+            buf.view(iters, stride)[:, :count] = x[:, r, :].cuda()
+            sends.append(buf)
+        recvs = filled_outputs(n, iters * stride, dtype)
+        llar.llar_sendrecv(sends, recvs, dst, count, p, iters, stride, stride)
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.OK
+        got = np.stack([inputs.bits_of(o).reshape(iters, stride)[:, :count] for o in recvs], axis=1)
+        xb = inputs.bits_of(x)
+        fill = np.full(xb.shape[1:], FILL[dtype], dtype=xb.dtype)
+        for it in range(iters):
+            assert np.array_equal(got[it], p2p.sendrecv(xb[it], dst, fill)), it
