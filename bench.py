@@ -532,6 +532,12 @@ def run_ours(args, world, rank, local, pg):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
 
     l2_us, write_us, sol_us = llar.llar_sol_probe()
+    detail = llar.llar_sol_probe_detail()
+    props = torch.cuda.get_device_properties(local)
+
+    def spread(v):
+        v = sorted(v)
+        return [round(v[0], 1), round(v[len(v) // 2], 1), round(v[-1], 1)] if v else None
     clocks = ClockSampler(local)
     clocks.start()
     lat = bw = None
@@ -572,7 +578,12 @@ def run_ours(args, world, rank, local, pg):
             "achieved_us": round(us, 4), "sol_us": round(sol_us, 4),
             "l2_round_trip_us": round(l2_us, 4), "write_us": round(write_us, 4),
             "frac": round(sol_us / us, 4), "within_2x_sol": bool(us <= 2 * sol_us),
-            "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run"}
+            "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run",
+            "probe_ns_min_median_max": {"l2_chase_per_sm": spread(detail["chase_ns"]),
+                                        "pingpong_round_trip_per_pair": spread(detail["rt_ns"])}}
+        res["device"] = {"name": props.name, "sms": props.multi_processor_count,
+                         "l2_bytes": getattr(props, "L2_cache_size", None),
+                         "memory_bytes": props.total_memory}
     if bw is not None:
         gbs = -max_over_ranks(pg, -bw["gbs"], dev)
         mib = args.bw_mib
