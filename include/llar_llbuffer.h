@@ -146,7 +146,10 @@ int llar_llbuffer_allreduce(const llar_llbuffer* b, const void* const* in, void*
  * b->nranks. Dot products accumulate in float32 with fused multiply-adds
  * (K split across warps, the slices added in order; for fp16/bf16 every
  * product is exact in float32), the rank sum in float32 with one
- * rounding. Runs on CUDA cores: HBM-bound up to M = 4, FMA-bound beyond. The partial p_r never goes to memory: the GEMV epilogue
+ * rounding. Up to 4 rows (and for fp32) the dot products run on CUDA
+ * cores; for fp16/bf16 with more rows on the tensor cores (mma.sync,
+ * float32 accumulation in an order and rounding of their own: within the
+ * same float32 error bound with 2^-23 per addition). The partial p_r never goes to memory: the GEMV epilogue
  * publishes it as LL lines and every rank reduces the lines it polls.
  * Limits: 1 <= M <= 16, 1 <= K, H >= 8, H % 8 == 0, M*H*elem <= b->bytes,
  * M*K*elem <= 96 KiB; pointers 16-byte aligned. Asynchronous on `stream`;

@@ -33,7 +33,11 @@ import numpy as np
 from . import allreduce as ar
 from . import fpformats as fp
 
-U32 = 2.0 ** -24  # unit roundoff of float32
+U32 = 2.0 ** -24  # unit roundoff of float32 (round to nearest)
+# relative error bound of one float32 addition whatever its rounding: the
+# tensor cores accumulate in float32 without stating the rounding of each
+# addition (round-toward-zero errs by up to 2^-23)
+U_ADD = 2.0 ** -23
 
 
 def _values(bits, dtype):
@@ -54,15 +58,17 @@ def linear_allreduce(x_bits, w_bits, dtype):
     return ar.allreduce(p.reshape(n, m * h), dtype).reshape(n, m, h)
 
 
-def linear_tolerance(x_bits, w_bits, dtype):
+def linear_tolerance(x_bits, w_bits, dtype, unit=U_ADD):
     """Per-element bound on |GPU output - linear_allreduce| ([M, H] float64).
 
-    With A_r = sum_k |x_r[m,k] w_r[k,h]| and gamma = K u / (1 - K u), u =
-    2^-24: any float32 evaluation of a K-term dot product (products rounded
-    and added, or fused multiply-adds, additions in any order) is within
-    gamma * A_r of the exact value (Higham, Accuracy and Stability of
-    Numerical Algorithms, ch. 3: every term goes through at most K
-    roundings, each a relative error of at most u).
+    With A_r = sum_k |x_r[m,k] w_r[k,h]| and gamma = K u / (1 - K u): any
+    float32 evaluation of a K-term dot product (products rounded and
+    added, fused multiply-adds, or tensor-core accumulation; additions in
+    any order) is within gamma * A_r of the exact value (Higham, Accuracy
+    and Stability of Numerical Algorithms, ch. 3: every term goes through at
+    most K roundings, each a relative error of at most u). u = `unit`:
+    2^-23 by default, which also covers additions rounded toward zero (the
+    tensor cores do not state their rounding); 2^-24 for round to nearest.
     Rounding both to the element type adds at most one ulp at (1 + gamma) A_r,
     so the partials differ by d_r = gamma A_r + ulp((1 + gamma) A_r). The two
     float32 rank-order sums then differ by at most sum_r d_r plus the error
@@ -73,17 +79,17 @@ def linear_tolerance(x_bits, w_bits, dtype):
     w = np.abs(_values(w_bits, dtype))
     n, _, k = x.shape
     a = np.matmul(x, w)  # [N, M, H]
-    gamma = k * U32 / (1.0 - k * U32)
+    gamma = k * unit / (1.0 - k * unit)
     d = gamma * a + fp.ulp((1.0 + gamma) * a, dtype)
     s = np.sum((1.0 + gamma) * a + d, axis=0)
     return np.sum(d, axis=0) + 2.0 * (n - 1) * U32 * s + fp.ulp(s, dtype)
 
 
-def compare_linear(got_bits, x_bits, w_bits, dtype):
+def compare_linear(got_bits, x_bits, w_bits, dtype, unit=U_ADD):
     """(ok, max error in tolerances) of a GPU result [N, M, H] against the oracle."""
     want = _values(linear_allreduce(x_bits, w_bits, dtype), dtype)
     got = _values(got_bits, dtype)
-    tol = linear_tolerance(x_bits, w_bits, dtype)
+    tol = linear_tolerance(x_bits, w_bits, dtype, unit)
     with np.errstate(invalid="ignore"):
         err = np.abs(got - want)
     ok = bool(np.all(np.isfinite(got)) and np.all(err <= tol))

@@ -159,6 +159,36 @@ def test_tolerance_covers_float32_evaluation_orders(dtype):
             assert ok, (trial, fma, rel)
 
 
+def _toward_zero_sum(x_bits, w_bits, dtype):
+    """float32 dot products with every addition rounded toward zero (as an
+    accumulator that truncates would), partials rounded to nearest, then
+    the rank-order AllReduce."""
+    x = fp.decode(x_bits, dtype).astype(np.float64)
+    w = fp.decode(w_bits, dtype).astype(np.float64)
+    n, m, k = x.shape
+    parts = []
+    for r in range(n):
+        acc = np.zeros((m, w.shape[2]), np.float64)
+        for t in range(k):
+            exact = acc + x[r][:, t:t + 1] * w[r][t:t + 1, :]
+            f = exact.astype(np.float32).astype(np.float64)  # nearest
+            toward0 = np.where(np.abs(f) > np.abs(exact), np.nextafter(f.astype(np.float32), np.float32(0)), f)
+            acc = np.asarray(toward0, np.float64)
+        parts.append(fp.encode_rne(acc.astype(np.float32), dtype))
+    p = np.stack(parts)
+    return orc.allreduce(p.reshape(n, -1), dtype).reshape(p.shape)
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_default_tolerance_covers_truncating_accumulation(dtype):
+    rng = np.random.default_rng(18)
+    n, m, k, h = 4, 2, 128, 16
+    x = fp.encode_rne(rng.standard_normal((n, m, k)).astype(np.float32), dtype)
+    w = fp.encode_rne((rng.standard_normal((n, k, h)) * 0.05).astype(np.float32), dtype)
+    got = _toward_zero_sum(x, w, dtype)
+    assert olin.compare_linear(got, x, w, dtype)[0]
+
+
 @pytest.mark.parametrize("dtype", fp.DTYPES)
 def test_tolerance_rejects_planted_mistakes(dtype):
     rng = np.random.default_rng(17)

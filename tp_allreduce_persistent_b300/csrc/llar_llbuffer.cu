@@ -20,6 +20,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "llar.h"
 #include "llar_llbuffer.cuh"
@@ -332,13 +333,31 @@ __global__ void __launch_bounds__(kLinearThreads, 2) kb_linear(const llar_llbuff
   const T* x = reinterpret_cast<const T*>(a.x[rank]);
   const char* w = a.w[rank];
   char* out = a.out[rank];
-  for (size_t i = threadIdx.x; i < (size_t)K * MT; i += blockDim.x) {
-    const size_t kk = i / MT, m = i % MT;
-    const unsigned b = m < (size_t)M ? (EB == 4 ? reinterpret_cast<const unsigned*>(x)[m * K + kk]
-                                                : reinterpret_cast<const unsigned short*>(x)[m * K + kk])
-                                     : 0u;
-    if (EB == 4) reinterpret_cast<unsigned*>(xs)[i] = b;
-    else reinterpret_cast<unsigned short*>(xs)[i] = (unsigned short)b;
+  constexpr int PV = 16 / EB;  // elements per 16-byte load
+  if (K % PV == 0) {  // rows of x start on 16-byte boundaries: 16-byte loads, scattered to [k][MT]
+    const int rowv = K / PV;
+    for (int i = threadIdx.x; i < MT * rowv; i += blockDim.x) {
+      const int m = i / rowv, j = i % rowv;
+      const uint4 v = m < M ? *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(x) +
+                                                              ((size_t)m * K + (size_t)j * PV) * EB)
+                            : make_uint4(0, 0, 0, 0);
+      const unsigned w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const size_t kk = (size_t)j * PV + u;
+        if (EB == 4) reinterpret_cast<unsigned*>(xs)[kk * MT + m] = w4[u];
+        else reinterpret_cast<unsigned short*>(xs)[kk * MT + m] = (unsigned short)llb::elem_get<T>(w4, u);
+      }
+    }
+  } else {
+    for (size_t i = threadIdx.x; i < (size_t)K * MT; i += blockDim.x) {
+      const size_t kk = i / MT, m = i % MT;
+      const unsigned b = m < (size_t)M ? (EB == 4 ? reinterpret_cast<const unsigned*>(x)[m * K + kk]
+                                                  : reinterpret_cast<const unsigned short*>(x)[m * K + kk])
+                                       : 0u;
+      if (EB == 4) reinterpret_cast<unsigned*>(xs)[i] = b;
+      else reinterpret_cast<unsigned short*>(xs)[i] = (unsigned short)b;
+    }
   }
   __syncthreads();
   const int tiles = (H + COLS - 1) / COLS;
@@ -440,6 +459,187 @@ __global__ void __launch_bounds__(kLinearThreads, 2) kb_linear(const llar_llbuff
         }
         *reinterpret_cast<u64*>(out + wid * 8) = llb::sum_words_ranks<T>(d, n);
       }
+    llb::end(b, 1u);
+  }
+}
+
+// ---------------------------------------------- tensor-core variant (M <= 16)
+// For 16-bit types and more than 4 rows the FMA rate bounds the kernel
+// above, so the same layer runs on the tensor cores: mma.sync m16n8k16
+// (fp16/bf16 operands, float32 accumulators), the rows of x padded to 16.
+// Each warp owns 32 output columns over the whole of K (no cross-warp
+// reduction): it streams its weight rows with coalesced 16-byte cp.async
+// copies into a warp-private ring of kTcStages shared tiles [16 k][32
+// columns] (80-byte pitch: the rows of an ldmatrix land in distinct
+// banks), from which ldmatrix.trans builds the B fragments; x sits in shared memory as [16 rows][Kp] (Kp = K rounded up
+// to 16, pitch 2 Kp + 16 bytes, zero beyond K and beyond M). The
+// accumulators become LL words (4 consecutive columns of a row) through
+// one shuffle between neighbouring lanes; the epilogue is the LL
+// AllReduce as in kb_linear. The tensor cores sum the 16 products of a
+// step in an order of their own.
+constexpr int kTcWarps = 8;
+constexpr int kTcCols = 32 * kTcWarps;  // columns per CTA tile
+constexpr int kTcPitch = 80;            // bytes per row of a warp's weight tile
+constexpr int kTcTile = 16 * kTcPitch;  // one buffer
+constexpr int kTcStages = 6;            // k-steps of weights in flight per warp (cp.async ring)
+
+__device__ __forceinline__ void ldsm_x4(unsigned addr, unsigned (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(unsigned addr, unsigned (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const unsigned (&a)[4], unsigned b0, unsigned b1) {
+  if constexpr (std::is_same<T, __half>::value)
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename T, bool FUSE>
+__global__ void __launch_bounds__(32 * kTcWarps, 2) kb_linear_tc(const llar_llbuffer b, const LinearArgs a, int G) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const u64 E = FUSE ? llb::begin(b) : 0;
+  const int n = a.n;
+  const int rank = (int)(blockIdx.x % n), cta = (int)(blockIdx.x / n);
+  const int M = a.m, K = a.k, H = a.h;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Kp = (K + 15) & ~15;
+  const int xpitch = 2 * Kp + 16;
+  unsigned char* xs = smem;                                               // [16][Kp]
+  unsigned char* wt = smem + 16 * xpitch + warp * kTcStages * kTcTile;    // my ring
+  const unsigned short* x = reinterpret_cast<const unsigned short*>(a.x[rank]);
+  const char* w = a.w[rank];
+  char* out = a.out[rank];
+  if (K % 8 == 0) {  // rows of x start on 16-byte boundaries: 16-byte loads
+    const int kv = Kp / 8, rowv = K / 8;
+    for (int i = threadIdx.x; i < 16 * kv; i += blockDim.x) {
+      const int m = i / kv, j = i % kv;
+      const uint4 v = (m < M && j < rowv) ? *reinterpret_cast<const uint4*>(x + (size_t)m * K + (size_t)j * 8)
+                                          : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(xs + m * xpitch + j * 16) = v;
+    }
+  } else {
+    for (int i = threadIdx.x; i < 16 * Kp; i += blockDim.x) {
+      const int m = i / Kp, kk = i % Kp;
+      reinterpret_cast<unsigned short*>(xs + m * xpitch)[kk] = (m < M && kk < K) ? x[(size_t)m * K + kk] : 0;
+    }
+  }
+  __syncthreads();
+  const int tiles = (H + kTcCols - 1) / kTcCols;
+  const int steps = Kp / 16;
+  const size_t row_bytes = (size_t)H * 2;
+  const int words_per_row = H / 4;
+  const int g = lane >> 2, q = lane & 3;
+  // my two 16-byte chunks of a k-step: rows id / 4, column chunks id % 4
+  const int id0 = lane, id1 = lane + 32;
+  const unsigned wt_s = (unsigned)__cvta_generic_to_shared(wt);
+  const unsigned xs_s = (unsigned)__cvta_generic_to_shared(xs);
+  // ldmatrix row addresses: A (x) rows (mi & 1) * 8 + l % 8, k half mi >> 1;
+  // B (weights) k rows (mi & 1) * 8 + l % 8, column block mi >> 1
+  const int mi = lane >> 3, li = lane & 7;
+  const unsigned a_row = xs_s + (unsigned)(((mi & 1) * 8 + li) * xpitch + (mi >> 1) * 16);
+  const unsigned b_row = (unsigned)(((mi & 1) * 8 + li) * kTcPitch + (mi >> 1) * 16);
+
+  for (int t = cta; t < tiles; t += G) {
+    const int c0 = t * kTcCols + warp * 32;  // my first column
+    // my two 16-byte chunks of k-step st into ring slot st % kTcStages;
+    // chunks past K or H are zero-filled (source size 0)
+    auto issue = [&](int st) {
+      if (st < steps) {
+        const unsigned slot = wt_s + (unsigned)((st % kTcStages) * kTcTile);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int id = h2 ? id1 : id0;
+          const int row = st * 16 + id / 4, col = c0 + (id % 4) * 8;
+          const bool in = row < K && col < H;
+          const char* src = in ? w + (size_t)row * row_bytes + (size_t)col * 2 : w;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                       :: "r"(slot + (unsigned)((id / 4) * kTcPitch + (id % 4) * 16)), "l"(src), "r"(in ? 16 : 0)
+                       : "memory");
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");  // one group per step, even if empty
+    };
+    float d[4][4];
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[nb][i] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kTcStages - 1; ++i) issue(i);
+    for (int st = 0; st < steps; ++st) {
+      issue(st + kTcStages - 1);
+      asm volatile("cp.async.wait_group %0;" :: "n"(kTcStages - 1) : "memory");  // step st is in
+      __syncwarp();  // ... for every lane's copies
+      unsigned af[4], bf0[4], bf1[4];
+      ldsm_x4(a_row + (unsigned)(st * 32), af);
+      const unsigned bs = wt_s + (unsigned)((st % kTcStages) * kTcTile);
+      ldsm_x4_trans(bs + b_row, bf0);       // column blocks 0, 1
+      ldsm_x4_trans(bs + b_row + 32, bf1);  // column blocks 2, 3
+      mma16816<T>(d[0], af, bf0[0], bf0[1]);
+      mma16816<T>(d[1], af, bf0[2], bf0[3]);
+      mma16816<T>(d[2], af, bf1[0], bf1[1]);
+      mma16816<T>(d[3], af, bf1[2], bf1[3]);
+      __syncwarp();  // every lane has read this slot before it is refilled
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // accumulators -> LL words: lane (g, q) holds columns 2q, 2q + 1 of rows
+    // g and g + 8 in each column block; an even q takes its neighbour's pair
+    // of row g (4 columns of row g), an odd q gives its row-(g + 8) pair to
+    // its neighbour and takes theirs (4 columns of row g + 8)
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      const float o0 = __shfl_xor_sync(0xFFFFFFFFu, (q & 1) ? d[nb][0] : d[nb][2], 1);
+      const float o1 = __shfl_xor_sync(0xFFFFFFFFu, (q & 1) ? d[nb][1] : d[nb][3], 1);
+      float v[4];
+      int row;
+      if (!(q & 1)) {
+        row = g;
+        v[0] = d[nb][0]; v[1] = d[nb][1]; v[2] = o0; v[3] = o1;
+      } else {
+        row = g + 8;
+        v[0] = o0; v[1] = o1; v[2] = d[nb][2]; v[3] = d[nb][3];
+      }
+      const int col = c0 + nb * 8 + 2 * (q & ~1);
+      if (row < M && col < H) {
+        unsigned y2[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) llb::elem_set<T>(y2, i, llb::Elem<T>::from_f(v[i]));
+        const u64 mine = (u64)y2[0] | ((u64)y2[1] << 32);
+        const size_t wid = (size_t)row * words_per_row + col / 4;
+        if (FUSE) llb::ll_put(b, rank, E, wid, mine);
+        else *reinterpret_cast<u64*>(out + wid * 8) = mine;
+      }
+    }
+  }
+  if (FUSE) {
+    bool ok = true;
+    for (int t = cta; t < tiles && ok; t += G) {
+      const int c0 = t * kTcCols + warp * 32;
+      for (int nb = 0; nb < 4 && ok; ++nb) {
+        const int row = (q & 1) ? g + 8 : g;
+        const int col = c0 + nb * 8 + 2 * (q & ~1);
+        if (row >= M || col >= H) continue;
+        const size_t wid = (size_t)row * words_per_row + col / 4;
+        u64 dd[8];
+        llb::ll_try(b, rank, E, wid, dd[rank]);  // my own line, written by this thread
+        if (!llb::ll_wait_ranks(b, rank, E, wid, dd)) {
+          ok = false;
+          break;
+        }
+        *reinterpret_cast<u64*>(out + wid * 8) = llb::sum_words_ranks<T>(dd, n);
+      }
+    }
     llb::end(b, 1u);
   }
 }
@@ -553,6 +753,15 @@ const void* linear_kernel(int m) {
   return (const void*)kb_linear<T, 16, 8, FUSE>;
 }
 template <bool FUSE>
+const void* linear_tc_kernel_for(int dtype) {
+  return dtype == LLAR_F16 ? (const void*)kb_linear_tc<__half, FUSE> : (const void*)kb_linear_tc<__nv_bfloat16, FUSE>;
+}
+// shared memory of the tensor-core variant: x [16][Kp] and a warp's ring
+size_t linear_tc_smem(int k) {
+  const size_t kp = ((size_t)k + 15) & ~size_t(15);
+  return 16 * (2 * kp + 16) + (size_t)kTcWarps * kTcStages * kTcTile;
+}
+template <bool FUSE>
 const void* linear_kernel_for(int dtype, int m) {
   if (dtype == LLAR_F32) return linear_kernel<float, FUSE>(m);
   if (dtype == LLAR_F16) return linear_kernel<__half, FUSE>(m);
@@ -588,11 +797,16 @@ int linear_launch(const llar_llbuffer* b, const void* const* x, const void* cons
   a.m = m;
   a.k = k;
   a.h = h;
-  const int cols = 32 * linear_lane_bytes(m) / (int)e;
+  // 16-bit types with more than 4 rows: the tensor-core variant, when its
+  // shared memory fits (measured: the FMA rate bounds the CUDA-core one)
+  const bool tc = e == 2 && m > 4 && linear_tc_smem(k) <= (200u << 10) && !std::getenv("LLAR_LINEAR_NO_TC");
+  const int cols = tc ? kTcCols : 32 * linear_lane_bytes(m) / (int)e;
   const int tiles = (h + cols - 1) / cols;
-  const size_t smem = (((size_t)k * linear_rows(m) * e + 15) & ~size_t(15)) + (size_t)kLinearWarps * m * cols * 4;
+  const size_t smem = tc ? linear_tc_smem(k)
+                         : (((size_t)k * linear_rows(m) * e + 15) & ~size_t(15)) + (size_t)kLinearWarps * m * cols * 4;
   if (smem > (227u << 10)) return LLAR_ERR_TOO_LARGE;  // not reached within the documented limits
-  const void* kern = fuse ? linear_kernel_for<true>(dtype, m) : linear_kernel_for<false>(dtype, m);
+  const void* kern = tc ? (fuse ? linear_tc_kernel_for<true>(dtype) : linear_tc_kernel_for<false>(dtype))
+                        : (fuse ? linear_kernel_for<true>(dtype, m) : linear_kernel_for<false>(dtype, m));
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return cuda_status(err);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
