@@ -432,13 +432,14 @@ def llbuffer_rows(llar, torch, dev, stream):
                 rows[name][proto] = round(us, 3)
     res = {"llbuffer_allreduce_us": rows}
 
-    # decode layers of a hidden-8192 model over 8 ranks, one token: attention
+    # decode layers of a hidden-8192 model over 8 ranks (m tokens): attention
     # output projection (K = 8192 / 8) and MLP down projection (K = 28672 / 8);
     # weight sets rotate so that each call streams weights not in L2
     peak = measured_peaks()[0]["hbm_gbs"]
     layers = {}
-    for name, k, sets in (("attn_out_k1024", 1024, 4), ("mlp_down_k3584", 3584, 2)):
-        n, m, h, dtype = 8, 1, 8192, "bf16"
+    for name, m, k, sets in (("attn_out_k1024_m1", 1, 1024, 4), ("attn_out_k1024_m8", 8, 1024, 4),
+                             ("attn_out_k1024_m16", 16, 1024, 4), ("mlp_down_k3584_m1", 1, 3584, 2)):
+        n, h, dtype = 8, 8192, "bf16"
         xs, ws = [], []
         for sidx in range(sets):
             x, w = inputs.linear_layer(n, m, k, h, dtype, seed=100 + sidx)
@@ -487,7 +488,7 @@ def llbuffer_rows(llar, torch, dev, stream):
                         "gemv_only_us": round(timing["gemv_only"], 2), "weight_bytes": wbytes,
                         "fused_weight_GB/s": round(gbs, 1), "fused_frac_of_measured_hbm": round(gbs / peak, 4)}
         del xs, ws
-    res["fused_linear_allreduce_8ranks_m1_h8192_bf16"] = layers
+    res["fused_linear_allreduce_8ranks_h8192_bf16"] = layers
     return res
 
 
