@@ -20,7 +20,7 @@ What is computed, and where the pages define it:
   every rank every segment (zcube page, collectives table, rows
   Reduce-Scatter and All-Gather).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * Accumulation: float32, ranks added in order 0, 1, ..., N-1 with IEEE
   addition (roundTiesToEven, no fused operations), one final

@@ -19,7 +19,7 @@ techniques that remove the global memory barrier.
   for D bytes per round; the flag costs about 1.5% of bandwidth in FP16
   and about 3% in FP32.
 
-Readings (listed in the design doc): the sentinel is the all-ones pattern of
+Readings where the pages are silent: the sentinel is the all-ones pattern of
 the element type (a NaN with the sign bit set, i.e. a -NaN, in all three
 formats); the LL flag is a 64-bit call counter; the LL128 flag is the
 line's first element, in the element type.
