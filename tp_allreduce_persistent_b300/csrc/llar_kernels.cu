@@ -522,10 +522,142 @@ __device__ __forceinline__ void red_add_flag(void* a, unsigned one_bits) {
   }
 }
 
+// A lane of LL128 line l of segment s carries the V elements at segment
+// positions l*P + j*V - 1 + k (k < V; lane 0's k = 0 is the flag): a window
+// of 16 bytes that starts one element before a lane boundary, so for
+// 63-element (31-element) lines its alignment to the 16-byte vectors of the
+// message rotates from line to line. Inside the message the window is read
+// with two aligned 16-byte loads and shifted into place, and written with
+// at most five naturally aligned stores; windows that reach past the
+// segment or the message (or start before it) take elements one by one.
+// ll128_window returns false there; ll128_first is the window's first
+// element index in the message.
+template <int DT>
+__device__ __forceinline__ bool ll128_window(size_t count, size_t seg, int s, size_t l, int j, size_t& first) {
+  constexpr int V = 16 / Fmt<DT>::kBytes;
+  constexpr int P = 128 / Fmt<DT>::kBytes - 1;
+  const size_t sl0 = l * P + (size_t)j * V;  // segment position of element k = 1
+  const size_t base = (size_t)s * seg;
+  const size_t lim = min(seg, count - min(count, base));  // elements of segment s
+  first = base + sl0 - 1;
+  return sl0 + V - 1 <= lim && base + sl0 >= 1;
+}
+// the V elements at `first` as 4 packed words, for an in-message window
+// whose two covering vectors lie inside the buffer (`nbytes` long)
+template <int DT>
+__device__ __forceinline__ bool ll128_gather_fast(const char* src, size_t first, size_t nbytes, unsigned w[4]) {
+  const size_t off = first * Fmt<DT>::kBytes;
+  const size_t vb = off & ~(size_t)15;
+  const unsigned h = (unsigned)(off & 15) >> 1;  // 16-bit halves into the vector
+  if (h != 0 && vb + 32 > nbytes) return false;
+  const uint4 a = *reinterpret_cast<const uint4*>(src + vb);
+  const uint4 b = h ? *reinterpret_cast<const uint4*>(src + vb + 16) : make_uint4(0, 0, 0, 0);
+  unsigned x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  if (h & 4) {
+#pragma unroll
+    for (int i = 0; i < 6; ++i) x[i] = x[i + 2];
+  }
+  if (h & 2) {
+#pragma unroll
+    for (int i = 0; i < 5; ++i) x[i] = x[i + 1];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = (h & 1) ? __byte_perm(x[i], x[i + 1], 0x5432) : x[i];
+  return true;
+}
+// store the window's elements (all V, or V-1 without element 0 for lane 0)
+template <int DT>
+__device__ __forceinline__ void ll128_scatter_fast(char* dst, size_t first, bool skip0, const unsigned w[4]) {
+  char* b = dst + first * Fmt<DT>::kBytes;
+  if (Fmt<DT>::kBytes == 4) {
+    if (!skip0 && (first & 3) == 0) {
+      *reinterpret_cast<uint4*>(b) = make_uint4(w[0], w[1], w[2], w[3]);
+      return;
+    }
+    if (!skip0) *reinterpret_cast<unsigned*>(b) = w[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i) *reinterpret_cast<unsigned*>(b + 4 * i) = w[i];
+    return;
+  }
+  if (!skip0 && (first & 7) == 0) {
+    *reinterpret_cast<uint4*>(b) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if ((first & 1) == 0) {
+    if (skip0) *reinterpret_cast<unsigned short*>(b + 2) = (unsigned short)(w[0] >> 16);
+    else *reinterpret_cast<unsigned*>(b) = w[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i) *reinterpret_cast<unsigned*>(b + 4 * i) = w[i];
+  } else {
+    if (!skip0) *reinterpret_cast<unsigned short*>(b) = (unsigned short)w[0];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) *reinterpret_cast<unsigned*>(b + 2 + 4 * i) = __byte_perm(w[i], w[i + 1], 0x5432);
+    *reinterpret_cast<unsigned short*>(b + 14) = (unsigned short)(w[3] >> 16);
+  }
+}
+// element by element (windows at the edges of a segment or the message)
+template <int DT>
+__device__ __forceinline__ bool ll128_gather_slow(const char* src, size_t count, size_t seg, int s, size_t l, int j,
+                                                  unsigned w[4]) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int V = 16 / EB;
+  constexpr int P = 128 / EB - 1;
+  bool any = false;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int pos = j * V + k;
+    const size_t sl = l * P + (size_t)pos - 1;
+    const size_t g = (size_t)s * seg + sl;
+    unsigned b = 0;
+    if (pos >= 1 && sl < seg && g < count) {
+      b = Fmt<DT>::load(src, g);
+      any = true;
+    }
+    const int word = (k * EB) / 4, sub = (EB == 4) ? 0 : (k & 1);
+    if (EB == 4) w[word] = b;
+    else w[word] = sub ? (w[word] | (b << 16)) : b;
+  }
+  return any;
+}
+template <int DT>
+__device__ __forceinline__ void ll128_scatter_slow(char* dst, size_t dst_off, size_t count, size_t seg, int s, size_t l,
+                                                   int j, const unsigned w[4]) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int V = 16 / EB;
+  constexpr int P = 128 / EB - 1;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int pos = j * V + k;
+    const size_t sl = l * P + (size_t)pos - 1;
+    const size_t g = (size_t)s * seg + sl;
+    if (pos >= 1 && sl < seg && g < count)
+      Fmt<DT>::store(dst, g - dst_off, word_elem<DT>(w[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
+  }
+}
+// lane j of line l of segment s: gather my input (zero where no element)
+template <int DT>
+__device__ __forceinline__ bool ll128_gather(const char* src, size_t count, size_t seg, int s, size_t l, int j,
+                                             unsigned w[4]) {
+  size_t first;
+  if (ll128_window<DT>(count, seg, s, l, j, first) &&
+      ll128_gather_fast<DT>(src, first, count * Fmt<DT>::kBytes, w)) {
+    if (j == 0) w[0] &= (Fmt<DT>::kBytes == 4) ? 0u : 0xFFFF0000u;  // the flag's element
+    return true;
+  }
+  return ll128_gather_slow<DT>(src, count, seg, s, l, j, w);
+}
+// store lane j of line l of segment s; message element g goes to dst
+// element g - dst_off (0: a whole-message output; s * seg: a segment output)
+template <int DT>
+__device__ __forceinline__ void ll128_scatter(char* dst, size_t dst_off, size_t count, size_t seg, int s, size_t l,
+                                              int j, const unsigned w[4]) {
+  size_t first;
+  if (ll128_window<DT>(count, seg, s, l, j, first) && first >= dst_off)
+    ll128_scatter_fast<DT>(dst, first - dst_off, j == 0, w);
+  else ll128_scatter_slow<DT>(dst, dst_off, count, seg, s, l, j, w);
+}
+
 template <int DT>
 __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
   constexpr int EB = Fmt<DT>::kBytes;
-  constexpr int V = 16 / EB;    // elements per lane
   constexpr int EL = 128 / EB;  // elements per line
   constexpr int P = EL - 1;     // data elements per line
   const int N = p.nranks;
@@ -537,8 +669,12 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
   const size_t Lc = (L + p.G - 1) / p.G;
   const size_t l0 = min(L, (size_t)c * Lc);
   const size_t nl = min(L, l0 + Lc) - l0;
-  const size_t items = (size_t)N * nl * kLL128Lanes;
-  const size_t T = blockDim.x;
+  // items of this CTA: (segment, line, lane), lane fastest; fewer than
+  // 2^32 (LL128 messages are at most 1 GiB per rank: a segment of at most
+  // 2^28 elements has under 2^23 lines)
+  const unsigned per_seg = (unsigned)(nl * kLL128Lanes);
+  const unsigned items = (unsigned)N * per_seg;
+  const unsigned T = blockDim.x;
   const unsigned one_bits = Fmt<DT>::from_f(1.0f);
   const unsigned n_bits = Fmt<DT>::from_f((float)N);
   const unsigned flag_mask = (EB == 4) ? 0xFFFFFFFFu : 0xFFFFu;
@@ -564,52 +700,37 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
 
     // ---- ReduceScatter: add my data into every owner's lines
     if (!skip) {
-      for (size_t i = threadIdx.x; i < items; i += T) {
-        const int s = (int)(i / (nl * kLL128Lanes));
-        const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+      for (unsigned i = threadIdx.x; i < items; i += T) {
+        const int s = (int)(i / per_seg);
+        const unsigned rem = i - (unsigned)s * per_seg;
         const size_t l = l0 + rem / kLL128Lanes;
         const int j = (int)(rem % kLL128Lanes);
         unsigned w[4];
-        bool any = false;
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-          const int pos = j * V + k;
-          const size_t sl = l * P + (size_t)pos - 1;
-          const size_t g = (size_t)s * seg + sl;
-          unsigned b = 0;
-          if (pos >= 1 && sl < seg && g < count) {
-            b = Fmt<DT>::load(src, g);
-            any = true;
-          }
-          const int word = (k * EB) / 4, sub = (EB == 4) ? 0 : (k & 1);
-          if (EB == 4) w[word] = b;
-          else w[word] = sub ? (w[word] | (b << 16)) : b;
-        }
-        if (any)
+        if (ll128_gather<DT>(src, count, seg, s, l, j, w))
           red_add_v4<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line + j * 16, w);
       }
     }
     __syncwarp();
     fence_gpu();  // every data reduction of this warp before its flags
     if (!skip) {
-      for (size_t i = threadIdx.x; i < items; i += T) {
+      for (unsigned i = threadIdx.x; i < items; i += T) {
         if ((i % kLL128Lanes) != 0) continue;
-        const int s = (int)(i / (nl * kLL128Lanes));
-        const size_t l = l0 + (i - (size_t)s * nl * kLL128Lanes) / kLL128Lanes;
+        const int s = (int)(i / per_seg);
+        const size_t l = l0 + (i - (unsigned)s * per_seg) / kLL128Lanes;
         red_add_flag<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line,
                          poison ? 0u : one_bits);
       }
     }
 
     // ---- owner: wait for count N, read, AllGather as LL lines, zero
-    for (size_t base = 0; base < items; base += T) {
-      const size_t i = base + threadIdx.x;
+    for (unsigned base = 0; base < items; base += T) {
+      const unsigned i = base + threadIdx.x;
       int s = -1;
       size_t l = 0;
       int j = 0;
       if (i < items) {
-        s = (int)(i / (nl * kLL128Lanes));
-        const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+        s = (int)(i / per_seg);
+        const unsigned rem = i - (unsigned)s * per_seg;
         l = l0 + rem / kLL128Lanes;
         j = (int)(rem % kLL128Lanes);
       }
@@ -632,18 +753,11 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
       __syncwarp();  // all 8 lanes have read the flag and their data before any zeroing
       if (own) {
         const unsigned w[4] = {v.x, v.y, v.z, v.w};
-        unsigned nx[4];
-        if (p.chain) chain_words<DT, 4>(w, nx, p.chain_scale);
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-          const int pos = j * V + k;
-          const size_t sl = l * P + (size_t)pos - 1;
-          const size_t g = (size_t)r * seg + sl;
-          if (pos >= 1 && sl < seg && g < count) {
-            Fmt<DT>::store(dst, g, word_elem<DT>(w[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
-            if (p.chain)
-              Fmt<DT>::store(chain_next_buf(p, r, e), g, word_elem<DT>(nx[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
-          }
+        ll128_scatter<DT>(dst, 0, count, seg, r, l, j, w);
+        if (p.chain) {
+          unsigned nx[4];
+          chain_words<DT, 4>(w, nx, p.chain_scale);
+          ll128_scatter<DT>(chain_next_buf(p, r, e), 0, count, seg, r, l, j, nx);
         }
         if (!skip) {
           const u64 lo = (u64)v.x | ((u64)v.y << 32);
@@ -658,10 +772,10 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
     }
 
     // ---- AllGather receive: poll the owners' LL lines, write my output
-    for (size_t i = threadIdx.x; i < items; i += T) {
-      const int s = (int)(i / (nl * kLL128Lanes));
+    for (unsigned i = threadIdx.x; i < items; i += T) {
+      const int s = (int)(i / per_seg);
       if (s == r) continue;
-      const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+      const unsigned rem = i - (unsigned)s * per_seg;
       const size_t l = l0 + rem / kLL128Lanes;
       const int j = (int)(rem % kLL128Lanes);
       const char* ag = p.l128ag + (size_t)s * p.l128ag_stride + slot * ag_slot + l * kAgLineBytes + j * 32;
@@ -684,18 +798,11 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
         }
       }
       const unsigned w[4] = {(unsigned)lo, (unsigned)(lo >> 32), (unsigned)hi, (unsigned)(hi >> 32)};
-      unsigned nx[4];
-      if (p.chain) chain_words<DT, 4>(w, nx, p.chain_scale);
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int pos = j * V + k;
-        const size_t sl = l * P + (size_t)pos - 1;
-        const size_t g = (size_t)s * seg + sl;
-        if (pos >= 1 && sl < seg && g < count) {
-          Fmt<DT>::store(dst, g, word_elem<DT>(w[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
-          if (p.chain)
-            Fmt<DT>::store(chain_next_buf(p, r, e), g, word_elem<DT>(nx[(k * EB) / 4], (EB == 4) ? 0 : (k & 1)));
-        }
+      ll128_scatter<DT>(dst, 0, count, seg, s, l, j, w);
+      if (p.chain) {
+        unsigned nx[4];
+        chain_words<DT, 4>(w, nx, p.chain_scale);
+        ll128_scatter<DT>(chain_next_buf(p, r, e), 0, count, seg, s, l, j, nx);
       }
     }
     if (__any_sync(0xFFFFFFFFu, failed)) return;
@@ -1275,7 +1382,6 @@ __device__ __forceinline__ void seg_store(char* base, size_t lo, size_t len, siz
 template <int DT>
 __device__ __forceinline__ void body_rs_ll128(const Params& p, const u64 E) {
   constexpr int EB = Fmt<DT>::kBytes;
-  constexpr int V = 16 / EB;    // elements per lane
   constexpr int P = 128 / EB - 1;
   const int N = p.nranks;
   const int r = rank_of_block(p);
@@ -1286,8 +1392,9 @@ __device__ __forceinline__ void body_rs_ll128(const Params& p, const u64 E) {
   const size_t Lc = (L + p.G - 1) / p.G;
   const size_t l0 = min(L, (size_t)c * Lc);
   const size_t nl = min(L, l0 + Lc) - l0;
-  const size_t items = (size_t)N * nl * kLL128Lanes;
-  const size_t T = blockDim.x;
+  const unsigned per_seg = (unsigned)(nl * kLL128Lanes);  // fewer than 2^32 items, as in body_ll128
+  const unsigned items = (unsigned)N * per_seg;
+  const unsigned T = blockDim.x;
   const int slot = (int)(E & 1);
   const size_t line_slot = p.l128_lines * (size_t)kLL128Line;
   const unsigned one_bits = Fmt<DT>::from_f(1.0f);
@@ -1296,45 +1403,31 @@ __device__ __forceinline__ void body_rs_ll128(const Params& p, const u64 E) {
   const bool skip = p.inject_rank == r && p.inject_mode == LLAR_INJECT_SKIP_;
   const char* src = p.in[r];
   if (!skip)
-    for (size_t i = threadIdx.x; i < items; i += T) {
-      const int s = (int)(i / (nl * kLL128Lanes));
-      const size_t rem = i - (size_t)s * nl * kLL128Lanes;
+    for (unsigned i = threadIdx.x; i < items; i += T) {
+      const int s = (int)(i / per_seg);
+      const unsigned rem = i - (unsigned)s * per_seg;
       const size_t l = l0 + rem / kLL128Lanes;
       const int j = (int)(rem % kLL128Lanes);
-      size_t lo, hi;
-      segment_of(count, N, s, lo, hi);
-      unsigned w[4] = {0u, 0u, 0u, 0u};
-      bool any = false;
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int pos = j * V + k;
-        const size_t sl = l * P + (size_t)pos - 1;
-        if (pos >= 1 && sl < hi - lo) {
-          const unsigned b = Fmt<DT>::load(src, lo + sl);
-          const int word = (k * EB) / 4;
-          w[word] = EB == 4 ? b : word_set<DT>(w[word], k & 1, b);
-          any = true;
-        }
-      }
-      if (any) red_add_v4<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line + j * 16, w);
+      unsigned w[4];
+      if (ll128_gather<DT>(src, count, seg, s, l, j, w))
+        red_add_v4<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line + j * 16, w);
     }
   __syncwarp();
   fence_gpu();  // every data reduction of this warp before its counts
   if (!skip)
-    for (size_t i = threadIdx.x; i < items; i += T) {
+    for (unsigned i = threadIdx.x; i < items; i += T) {
       if ((i % kLL128Lanes) != 0) continue;
-      const int s = (int)(i / (nl * kLL128Lanes));
-      const size_t l = l0 + (i - (size_t)s * nl * kLL128Lanes) / kLL128Lanes;
+      const int s = (int)(i / per_seg);
+      const size_t l = l0 + (i - (unsigned)s * per_seg) / kLL128Lanes;
       red_add_flag<DT>(p.l128 + (size_t)s * p.l128_stride + slot * line_slot + l * kLL128Line, one_bits);
     }
-  // owner r: my lines [l0, l0 + nl), 8 lanes each
-  size_t lo, hi;
-  segment_of(count, N, r, lo, hi);
+  // owner r: my lines [l0, l0 + nl), 8 lanes each; out[r] holds segment r
+  const size_t lo = min(count, (size_t)r * seg);
   char* const my_lines = p.l128 + (size_t)r * p.l128_stride + slot * line_slot;
   bool failed = false;
-  const size_t mine = nl * kLL128Lanes;
-  for (size_t base = 0; base < mine; base += T) {  // warp-uniform trip count
-    const size_t i = base + threadIdx.x;
+  const unsigned mine = per_seg;
+  for (unsigned base = 0; base < mine; base += T) {  // warp-uniform trip count
+    const unsigned i = base + threadIdx.x;
     const bool active = i < mine;
     const size_t l = l0 + i / kLL128Lanes;
     const int j = (int)(i % kLL128Lanes);
@@ -1354,12 +1447,7 @@ __device__ __forceinline__ void body_rs_ll128(const Params& p, const u64 E) {
     if (active && !failed) {
       st_relaxed_v4(line + j * 16, make_uint4(0, 0, 0, 0));
       const unsigned w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int pos = j * V + k;
-        const size_t sl = l * P + (size_t)pos - 1;
-        if (pos >= 1 && sl < hi - lo) Fmt<DT>::store(p.out[r], sl, word_elem<DT>(w[(k * EB) / 4], EB == 4 ? 0 : (k & 1)));
-      }
+      ll128_scatter<DT>(p.out[r], lo, count, seg, r, l, j, w);
     }
   }
 }

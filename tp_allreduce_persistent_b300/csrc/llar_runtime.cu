@@ -20,6 +20,7 @@ using llar::Params;
 constexpr size_t kAlign = 256;
 constexpr size_t kDefaultLLCap = 1u << 20;      // LL messages up to 1 MiB per rank
 constexpr size_t kDefaultLL128Cap = 64u << 20;  // LL128 messages up to 64 MiB per rank
+constexpr size_t kMaxLL128Cap = size_t(1) << 30;  // the LL128 kernels index a CTA's items in 32 bits
 constexpr size_t kDefaultChunk = 64u << 10;     // sentinel chunk per rank: every chunk costs a round trip and a fence
 constexpr size_t kMaxChunk = 64u << 10;         // largest sentinel chunk
 constexpr int kFlagsGmax = 1024;                // CTAs per rank the chain flags can address
@@ -535,7 +536,8 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   c->esize = elem_bytes(dtype);
   c->max_bytes = round_up(max_bytes, 16);
   c->ll_cap = std::min(c->max_bytes, round_up(env_size("LLAR_LL_MAX_BYTES", kDefaultLLCap), 16));
-  c->ll128_cap = std::min(c->max_bytes, round_up(env_size("LLAR_LL128_MAX_BYTES", kDefaultLL128Cap), 16));
+  c->ll128_cap = std::min(c->max_bytes,
+                           std::min(kMaxLL128Cap, round_up(env_size("LLAR_LL128_MAX_BYTES", kDefaultLL128Cap), 16)));
   c->chunk_bytes = round_up(std::min(env_size("LLAR_CHUNK_BYTES", kDefaultChunk), kMaxChunk), 16);
   g_timeout_ns = env_size("LLAR_TIMEOUT_NS", g_timeout_ns);
   g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", (size_t)g_force_G);
