@@ -163,3 +163,25 @@ def test_bench_bandwidth_launch_exactly_sampled():
         torch.cuda.synchronize()
         rng = np.random.default_rng(6)
         _sampled_check(ins, outs, count, np.concatenate([rng.integers(0, count, 20000), [0, count - 1]]))
+
+
+@pytest.mark.parametrize("n,count,chain", [(8, 65536, 0.5), (4, 65536, 0.5), (8, 32768, 0.0), (8, 8192, 0.0),
+                                           (8, 2048, 0.0), (3, 40000, 0.0)])
+def test_ll128_threads_cover_a_ctas_lines_in_one_pass(n, count, chain):
+    # an LL128 CTA takes ceil(L / G) whole lines of every segment (8 lanes
+    # each); below the wide shape (more items than one 512-thread CTA per
+    # SM holds) its threads cover them in one pass
+    x = inputs.normal(n, count, "bf16", seed=9, scale=0.02)
+    with context(n, "bf16", count * 2):
+        ins = device_inputs(x)
+        outs = filled_outputs(n, count, "bf16")
+        llar.llar_allreduce_iters(ins, outs, count, "ll128", 2, 0, 0, chain)
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.OK
+        proto, G, T, _ = llar.llar_last_launch()
+        got = np.stack([inputs.bits_of(o) for o in outs])
+    assert proto == "ll128"
+    lines = -(-(-(-count // n)) // 63)
+    items = n * (-(-lines // G)) * 8
+    assert T >= min(items, 512), (G, T, items)
+    assert all(np.array_equal(got[0], got[q]) for q in range(n))

@@ -168,6 +168,15 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
       const size_t per_cta = (units + g - 1) / g;
       t = (int)std::min<size_t>(llar::kMaxThreads, round_up(per_cta, 32));
     }
+    if (proto == LLAR_PROTO_LL128_ATOMIC) {
+      // a CTA takes whole lines, ceil(L / g) of every segment: threads for
+      // all of its items in one pass (8 ranks x 128 KiB bf16 chain: 480
+      // threads left 32 of 512 items for a second pass, 5.17 us per layer;
+      // 512 threads 4.18 us)
+      const size_t lines = units / ((size_t)n * llar::kLL128Lanes);
+      const size_t items = (lines + g - 1) / g * (size_t)n * llar::kLL128Lanes;
+      t = (int)std::min<size_t>(llar::kMaxThreads, round_up(items, 32));
+    }
   }
   if (g_force_G > 0) g = g_force_G;
   if (g_force_T > 0) t = g_force_T;
