@@ -192,8 +192,10 @@ def linear(buf, x, w, dtype, fused=True):
     return np.stack([inputs.bits_of(o).reshape(m, h) for o in outs])
 
 
+# the last two give 8 ranks more column tiles than CTAs (40 and 48 tiles of
+# 256 columns on the tensor-core path): CTAs with two tiles
 SHAPES = [(2, 1, 1, 8), (2, 3, 37, 136), (4, 16, 64, 264), (8, 1, 1024, 512), (8, 5, 200, 8),
-          (3, 2, 9, 1000)]
+          (3, 2, 9, 1000), (8, 8, 64, 10240), (8, 16, 32, 12288)]
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])

@@ -550,6 +550,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 2) kb_linear_tc(const llar_llbu
   const unsigned a_row = xs_s + (unsigned)(((mi & 1) * 8 + li) * xpitch + (mi >> 1) * 16);
   const unsigned b_row = (unsigned)(((mi & 1) * 8 + li) * kTcPitch + (mi >> 1) * 16);
 
+  u64 own[4] = {0, 0, 0, 0};  // my published words of my last tile (nb = 0..3)
   for (int t = cta; t < tiles; t += G) {
     const int c0 = t * kTcCols + warp * 32;  // my first column
     // my two 16-byte chunks of k-step st into ring slot st % kTcStages;
@@ -617,27 +618,62 @@ __global__ void __launch_bounds__(32 * kTcWarps, 2) kb_linear_tc(const llar_llbu
         for (int i = 0; i < 4; ++i) llb::elem_set<T>(y2, i, llb::Elem<T>::from_f(v[i]));
         const u64 mine = (u64)y2[0] | ((u64)y2[1] << 32);
         const size_t wid = (size_t)row * words_per_row + col / 4;
+        own[nb] = mine;
         if (FUSE) llb::ll_put(b, rank, E, wid, mine);
         else *reinterpret_cast<u64*>(out + wid * 8) = mine;
       }
     }
   }
   if (FUSE) {
+    // The LL AllReduce of my words: two words per polling round (their
+    // 2(N-1) peer lines in flight together); my own word from registers
+    // for my last tile, from my line for earlier ones.
+    const int row = (q & 1) ? g + 8 : g;
     bool ok = true;
     for (int t = cta; t < tiles && ok; t += G) {
       const int c0 = t * kTcCols + warp * 32;
-      for (int nb = 0; nb < 4 && ok; ++nb) {
-        const int row = (q & 1) ? g + 8 : g;
-        const int col = c0 + nb * 8 + 2 * (q & ~1);
-        if (row >= M || col >= H) continue;
-        const size_t wid = (size_t)row * words_per_row + col / 4;
-        u64 dd[8];
-        llb::ll_try(b, rank, E, wid, dd[rank]);  // my own line, written by this thread
-        if (!llb::ll_wait_ranks(b, rank, E, wid, dd)) {
-          ok = false;
-          break;
+      const bool last = t + G >= tiles;
+#pragma unroll
+      for (int nb0 = 0; nb0 < 4; nb0 += 2) {
+        size_t wid[2];
+        u64 dd[2][8];
+        unsigned pend = 0;  // bit 8u + q: word u of rank q not yet in
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col = c0 + (nb0 + u) * 8 + 2 * (q & ~1);
+          wid[u] = (size_t)row * words_per_row + col / 4;
+          if (row < M && col < H) {
+            u64 mine = own[nb0 + u];
+            if (!last) llb::ll_try(b, rank, E, wid[u], mine);  // my own line, written by this thread
+#pragma unroll
+            for (int r2 = 0; r2 < 8; ++r2)  // constant indices: dd stays in registers
+              if (r2 == rank) dd[u][r2] = mine;
+            pend |= (((1u << n) - 1u) & ~(1u << rank)) << (8 * u);
+          }
         }
-        *reinterpret_cast<u64*>(out + wid * 8) = llb::sum_words_ranks<T>(dd, n);
+        const unsigned valid = pend;
+        llb::Wait wt;
+        while (pend != 0u) {
+          u64 lo[16], hi[16];
+#pragma unroll
+          for (int h2 = 0; h2 < 16; ++h2)
+            if ((pend >> h2) & 1u) llb::ld_relaxed_b128(llb::ll_line(b, h2 & 7, E, wid[h2 >> 3]), lo[h2], hi[h2]);
+#pragma unroll
+          for (int h2 = 0; h2 < 16; ++h2)
+            if (((pend >> h2) & 1u) && hi[h2] == E) {
+              dd[h2 >> 3][h2 & 7] = lo[h2];
+              pend &= ~(1u << h2);
+            }
+          if (pend != 0u && wt.expired(b)) {
+            llb::fail(b, rank, E);
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if ((valid >> (8 * u)) & 0xFFu) *reinterpret_cast<u64*>(out + wid[u] * 8) = llb::sum_words_ranks<T>(dd[u], n);
       }
     }
     llb::end(b, 1u);
