@@ -57,8 +57,10 @@ def parse(argv=None):
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
-    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer"],
-                    help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone")
+    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer", "config"],
+                    help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone; "
+                         "config: one row of the per-configuration table (--case)")
+    ap.add_argument("--case", default="C4_sentinel", choices=sorted(CONFIG_CASES), help="row for --leg config")
     ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
     ap.add_argument("--bw-mib", type=int, default=BW_COUNT * 2 >> 20, help="MiB per rank, bandwidth leg")
     return ap.parse_args(argv)
@@ -288,31 +290,48 @@ def e2e_leg(args, llar, torch, stream, x, pg, local):
     return e0.elapsed_time(e1) * 1e3 / calls
 
 
+def timed_config(llar, torch, dev, stream, n, dtype, count, proto, iters, chain=0.0, chunk=None, max_bytes=None):
+    """One workload configuration: a warm-up launch of min(iters, 20)
+    AllReduces, then one timed launch of `iters`; microseconds per AllReduce."""
+    from tp_allreduce_persistent_b300 import inputs
+    llar.llar_init(n, dtype, max_bytes or max(count * inputs.ELEM_BYTES[dtype], 4096))
+    try:
+        if chunk:
+            llar.llar_set_sentinel_chunk(chunk)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        td = inputs.TORCH_DTYPE[dtype]
+        ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(td) for _ in range(n)]
+        outs = [torch.empty_like(t) for t in ins]
+        llar.llar_allreduce_iters(ins, outs, count, proto, min(iters, 20), 0, 0, chain)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        llar.llar_allreduce_iters(ins, outs, count, proto, iters, 0, 0, chain)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if llar.llar_get_status()[0] != llar.OK:
+            raise RuntimeError("device status not ok")
+        return round(a.elapsed_time(b) * 1e3 / iters, 3)
+    finally:
+        llar.llar_destroy()
+
+
+# single rows of the per-configuration table, for profiling one kernel
+# (`--leg config --case NAME`): (ranks, dtype, elements per rank, protocol,
+# AllReduces per launch, chain scale, sentinel chunk bytes)
+CONFIG_CASES = {
+    "C3_ll128_1MiB": (8, "bf16", 1024 * 512, "ll128", 200, 0.0, None),
+    "C3_ll128_16KiB": (8, "bf16", 16 * 512, "ll128", 1000, 0.0, None),
+    "C4_sentinel": (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192),
+    "C5_ll128_chain_N8": (8, "bf16", 65536, "ll128", 160, 0.5, None),
+}
+
+
 def configs_leg(llar, torch, dev, stream):
     """Per-AllReduce time of each workload configuration (persistent launches)."""
     def timed(n, dtype, count, proto, iters, chain=0.0, chunk=None, max_bytes=None):
-        from tp_allreduce_persistent_b300 import inputs
-        llar.llar_init(n, dtype, max_bytes or max(count * inputs.ELEM_BYTES[dtype], 4096))
-        try:
-            if chunk:
-                llar.llar_set_sentinel_chunk(chunk)
-            gen = torch.Generator(device=dev)
-            gen.manual_seed(7)
-            td = inputs.TORCH_DTYPE[dtype]
-            ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(td) for _ in range(n)]
-            outs = [torch.empty_like(t) for t in ins]
-            llar.llar_allreduce_iters(ins, outs, count, proto, min(iters, 20), 0, 0, chain)
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            llar.llar_allreduce_iters(ins, outs, count, proto, iters, 0, 0, chain)
-            b.record(stream)
-            torch.cuda.synchronize()
-            if llar.llar_get_status()[0] != llar.OK:
-                raise RuntimeError("device status not ok")
-            return round(a.elapsed_time(b) * 1e3 / iters, 3)
-        finally:
-            llar.llar_destroy()
+        return timed_config(llar, torch, dev, stream, n, dtype, count, proto, iters, chain, chunk, max_bytes)
 
     out = {
         "C1_2ranks_128B_fp32_us": {p: timed(2, "fp32", 32, p, 1000) for p in ("ll", "fixed_oneshot")},
@@ -523,6 +542,12 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
+    if args.leg == "config":
+        n, dtype, count, proto, iters, chain, chunk = CONFIG_CASES[args.case]
+        us = timed_config(llar, torch, dev, stream, n, dtype, count, proto, iters, chain, chunk)
+        if rank == 0:
+            print(json.dumps({"leg": "config", "case": args.case, "us_per_allreduce": us}))
+        return
     if args.leg == "llbuffer":
         if rank == 0:
             print(json.dumps({"leg": "llbuffer", **llbuffer_rows(llar, torch, dev, stream)}))
@@ -669,7 +694,7 @@ def main():
             print(json.dumps(res), flush=True)
         return
     res = run_ours(args, world, rank, local, pg)
-    if rank == 0:
+    if rank == 0 and res is not None:  # the llbuffer and config legs print their own line
         if not args.no_cpu_baseline:
             us, n = time_oracle(10.0)
             res["cpu_baseline"] = {"value": round(us, 3), "unit": "us", "cores": 1, "kind": "oracle",

@@ -74,3 +74,13 @@ def test_reference_arm_line(monkeypatch):
 def test_oracle_timing_runs():
     us, n = bench.time_oracle(0.05, count=256, nranks=4)
     assert us > 0 and n >= 1
+
+
+def test_config_cases_parse_and_match_the_table_rows():
+    # `--leg config --case NAME` reruns one row of the per-configuration table
+    for name in bench.CONFIG_CASES:
+        assert bench.parse(["--leg", "config", "--case", name]).case == name
+    assert bench.CONFIG_CASES["C4_sentinel"] == (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192)
+    assert bench.CONFIG_CASES["C3_ll128_1MiB"][:4] == (8, "bf16", 1 << 19, "ll128")
+    with pytest.raises(SystemExit):
+        bench.parse(["--leg", "config", "--case", "no_such_row"])
