@@ -60,7 +60,8 @@ def parse(argv=None):
     ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer", "config"],
                     help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone; "
                          "config: one row of the per-configuration table (--case)")
-    ap.add_argument("--case", default="C4_sentinel", choices=sorted(CONFIG_CASES), help="row for --leg config")
+    ap.add_argument("--case", default="C4_sentinel", choices=sorted(CONFIG_CASES) + sorted(FUSED_CASES),
+                    help="row for --leg config")
     ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
     ap.add_argument("--bw-mib", type=int, default=BW_COUNT * 2 >> 20, help="MiB per rank, bandwidth leg")
     return ap.parse_args(argv)
@@ -326,6 +327,33 @@ CONFIG_CASES = {
     "C4_sentinel": (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192),
     "C5_ll128_chain_N8": (8, "bf16", 65536, "ll128", 160, 0.5, None),
 }
+# fused decode layers for `--leg config --case NAME`: (ranks, tokens m, K, H), bf16
+FUSED_CASES = {
+    "fused_m1_k1024": (8, 1, 1024, 8192),
+    "fused_m16_k1024": (8, 16, 1024, 8192),
+}
+
+
+def fused_case_us(llar, torch, dev, stream, n, m, k, h, calls=4):
+    """A warm-up call, then `calls` timed calls of the fused layer on one
+    weight set; microseconds per call."""
+    from tp_allreduce_persistent_b300 import inputs
+    x, w = inputs.linear_layer(n, m, k, h, "bf16", seed=100)
+    xs = [x[r].to(dev) for r in range(n)]
+    ws = [w[r].to(dev) for r in range(n)]
+    outs = [torch.empty(m * h, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    with llar.LLBuffer(n, m * h * 2) as buf:
+        buf.fused_linear_allreduce(xs, ws, outs, m, k, h, "bf16")
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(calls):
+            buf.fused_linear_allreduce(xs, ws, outs, m, k, h, "bf16")
+        b.record(stream)
+        torch.cuda.synchronize()
+        if buf.status()[0] != llar.OK:
+            raise RuntimeError("LL buffer status not ok")
+    return round(a.elapsed_time(b) * 1e3 / calls, 3)
 
 
 def configs_leg(llar, torch, dev, stream):
@@ -543,10 +571,14 @@ def run_ours(args, world, rank, local, pg):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     if args.leg == "config":
-        n, dtype, count, proto, iters, chain, chunk = CONFIG_CASES[args.case]
-        us = timed_config(llar, torch, dev, stream, n, dtype, count, proto, iters, chain, chunk)
+        if args.case in FUSED_CASES:
+            us = fused_case_us(llar, torch, dev, stream, *FUSED_CASES[args.case])
+        else:
+            n, dtype, count, proto, iters, chain, chunk = CONFIG_CASES[args.case]
+            us = timed_config(llar, torch, dev, stream, n, dtype, count, proto, iters, chain, chunk)
         if rank == 0:
-            print(json.dumps({"leg": "config", "case": args.case, "us_per_allreduce": us}))
+            key = "us_per_call" if args.case in FUSED_CASES else "us_per_allreduce"
+            print(json.dumps({"leg": "config", "case": args.case, key: us}))
         return
     if args.leg == "llbuffer":
         if rank == 0:

@@ -78,7 +78,7 @@ def test_oracle_timing_runs():
 
 def test_config_cases_parse_and_match_the_table_rows():
     # `--leg config --case NAME` reruns one row of the per-configuration table
-    for name in bench.CONFIG_CASES:
+    for name in list(bench.CONFIG_CASES) + list(bench.FUSED_CASES):
         assert bench.parse(["--leg", "config", "--case", name]).case == name
     assert bench.CONFIG_CASES["C4_sentinel"] == (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192)
     assert bench.CONFIG_CASES["C3_ll128_1MiB"][:4] == (8, "bf16", 1 << 19, "ll128")
