@@ -625,26 +625,37 @@ __global__ void __launch_bounds__(32 * kTcWarps, 2) kb_linear_tc(const llar_llbu
     }
   }
   if (FUSE) {
-    // The LL AllReduce of my words: two words per polling round (their
-    // 2(N-1) peer lines in flight together); my own word from registers
-    // for my last tile, from my line for earlier ones.
-    const int row = (q & 1) ? g + 8 : g;
+    // The LL AllReduce of my words, two per polling round (their 2(N-1)
+    // peer lines in flight together). Lanes q and q ^ 1 share rows g and
+    // g + 8 of column blocks 0-3: the even lane takes blocks 0, 1 and the
+    // odd lane blocks 2, 3 of both rows, so up to 8 rows take one round.
+    // My own word comes from registers (mine, or my neighbour's by a
+    // shuffle) for my last tile, from my line for earlier ones.
+    const bool odd = (q & 1) != 0;
+    const int nbA = odd ? 2 : 0;  // my two column blocks nbA, nbA + 1
+    u64 nbr[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) nbr[k] = __shfl_xor_sync(0xFFFFFFFFu, own[k], 1);
+    const u64 myA = odd ? own[2] : own[0], myB = odd ? own[3] : own[1];
+    const u64 nbrA = odd ? nbr[2] : nbr[0], nbrB = odd ? nbr[3] : nbr[1];
     bool ok = true;
     for (int t = cta; t < tiles && ok; t += G) {
       const int c0 = t * kTcCols + warp * 32;
       const bool last = t + G >= tiles;
 #pragma unroll
-      for (int nb0 = 0; nb0 < 4; nb0 += 2) {
+      for (int half = 0; half < 2; ++half) {  // row g, then row g + 8
+        const int row = g + 8 * half;
+        const bool held = (int)odd == half;  // my lane published this row's words
         size_t wid[2];
         u64 dd[2][8];
         unsigned pend = 0;  // bit 8u + q: word u of rank q not yet in
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int col = c0 + (nb0 + u) * 8 + 2 * (q & ~1);
+          const int col = c0 + (nbA + u) * 8 + 2 * (q & ~1);
           wid[u] = (size_t)row * words_per_row + col / 4;
           if (row < M && col < H) {
-            u64 mine = own[nb0 + u];
-            if (!last) llb::ll_try(b, rank, E, wid[u], mine);  // my own line, written by this thread
+            u64 mine = held ? (u ? myB : myA) : (u ? nbrB : nbrA);
+            if (!last) llb::ll_try(b, rank, E, wid[u], mine);  // my rank's line
 #pragma unroll
             for (int r2 = 0; r2 < 8; ++r2)  // constant indices: dd stays in registers
               if (r2 == rank) dd[u][r2] = mine;
