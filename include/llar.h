@@ -246,6 +246,22 @@ unsigned long long llar_epoch(void);
  * threads per CTA, iterations. Any pointer may be NULL. */
 int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters);
 
+/* Diagnostic, host arithmetic only (no GPU work, no llar_init needed; no
+ * page describes it: it exposes the launch-shape rule to tests). The shape
+ * (CTAs per rank, threads per CTA) the runtime picks for a call of `count`
+ * elements per rank with `nranks` ranks (2..8), element type `dtype` and
+ * `protocol` (LLAR_PROTO_LL .. LLAR_PROTO_FIXED_TWOSHOT, not AUTO),
+ * chained (`chained` != 0: llar_allreduce_iters with a chain scale) or not,
+ * on a GPU with `sms` SMs and sentinel chunks of `chunk_bytes` (16 ..
+ * 65536, a multiple of 16). It is the shape before a launch applies the
+ * GPU's residency limit (fewer CTAs per rank when not all can be resident)
+ * and before an unchained fixed two-shot at or above its TMA threshold
+ * switches to the TMA kernel's own shape; a shape forced with
+ * llar_set_launch is reported as forced. Either pointer may be NULL.
+ * LLAR_ERR_INVALID for arguments out of range. */
+int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, int chained, int sms,
+                            size_t chunk_bytes, int* ctas_per_rank, int* threads);
+
 /* One LL AllReduce that allocates nothing: no cudaMalloc, no cudaFree and
  * no allocating library routine, before or during the call, and no
  * llar_init needed. (No page describes this entry point; it exists for

@@ -889,6 +889,27 @@ int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters
   return LLAR_OK;
 }
 
+int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, int chained, int sms,
+                            size_t chunk_bytes, int* ctas_per_rank, int* threads) {
+  if (nranks < 2 || nranks > llar::kMaxRanks || !valid_dtype(dtype) || count == 0 || sms < 1) return LLAR_ERR_INVALID;
+  if (protocol < LLAR_PROTO_LL || protocol > LLAR_PROTO_FIXED_TWOSHOT) return LLAR_ERR_INVALID;
+  if (chunk_bytes == 0 || chunk_bytes % 16 || chunk_bytes > kMaxChunk) return LLAR_ERR_INVALID;
+  Ctx c;  // host arithmetic only: no device memory behind it
+  c.n = nranks;
+  c.dtype = dtype;
+  c.esize = elem_bytes(dtype);
+  c.sms = sms;
+  c.chunk_bytes = chunk_bytes;
+  int G = 1, T = 128;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);  // a shape forced by llar_set_launch is read under the lock
+    choose_shape(c, protocol, count, chained ? 1 : 0, &G, &T);
+  }
+  if (ctas_per_rank) *ctas_per_rank = G;
+  if (threads) *threads = T;
+  return LLAR_OK;
+}
+
 const char* llar_strerror(int status) {
   switch (status) {
     case LLAR_OK: return "ok";

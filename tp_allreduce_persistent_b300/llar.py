@@ -90,6 +90,8 @@ def lib():
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
+        "llar_debug_launch_shape": (c_int, [c_int, c_int, c_size, c_int, c_int, c_int, c_size,
+                                            ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
         "llar_strerror": (ctypes.c_char_p, [c_int]),
         "llar_llbuffer_create": (c_int, [c_int, c_size, ctypes.POINTER(LLBufferDesc)]),
         "llar_llbuffer_destroy": (c_int, [ctypes.POINTER(LLBufferDesc)]),
@@ -304,6 +306,15 @@ def llar_last_launch():
     v = [ctypes.c_int() for _ in range(4)]
     lib().llar_last_launch(*[ctypes.byref(x) for x in v])
     return PROTOCOL_NAMES.get(v[0].value, v[0].value), v[1].value, v[2].value, v[3].value
+
+
+def llar_debug_launch_shape(nranks, dtype, count, protocol, chained=False, sms=148, chunk_bytes=64 << 10):
+    """(CTAs per rank, threads per CTA) the launch-shape rule picks; host arithmetic only."""
+    g, t = ctypes.c_int(), ctypes.c_int()
+    _check(lib().llar_debug_launch_shape(int(nranks), _enum(DTYPES, dtype), int(count), _enum(PROTOCOLS, protocol),
+                                         int(bool(chained)), int(sms), int(chunk_bytes), ctypes.byref(g),
+                                         ctypes.byref(t)), "llar_debug_launch_shape")
+    return g.value, t.value
 
 
 # ------------------------------------------------------------ LL buffer API
