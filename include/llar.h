@@ -169,6 +169,25 @@ int llar_sendrecv(const void* const* send, void* const* recv, const int* dst, si
 int llar_allreduce_host(const void* in_host, void* out_host, size_t count,
                         int protocol, void* stream);
 
+/* Register a page-locked host buffer that the device can address (from
+ * cudaHostAlloc, or torch's pin_memory) of `bytes` bytes with the context:
+ * llar_allreduce_host calls whose input and output each lie inside a
+ * registered buffer take its device address from this table instead of
+ * querying the pointers' attributes on every call. (No page describes it;
+ * it trims the host cost of the host-buffer entry.) The caller must
+ * unregister a buffer before freeing it: a freed and reused address left in
+ * the table would hand the kernel memory it cannot reach. At most 64
+ * buffers, none overlapping another. LLAR_ERR_NOT_INIT without a context
+ * (llar_destroy drops the table); LLAR_ERR_INVALID for NULL, zero bytes, an
+ * overlap, a full table, or memory that is not page-locked and
+ * device-addressable. Synchronous; no device work. */
+int llar_host_register(const void* ptr, size_t bytes);
+
+/* Remove the buffer registered at `ptr` (the address given to
+ * llar_host_register). LLAR_ERR_INVALID if none is; LLAR_ERR_NOT_INIT
+ * without a context. */
+int llar_host_unregister(const void* ptr);
+
 /* The status word written by the device: LLAR_OK, or LLAR_ERR_TIMEOUT with
  * the virtual rank, CTA and epoch of the first wait that ran out. Any
  * pointer may be NULL. Reads the word without synchronising. */

@@ -190,6 +190,43 @@ def test_host_buffer_entry_point():
             assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
 
 
+def test_host_buffer_registration():
+    # registered pinned buffers skip the per-call pointer queries; results
+    # are the same, sub-ranges of a registered buffer resolve too, and the
+    # table refuses overlaps, pageable memory and unknown addresses
+    n, dtype, count = 8, "bf16", 8192
+    with context(n, dtype, 1 << 20):
+        x = inputs.normal(n, 2 * count, dtype, seed=11).pin_memory()
+        out = torch.empty_like(x).pin_memory()
+        llar.llar_host_register(x)
+        llar.llar_host_register(out)
+        try:
+            for proto in ("ll", "fixed_twoshot"):
+                for _ in range(2):
+                    llar.llar_allreduce_host(x, out, 2 * count, proto)
+                    torch.cuda.synchronize()
+                    assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
+            # a [n][count] view that starts inside the registered buffers
+            xs = x.view(-1)[count:count + n * count].view(n, count)
+            os_ = out.view(-1)[count:count + n * count].view(n, count)
+            llar.llar_allreduce_host(xs, os_, count, "ll")
+            torch.cuda.synchronize()
+            assert np.array_equal(inputs.bits_of(os_), orc.allreduce(inputs.bits_of(xs.clone()), dtype))
+            with pytest.raises(llar.LlarError):
+                llar.llar_host_register(x.view(-1)[8:], 64)  # overlaps x
+            with pytest.raises(llar.LlarError):
+                llar.llar_host_register(torch.empty(64, dtype=torch.uint8))  # pageable
+        finally:
+            llar.llar_host_unregister(x)
+            llar.llar_host_unregister(out)
+        with pytest.raises(llar.LlarError):
+            llar.llar_host_unregister(x)  # no longer registered
+        # unregistered pinned buffers still work (queried per call)
+        llar.llar_allreduce_host(x, out, 2 * count, "ll")
+        torch.cuda.synchronize()
+        assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
+
+
 def test_host_buffer_entry_point_pageable_and_ragged():
     # pageable host memory (and a row size that is not a multiple of 16
     # bytes) takes the staged-copy path

@@ -21,6 +21,7 @@ constexpr size_t kAlign = 256;
 constexpr size_t kDefaultLLCap = 1u << 20;      // LL messages up to 1 MiB per rank
 constexpr size_t kDefaultLL128Cap = 64u << 20;  // LL128 messages up to 64 MiB per rank
 constexpr size_t kMaxLL128Cap = size_t(1) << 30;  // the LL128 kernels index a CTA's items in 32 bits
+constexpr size_t kMaxHostRegs = 64;               // registered host buffers per context
 constexpr size_t kDefaultChunk = 64u << 10;     // sentinel chunk per rank: every chunk costs a round trip and a fence
 constexpr size_t kMaxChunk = 64u << 10;         // largest sentinel chunk
 constexpr int kFlagsGmax = 1024;                // CTAs per rank the chain flags can address
@@ -52,6 +53,13 @@ struct Ctx {
   // host-API staging
   char* io = nullptr;
   size_t io_stride = 0;
+  // host buffers registered by the caller: host range -> device address
+  struct HostReg {
+    const char* host;
+    size_t bytes;
+    char* dev;
+  };
+  std::vector<HostReg> host_regs;
   // resident-CTA capacity per (protocol, chain, threads, clustered): the
   // occupancy queries cost microseconds, so each is made once
   std::map<long long, int> capacity;
@@ -670,6 +678,26 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
   // Measured against one DMA each way (or DMA in, zero-copy out), this is
   // the fastest of the three for the small messages this entry serves.
   if (bytes % 16 == 0) {
+    // registered buffers: device addresses without per-call queries
+    auto registered = [&](const void* p, size_t len) -> char* {
+      const uintptr_t q = (uintptr_t)p;
+      for (const auto& h : c.host_regs) {
+        const uintptr_t h0 = (uintptr_t)h.host;
+        if (q >= h0 && len <= h.bytes && q - h0 <= h.bytes - len) return h.dev + (q - h0);
+      }
+      return nullptr;
+    };
+    char* rin = registered(in_host, bytes * c.n);
+    char* rout = registered(out_host, bytes * c.n);
+    if (rin && rout && ((((uintptr_t)rin) | ((uintptr_t)rout)) & 15u) == 0) {
+      const void* ins[llar::kMaxRanks];
+      void* outs[llar::kMaxRanks];
+      for (int r = 0; r < c.n; ++r) {
+        ins[r] = rin + r * bytes;
+        outs[r] = rout + r * bytes;
+      }
+      return run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
+    }
     cudaPointerAttributes ai, ao;
     if (cudaPointerGetAttributes(&ai, in_host) == cudaSuccess && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
         ai.type == cudaMemoryTypeHost && ao.type == cudaMemoryTypeHost && ai.devicePointer && ao.devicePointer &&
@@ -712,6 +740,36 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
   err = rows16 ? cudaMemcpyAsync(out_host, dout, bytes * c.n, cudaMemcpyDeviceToHost, s)
                : cudaMemcpy2DAsync(out_host, bytes, dout, c.io_stride, bytes, c.n, cudaMemcpyDeviceToHost, s);
   return cuda_status(err);
+}
+
+int llar_host_register(const void* ptr, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (!ptr || bytes == 0) return LLAR_ERR_INVALID;
+  Ctx& c = *g;
+  if (c.host_regs.size() >= kMaxHostRegs) return LLAR_ERR_INVALID;
+  const uintptr_t q = (uintptr_t)ptr;
+  for (const auto& h : c.host_regs)
+    if (q < (uintptr_t)h.host + h.bytes && (uintptr_t)h.host < q + bytes) return LLAR_ERR_INVALID;  // overlap
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess || a.type != cudaMemoryTypeHost || !a.devicePointer) {
+    cudaGetLastError();
+    return LLAR_ERR_INVALID;  // not page-locked memory the device can address
+  }
+  c.host_regs.push_back({static_cast<const char*>(ptr), bytes, static_cast<char*>(a.devicePointer)});
+  return LLAR_OK;
+}
+
+int llar_host_unregister(const void* ptr) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  auto& regs = g->host_regs;
+  for (size_t i = 0; i < regs.size(); ++i)
+    if (regs[i].host == static_cast<const char*>(ptr)) {
+      regs.erase(regs.begin() + (long)i);
+      return LLAR_OK;
+    }
+  return LLAR_ERR_INVALID;
 }
 
 int llar_get_status(int* rank, int* cta, unsigned long long* epoch) {

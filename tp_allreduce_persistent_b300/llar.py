@@ -90,6 +90,8 @@ def lib():
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
+        "llar_host_register": (c_int, [c_vp, c_size]),
+        "llar_host_unregister": (c_int, [c_vp]),
         "llar_debug_launch_shape": (c_int, [c_int, c_int, c_size, c_int, c_int, c_int, c_size,
                                             ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
         "llar_strerror": (ctypes.c_char_p, [c_int]),
@@ -214,6 +216,17 @@ def llar_allreduce_host(in_host, out_host, count, protocol="auto", stream=None):
                                      int(count), _enum(PROTOCOLS, protocol),
                                      ctypes.c_void_p(_stream(stream))),
            "llar_allreduce_host")
+
+
+def llar_host_register(buf, nbytes=None):
+    """Register a pinned host buffer (tensor or raw pointer + nbytes) for llar_allreduce_host."""
+    if nbytes is None:
+        nbytes = buf.numel() * buf.element_size()
+    _check(lib().llar_host_register(ctypes.c_void_p(_ptr(buf)), int(nbytes)), "llar_host_register")
+
+
+def llar_host_unregister(buf):
+    _check(lib().llar_host_unregister(ctypes.c_void_p(_ptr(buf))), "llar_host_unregister")
 
 
 def llar_allreduce_noalloc(ins, outs, count, nranks, dtype, stream=None):
