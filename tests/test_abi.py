@@ -100,6 +100,11 @@ def test_argument_checks_without_device():
         llar.llar_allreduce([0] * 4, [0] * 4, 16, "ll", stream=0)
     assert ei.value.code == llar.ERR_NOT_INIT
     assert llar.llar_get_status()[0] == llar.ERR_NOT_INIT
+    # the host-buffer table belongs to a context
+    for call in (lambda: llar.llar_host_register(4096, 64), lambda: llar.llar_host_unregister(4096)):
+        with pytest.raises(llar.LlarError) as ei:
+            call()
+        assert ei.value.code == llar.ERR_NOT_INIT
     assert llar.strerror(llar.ERR_TIMEOUT) == "a device-side wait timed out"
 
 
