@@ -134,3 +134,28 @@ def test_ll128_windows_fast_path_equals_element_path(tmp_path):
                    capture_output=True, text=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and "bad 0" in out.stdout, out.stdout + out.stderr
+
+
+# plausible mistakes, each planted in a host copy of the helpers: the check
+# above must fail on every one of them
+MUTATIONS = {
+    "byte permutation": ("0x5432", "0x5410"),
+    "two-word shift": ("x[i] = x[i + 2]", "x[i] = x[i + 1]"),
+    "lane-0 flag element": ("if (!skip0 && (first & 7) == 0)", "if ((first & 7) == 0)"),
+    "segment bound": ("sl0 + V - 1 <= lim", "sl0 + V - 2 <= lim"),
+}
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_ll128_window_check_catches_planted_mistakes(name, tmp_path):
+    old, new = MUTATIONS[name]
+    helpers = _helpers()
+    assert old in helpers, name
+    cpp = tmp_path / "mutant.cpp"
+    cpp.write_text(SHIM + helpers.replace(old, new, 1) + MAIN)
+    exe = tmp_path / "mutant"
+    subprocess.run(["g++", "-O1", "-std=c++17", "-o", str(exe), str(cpp)], check=True,
+                   capture_output=True, text=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode != 0 and "bad 0" not in out.stdout, name
