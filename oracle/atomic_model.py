@@ -9,7 +9,18 @@ summary page, technique 4). This model performs that accumulation for one
 given arrival order: start from zero, and after every add round the partial
 sum to the dtype (an atomic add in the dtype returns a dtype value).
 It is not used to judge the GPU; tests use it to show that
-`allreduce.atomic_tolerance` admits every arrival order and is not vacuous.
+`allreduce.atomic_tolerance` admits every arrival order and is not vacuous,
+and to show where that tolerance stops holding (a 16-bit partial sum that
+overflows).
+
+Pins (tests/test_oracle.py): hand-worked arrival orders in
+tests/golden/atomic_order_cases.json (ties decided by the order, a partial
+that overflows, the +0 start); equality with an exact rational model that
+rounds every partial once, over tie-, subnormal- and overflow-heavy inputs;
+the float32 carrier against exact roundings of values that sit just off a
+midpoint (where rounding to float32 first would double-round); planted
+mistakes (no sticky bit, plain float32 rounding, no step toward zero,
+unrounded partials, ignored order) each fail one of them.
 """
 
 import numpy as np
@@ -24,11 +35,11 @@ def atomic_sum(x_bits, order, dtype):
     with np.errstate(over="ignore", invalid="ignore"):
         for r in order:
             s = (acc + vals[r]).astype(np.float32)
-            # the add of two dtype values, rounded once to the dtype: for
-            # fp16/bf16 the float32 sum of two such values is exact unless
-            # the exponents differ by more than 16, where float32 rounding
-            # followed by dtype rounding could double-round; fall back to
-            # float64 for those elements so the model stays a single rounding.
+            # the add of two dtype values, rounded once to the dtype. For
+            # fp16/bf16 the model takes the float64 sum and a float32
+            # carrier that rounds to the dtype like the float64 value does,
+            # so that there is visibly one rounding. (A float32 sum would also
+            # round innocuously here: 24 >= 2p + 2 for p = 11 and 8.)
             if dtype != fp.FP32:
                 s64 = acc.astype(np.float64) + vals[r].astype(np.float64)
                 s = _round64(s64, dtype)

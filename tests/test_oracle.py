@@ -302,6 +302,208 @@ def test_atomic_model_of_identical_values_matches_oracle():
         assert np.array_equal(atomic_model.atomic_sum(x, order, "fp32"), orc.allreduce(x, "fp32")[0])
 
 
+# ----------------------------------------------- atomic model: exact pins
+ATOMIC_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "atomic_order_cases.json")
+FORMAT = {"fp32": (24, -126, 127), "fp16": (11, -14, 15), "bf16": (8, -126, 127)}
+
+
+def _bits_of_value(v, dtype):
+    """Bits of a value that the format holds exactly (no rounding happens)."""
+    if dtype == "fp16":
+        return int(np.array([v], np.float16).view(np.uint16)[0])
+    u = int(np.array([v], np.float32).view(np.uint32)[0])
+    return u >> 16 if dtype == "bf16" else u
+
+
+def _round_exact(q, neg_zero, dtype):
+    """roundTiesToEven of the rational q to `dtype`, from the definition
+    (IEEE 754-2008 4.3.1, 7.4); returns bits. An exact zero keeps the sign
+    IEEE 6.3 gives it (neg_zero)."""
+    p, emin, emax = FORMAT[dtype]
+    if q == 0:
+        return _bits_of_value(-0.0 if neg_zero else 0.0, dtype)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, emin)  # subnormals share the quantum of the smallest binade
+    quantum = Fraction(2) ** (e - p + 1)
+    m = a / quantum
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    v = n * quantum
+    if v >= Fraction(2) ** (emax + 1):
+        return _bits_of_value(sign * float("inf"), dtype)
+    return _bits_of_value(sign * float(v), dtype)
+
+
+def _exact_atomic_sum(x_bits, order, dtype):
+    """Per element: start from +0, add the ranks in `order`, each sum exact
+    as a rational and then rounded once to `dtype` (finite inputs; a partial
+    that overflows stays infinite)."""
+    vals = fp.decode(x_bits, dtype).astype(np.float64)
+    out = []
+    for i in range(vals.shape[1]):
+        acc, neg, inf = Fraction(0), False, 0.0
+        for r in order:
+            xv = float(vals[r, i])
+            if inf:
+                continue
+            xneg = xv == 0 and np.signbit(xv)
+            s = acc + Fraction(xv)
+            neg = s == 0 and neg and xneg
+            bits = _round_exact(s, neg, dtype)
+            v = float(fp.decode(np.array([bits], fp.BITS_DTYPE[dtype]), dtype)[0])
+            if np.isinf(v):
+                inf = v
+            else:
+                acc = Fraction(v)
+        out.append(_bits_of_value(inf, dtype) if inf else _round_exact(acc, neg, dtype))
+    return np.array(out, dtype=fp.BITS_DTYPE[dtype])
+
+
+def _hard_atomic_inputs(n, count, dtype, seed):
+    """Finite values built to hit ties, subnormals, cancellation and the
+    overflow threshold: a shared magnitude per element with small offsets,
+    random exponents over the whole range, and halves of the spacing."""
+    p, emin, emax = FORMAT[dtype]
+    rng = np.random.default_rng(seed)
+    base = rng.integers(emin - p + 2, emax + 1, count)
+    kind = rng.integers(0, 4, (n, count))
+    x = np.zeros((n, count), np.float64)
+    for r in range(n):
+        for i in range(count):
+            mant = 1.0 + rng.integers(0, 2 ** (p - 1)) / 2.0 ** (p - 1)
+            sgn = -1.0 if rng.random() < 0.4 else 1.0
+            k = kind[r, i]
+            if k == 0:  # same binade as the element's base
+                ex = base[i]
+            elif k == 1:  # half a spacing of the base binade, or a few spacings
+                ex = base[i] - p + int(rng.integers(0, 3))
+            elif k == 2:  # anywhere in the range, subnormals included
+                ex = int(rng.integers(emin - p + 1, emax + 1))
+            else:
+                ex = base[i] - int(rng.integers(0, p + 3))
+            x[r, i] = sgn * np.ldexp(mant, int(ex))
+    bits = fp.encode_rne(x.astype(np.float32), dtype)
+    vals = fp.decode(bits, dtype)
+    return np.where(np.isfinite(vals), bits, np.zeros_like(bits))
+
+
+@pytest.mark.parametrize("dtype", fp.DTYPES)
+def test_atomic_model_equals_exact_per_add_rounding(dtype):
+    # every partial sum rounded once to the element type, checked against
+    # exact rational arithmetic for several arrival orders
+    rng = np.random.default_rng(41)
+    for n, count, seed in ((2, 300, 1), (5, 200, 2), (8, 150, 3)):
+        x = _hard_atomic_inputs(n, count, dtype, seed)
+        for _ in range(3):
+            order = [int(v) for v in rng.permutation(n)]
+            got = atomic_model.atomic_sum(x, order, dtype)
+            want = _exact_atomic_sum(x, order, dtype)
+            assert np.array_equal(got, want), (dtype, n, order)
+
+
+def _atomic_golden_orders_hold(fn):
+    for c in json.load(open(ATOMIC_GOLDEN))["orders"]:
+        dt = c["dtype"]
+        x = np.stack([_bits_array(r, dt) for r in c["inputs"]])
+        got = fn(x, c["order"], dt)
+        if [hex(v) for v in got] != [hex(v) for v in _bits_array(c["expected"], dt)]:
+            return False
+    return True
+
+
+def _carrier_golden_holds(fn):
+    for c in json.load(open(ATOMIC_GOLDEN))["carrier"]["cases"]:
+        v = np.array([sum(s * 2.0 ** k for s, k in c["terms"])], np.float64)
+        exact = sum(Fraction(s) * Fraction(2) ** k for s, k in c["terms"])
+        assert float(exact) == v[0]  # the float64 literal holds the value exactly
+        got = int(fp.encode_rne(fn(v, c["dtype"]), c["dtype"])[0])
+        if got != int(c["expected"], 16):
+            return False
+    return True
+
+
+def test_atomic_model_golden_orders():
+    assert _atomic_golden_orders_hold(atomic_model.atomic_sum)
+    # and the exact model agrees with the hand-worked values
+    assert _atomic_golden_orders_hold(_exact_atomic_sum)
+
+
+def test_atomic_golden_overflow_case_breaks_the_tolerance():
+    # reading: 16-bit atomics round every partial in the element type, so a
+    # partial that passes the largest finite value becomes inf even where the
+    # float32 sum is finite; the tolerance only holds while sum |x| stays
+    # below the overflow threshold
+    x = np.stack([_bits_array(["7a00"], "fp16"), _bits_array(["7a00"], "fp16"), _bits_array(["fa00"], "fp16")])
+    want = orc.allreduce(x, "fp16")
+    bad = atomic_model.atomic_sum(x, [0, 1, 2], "fp16")
+    good = atomic_model.atomic_sum(x, [0, 2, 1], "fp16")
+    assert not orc.compare_atomic(np.stack([bad] * 3), want, x, "fp16")[0]
+    assert orc.compare_atomic(np.stack([good] * 3), want, x, "fp16")[0]
+
+
+def test_carrier_rounds_like_the_exact_value():
+    assert _carrier_golden_holds(atomic_model._round64)
+
+
+def test_float32_sum_of_two_16bit_values_rounds_innocuously():
+    # why the carrier is only reachable through its own pins: float32 has
+    # p32 = 24 >= 2 p + 2 bits for fp16 (p = 11) and bf16 (p = 8), so a
+    # float32 sum of two such values followed by rounding to the format is
+    # the correctly rounded sum (innocuous double rounding, Figueroa 1995)
+    rng = np.random.default_rng(43)
+    for dtype in ("fp16", "bf16"):
+        x = _hard_atomic_inputs(2, 3000, dtype, 44)
+        s32 = (fp.decode(x[0], dtype) + fp.decode(x[1], dtype)).astype(np.float32)
+        with np.errstate(over="ignore"):
+            got = fp.encode_rne(s32, dtype)
+        want = _exact_atomic_sum(x, [0, 1], dtype)
+        vals = fp.decode(x, dtype)
+        nz = (vals[0] != 0) | (vals[1] != 0)  # signed zeros: both rules agree, skip the start value
+        assert np.array_equal(got[nz], want[nz]), dtype
+    del rng
+
+
+def test_atomic_model_pins_catch_planted_mistakes():
+    # each plausible mistake in the model fails at least one pin above
+    def no_sticky(v, dtype):
+        v = np.asarray(v, dtype=np.float64)
+        f = v.astype(np.float32)
+        over = np.abs(f.astype(np.float64)) > np.abs(v)
+        return np.where(over, np.nextafter(f, np.float32(0)), f)
+
+    def double_rounding(v, dtype):
+        return np.asarray(v, dtype=np.float64).astype(np.float32)
+
+    def sticky_without_toward_zero(v, dtype):
+        v = np.asarray(v, dtype=np.float64)
+        f = v.astype(np.float32)
+        inexact = f.astype(np.float64) != v
+        return (f.view(np.uint32) | inexact.astype(np.uint32)).view(np.float32)
+
+    for bad in (no_sticky, double_rounding, sticky_without_toward_zero):
+        assert not _carrier_golden_holds(bad), bad.__name__
+
+    def unrounded_partials(x_bits, order, dtype):  # one rounding at the end
+        vals = fp.decode(np.asarray(x_bits), dtype).astype(np.float64)
+        acc = np.zeros(vals.shape[1])
+        for r in order:
+            acc = acc + vals[r]
+        return fp.encode_rne(atomic_model._round64(acc, dtype) if dtype != "fp32"
+                             else acc.astype(np.float32), dtype)
+
+    def ignores_order(x_bits, order, dtype):
+        return atomic_model.atomic_sum(x_bits, sorted(order), dtype)
+
+    for bad in (unrounded_partials, ignores_order):
+        assert not _atomic_golden_orders_hold(bad), bad.__name__
+
+
 # -------------------------------------------------------- protocol constants
 def test_ll_line_halves_bandwidth_and_doubles_staging():
     assert protocol.ll_payload_fraction() == 0.5
