@@ -126,7 +126,7 @@ def allreduce_iters(x_bits, iters, dtype, chain_scale=0.0):
     return np.stack(outs, axis=0)
 
 
-def atomic_tolerance(x_bits, dtype):
+def atomic_tolerance(x_bits, dtype, flush_subnormals=False):
     """Per-element bound for paths that sum with atomics in any order.
 
     The LL128 path adds the N contributions with floating-point atomics in
@@ -136,14 +136,23 @@ def atomic_tolerance(x_bits, dtype):
     taken at sum_r |x_r| (reading: a sum with cancellation has a tiny
     result whose own ulp says nothing about the rounding of the partial
     sums; sum |x_r| bounds every partial sum).
+
+    flush_subnormals: the atomic additions treat a subnormal operand as zero
+    and return zero for a subnormal result (the page leaves the atomics'
+    arithmetic open; float32 atomic adds on the GPU work that way). Each of
+    the N additions then moves by less than the smallest normal 2^emin
+    twice (its operand, its result), so 2 N 2^emin is added to the bound.
     """
     x_bits = np.asarray(x_bits)
     n = x_bits.shape[0]
     mag = np.sum(np.abs(fp.decode(x_bits, dtype).astype(np.float64)), axis=0)
-    return (n - 1) * fp.ulp(mag, dtype)
+    tol = (n - 1) * fp.ulp(mag, dtype)
+    if flush_subnormals:
+        tol = tol + 2 * n * 2.0 ** fp.EMIN[dtype]
+    return tol
 
 
-def compare_atomic(got_bits, want_bits, x_bits, dtype):
+def compare_atomic(got_bits, want_bits, x_bits, dtype, flush_subnormals=False):
     """Check an order-free result against the oracle within `atomic_tolerance`.
 
     Returns (ok, max_abs_err, max_err_in_tolerances). Infinities and NaNs
@@ -151,7 +160,7 @@ def compare_atomic(got_bits, want_bits, x_bits, dtype):
     """
     got = fp.decode(got_bits, dtype).astype(np.float64)
     want = fp.decode(want_bits, dtype).astype(np.float64)
-    tol = np.broadcast_to(atomic_tolerance(x_bits, dtype), want.shape)
+    tol = np.broadcast_to(atomic_tolerance(x_bits, dtype, flush_subnormals), want.shape)
     nan_ok = np.isnan(got) == np.isnan(want)
     inf_ok = np.where(np.isinf(want) | np.isinf(got), got == want, True)
     finite = np.isfinite(got) & np.isfinite(want)

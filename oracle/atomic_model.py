@@ -28,22 +28,35 @@ import numpy as np
 from . import fpformats as fp
 
 
-def atomic_sum(x_bits, order, dtype):
-    """Sum rows of x_bits ([N, count] raw bits) in `order`, rounding each add."""
+def _flush(v, dtype):
+    """Subnormal values of the format -> zero of the same sign."""
+    tiny = np.abs(v) < np.float32(2.0 ** fp.EMIN[dtype])
+    return np.where(tiny, np.copysign(np.float32(0), v), v).astype(np.float32)
+
+
+def atomic_sum(x_bits, order, dtype, flush_subnormals=False):
+    """Sum rows of x_bits ([N, count] raw bits) in `order`, rounding each add.
+
+    flush_subnormals: each addition reads a subnormal operand as zero and
+    returns zero for a subnormal result (sign kept), as float32 atomic adds
+    on the GPU do."""
     vals = fp.decode(np.asarray(x_bits), dtype)
     acc = np.zeros(vals.shape[1], dtype=np.float32)
     with np.errstate(over="ignore", invalid="ignore"):
         for r in order:
-            s = (acc + vals[r]).astype(np.float32)
+            xr = _flush(vals[r], dtype) if flush_subnormals else vals[r]
+            s = (acc + xr).astype(np.float32)
             # the add of two dtype values, rounded once to the dtype. For
             # fp16/bf16 the model takes the float64 sum and a float32
             # carrier that rounds to the dtype like the float64 value does,
             # so that there is visibly one rounding. (A float32 sum would also
             # round innocuously here: 24 >= 2p + 2 for p = 11 and 8.)
             if dtype != fp.FP32:
-                s64 = acc.astype(np.float64) + vals[r].astype(np.float64)
+                s64 = acc.astype(np.float64) + xr.astype(np.float64)
                 s = _round64(s64, dtype)
             acc = fp.decode(fp.encode_rne(s, dtype), dtype)
+            if flush_subnormals:
+                acc = _flush(acc, dtype)
     return fp.encode_rne(acc, dtype)
 
 

@@ -469,6 +469,45 @@ def test_float32_sum_of_two_16bit_values_rounds_innocuously():
     del rng
 
 
+def test_flushing_atomic_model_golden_cases():
+    # the flush reading of float32 atomic adds: hand-worked cases, the plain
+    # tolerance rejects them, the flush-aware one admits them
+    for c in json.load(open(ATOMIC_GOLDEN))["flush"]["cases"]:
+        dt = c["dtype"]
+        x = np.stack([_bits_array(r, dt) for r in c["inputs"]])
+        got = atomic_model.atomic_sum(x, c["order"], dt, flush_subnormals=True)
+        assert [hex(v) for v in got] == [hex(v) for v in _bits_array(c["expected"], dt)], c["name"]
+        want = orc.allreduce(x, dt)
+        assert [hex(v) for v in want[0]] == [hex(v) for v in _bits_array(c["oracle"], dt)], c["name"]
+        ys = np.stack([got] * x.shape[0])
+        assert orc.compare_atomic(ys, want, x, dt, flush_subnormals=True)[0], c["name"]
+        assert orc.compare_atomic(ys, want, x, dt)[0] == c["plain_tolerance_admits"], c["name"]
+
+
+def test_flush_aware_tolerance_admits_every_order_and_still_rejects_a_lost_term():
+    rng = np.random.default_rng(45)
+    n, count = 8, 3000
+    # subnormal-heavy float32 data: subnormals, values near the smallest
+    # normal of both signs, and a few ordinary ones
+    mags = np.where(rng.random((n, count)) < 0.6,
+                    rng.integers(1, 2 ** 23, (n, count)),
+                    rng.integers(2 ** 23, 2 ** 25, (n, count))).astype(np.uint32)
+    sign = np.where(rng.random((n, count)) < 0.5, np.uint32(0x80000000), np.uint32(0))
+    x = mags | sign
+    x[:, :50] = fp.encode_rne(rng.standard_normal((n, 50)).astype(np.float32), "fp32")
+    want = orc.allreduce(x, "fp32")
+    needed = False
+    for _ in range(6):
+        order = [int(v) for v in rng.permutation(n)]
+        got = np.stack([atomic_model.atomic_sum(x, order, "fp32", flush_subnormals=True)] * n)
+        assert orc.compare_atomic(got, want, x, "fp32", flush_subnormals=True)[0]
+        needed |= not orc.compare_atomic(got, want, x, "fp32")[0]
+    assert needed  # the plain bound alone would not admit the flushing adds
+    lost = np.stack([orc.allreduce(x[:7], "fp32")[0]] * n)
+    lost_ok = orc.compare_atomic(lost[:, :50], want[:, :50], x[:, :50], "fp32", flush_subnormals=True)[0]
+    assert not lost_ok
+
+
 def test_atomic_model_pins_catch_planted_mistakes():
     # each plausible mistake in the model fails at least one pin above
     def no_sticky(v, dtype):
