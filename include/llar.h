@@ -28,6 +28,17 @@
  * element type, so its result is bit-identical to that definition.
  * LL128_ATOMIC adds with floating-point atomics in the element type in
  * arrival order; its result is not deterministic (technique 4 says so).
+ * Its bound: per element, |result - rank-order sum| <= (N-1) ulp of the
+ * element type at sum_r |x_r|, with two limits:
+ *  - float32: the GPU's float32 atomic add reads a subnormal operand as
+ *    zero and returns zero for a subnormal result, so on subnormal data the
+ *    error can grow by up to 2 N 2^-126 (an all-subnormal column sums to
+ *    +0); fp16 and bf16 use the non-flushing (.noftz) atomics;
+ *  - fp16 / bf16: every partial sum is rounded in the element type, so the
+ *    bound holds while sum_r |x_r| <= max - N ulp(max) / 2 (fp16 at 8
+ *    ranks: 65376); beyond it, with cancelling values, a partial sum can
+ *    overflow to an infinity where the float32 sum is finite (in the
+ *    arrival orders that add same-signed values first).
  *
  * Errors: calls return an llar_status_t. Invalid arguments are rejected
  * before any device work. Every device-side wait is bounded by a timeout
@@ -296,9 +307,18 @@ int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, i
  * any stream capture. Every call shares the array: calls that overlap on
  * the GPU (other streams, other threads) race and must be avoided; calls
  * in one stream are safe. Each call uses a fresh epoch, so no clearing is
- * needed between calls. A device wait that ran out in an earlier call is
- * returned as LLAR_ERR_TIMEOUT by a later call made once the stream is
- * idle (checked with cudaStreamQuery; a 4-byte device-to-host copy). */
+ * needed between calls. Device waits are bounded by llar_set_timeout_ns
+ * and honour llar_debug_inject, as the context's launches do. A wait that
+ * runs out sets an abort word in the array, and the call's outputs are
+ * invalid. The host learns of it only later: the first call made while
+ * `stream` is idle (cudaStreamQuery, then a 4-byte device-to-host copy and
+ * a stream synchronisation, paid by every call on an idle stream) returns
+ * LLAR_ERR_TIMEOUT once, clears the word and launches nothing; the next
+ * call works normally. Calls queued while the stream was still busy
+ * (between the call whose wait ran out and the one that reports it) find
+ * the abort word set, give up their waits at once, return LLAR_OK and
+ * also leave invalid outputs. No check is made while `stream` is being
+ * captured. */
 int llar_allreduce_noalloc(const void* const* in, void* const* out, size_t count,
                            int nranks, int dtype, void* stream);
 
