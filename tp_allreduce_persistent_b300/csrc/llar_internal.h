@@ -85,6 +85,11 @@ struct Params {
   DevStatus* status;         // mapped host memory (device pointer)
 };
 
+// Process-wide wait bound (llar_set_timeout_ns) and fault injection
+// (llar_debug_inject), for launches made outside the context (defined in
+// llar_runtime.cu).
+void fault_settings(unsigned long long* timeout_ns, int* inject_rank, int* inject_mode);
+
 // Launchers, defined in llar_kernels.cu. Return a cudaError_t.
 cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_t s);

@@ -2164,6 +2164,7 @@ struct NoAllocDevice {
   bool ready = false;
   char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sms = 0;
+  int cap[3][kMaxRanks + 1] = {};  // resident-CTA capacity per (dtype, ranks), queried once
 };
 NoAllocDevice g_noalloc[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
@@ -2208,8 +2209,15 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
     d.ready = true;
   }
   // a wait that ran out in an earlier call is reported once that call has
-  // drained from the stream; the word is then cleared
-  if (cudaStreamQuery(s) == cudaSuccess) {
+  // drained from the stream; the word is then cleared. A stream that is
+  // being captured must not be queried (the query would invalidate the
+  // capture), so the check waits for a later call there.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+    cudaGetLastError();
+    capture = cudaStreamCaptureStatusActive;  // unknown: treat as capturing, skip the check
+  }
+  if (capture == cudaStreamCaptureStatusNone && cudaStreamQuery(s) == cudaSuccess) {
     unsigned word = 0;
     if (cudaMemcpyAsync(&word, d.scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
@@ -2221,7 +2229,7 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
       cudaMemsetAsync(d.scratch + 256, 0, 256, s);  // status
       return LLAR_ERR_TIMEOUT;
     }
-  } else {
+  } else if (capture == cudaStreamCaptureStatusNone) {
     cudaGetLastError();  // cudaErrorNotReady: still busy, check on a later call
   }
 
@@ -2239,8 +2247,8 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
   p.ll = d.scratch + kNoAllocHeader;
   p.ll_stride = kNoAllocRankBytes;
   p.ll_slot_words = kNoAllocWords;
-  p.timeout_ns = 1000000000ull;
-  p.inject_rank = -1;
+  fault_settings(&p.timeout_ns, &p.inject_rank, &p.inject_mode);  // as llar_set_timeout_ns / llar_debug_inject
+  if (p.inject_rank >= nranks) p.inject_rank = -1;
   p.abort_flag = reinterpret_cast<unsigned*>(d.scratch);
   p.status = reinterpret_cast<DevStatus*>(d.scratch + 256);
   const size_t words = (bytes + 7) / 8;
@@ -2250,7 +2258,8 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
   const int one_per_sm = d.sms / nranks > 0 ? d.sms / nranks : 1;
   G = G > one_per_sm ? one_per_sm : G;
   p.clustered = 0;  // the LL kernel runs faster with its CTAs spread over the GPU
-  const int cap = max_resident_ctas(1, dtype, nranks, threads, false, 0);
+  int& cap = d.cap[dtype][nranks];  // an occupancy query costs microseconds: once per shape
+  if (cap <= 0) cap = max_resident_ctas(1, dtype, nranks, threads, false, 0);
   if (cap <= 0) return LLAR_ERR_CUDA;
   if (nranks * G > cap) G = cap / nranks > 0 ? cap / nranks : 1;
   p.G = G;

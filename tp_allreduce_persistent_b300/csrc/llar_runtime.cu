@@ -540,6 +540,15 @@ int fill_staging(Ctx& c, cudaStream_t s) {
 
 }  // namespace
 
+namespace llar {
+void fault_settings(unsigned long long* timeout_ns, int* inject_rank, int* inject_mode) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *timeout_ns = g_timeout_ns;
+  *inject_rank = g_inject_rank;
+  *inject_mode = g_inject_mode;
+}
+}  // namespace llar
+
 extern "C" {
 
 int llar_init(int nranks, int dtype, size_t max_bytes) {
