@@ -239,8 +239,32 @@ def latency_leg(args, llar, inputs, torch, dev, stream, flush, pg, local):
     if code != llar.OK:
         raise RuntimeError(f"device status {code} during the latency leg")
     step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    dep = dependent_chain_us(args, llar, torch, ins, outs, stream, flush)
     return {"us_per_ar": step_ms * 1e3 / iters, "step_ms": step_ms, "proto": used_proto,
-            "G": g, "T": t, "wall_s": wall, "x": x}
+            "G": g, "T": t, "wall_s": wall, "x": x, "dependent": dep}
+
+
+def dependent_chain_us(args, llar, torch, ins, outs, stream, flush):
+    """The same shape as a chain of DEPENDENT AllReduces in one persistent
+    launch: each one's input is 1/N times the previous output (rounded), so
+    no AllReduce can start before the previous one has finished everywhere
+    and the values stay put. Microseconds per AllReduce, mean over steps."""
+    iters, proto = args.iters, args.protocol
+    for _ in range(max(1, args.warmup)):
+        llar.llar_allreduce_iters(ins, outs, COUNT, proto, iters, 0, 0, 1.0 / NRANKS)
+    torch.cuda.synchronize()
+    used = llar.llar_last_launch()
+    ev = _events(args.steps)
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        llar.llar_allreduce_iters(ins, outs, COUNT, proto, iters, 0, 0, 1.0 / NRANKS)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    if llar.llar_get_status()[0] != llar.OK:
+        raise RuntimeError("device status not ok in the dependent chain")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return {"us_per_ar": ms * 1e3 / iters, "proto": used[0], "G": used[1], "T": used[2]}
 
 
 def bandwidth_leg(args, llar, torch, dev, stream, pg, local):
@@ -378,6 +402,14 @@ def configs_leg(llar, torch, dev, stream):
                       for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")}
             for n in (4, 8)},
     }
+    # the headline shape as a chain of dependent AllReduces (input of each =
+    # RNE(previous output / 8)), every protocol
+    out["dependent_chain_8ranks_16KiB_bf16_us"] = {
+        p: timed(8, "bf16", 8192, p, 2000, chain=1.0 / 8) for p in ("ll", "sentinel", "ll128", "fixed_oneshot",
+                                                                   "fixed_twoshot")}
+    out["C2_mode_b_graph_10000_launches_4ranks_16KiB_bf16_us"] = {
+        p: mode_b_us(llar, torch, dev, stream, p) for p in ("ll", "sentinel")}
+    out["noalloc_8ranks_16KiB_bf16"] = noalloc_rows(llar, torch, dev, stream)
     # single calls, one launch each, replayed from a CUDA graph of 200 calls
     # (GPU time per call including launch gaps, without host overhead)
     def graph_call_us(kind, proto, n=8, count=8192, dtype="bf16"):
@@ -450,6 +482,91 @@ def configs_leg(llar, torch, dev, stream):
         sweep[f"{mib}MiB"] = {"us": us, "GB/s": round(2 * 8 * count * 2 / (us * 1e-6) / 1e9, 1)}
     out["C5_sweep_8ranks_bf16_fixed_twoshot"] = sweep
     return out
+
+
+def mode_b_us(llar, torch, dev, stream, proto, n=4, count=8192, launches=10000):
+    """C2 Mode B: a CUDA graph of `launches` single-AllReduce launches of
+    N=4 x 16 KiB bf16 on the same buffers, replayed; microseconds per launch
+    including the gaps between launches (no host overhead)."""
+    llar.llar_init(n, "bf16", count * 2)
+    try:
+        llar.llar_set_sentinel_chunk(16384)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(torch.bfloat16) for _ in range(n)]
+        outs = [torch.empty_like(t) for t in ins]
+        llar.llar_allreduce(ins, outs, count, proto)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(launches):
+                llar.llar_allreduce(ins, outs, count, proto)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if llar.llar_get_status()[0] != llar.OK:
+            raise RuntimeError("device status not ok")
+        del g
+        return round(a.elapsed_time(b) * 1e3 / launches, 3)
+    finally:
+        llar.llar_destroy()
+
+
+def noalloc_rows(llar, torch, dev, stream, n=8, count=8192, calls=2000):
+    """The allocation-free entry point against llar_allreduce (LL, 8 ranks
+    x 16 KiB bf16): GPU time per call when calls are queued back to back
+    (the stream stays busy, so the allocation-free call skips its status
+    check), and host wall time per call when every call is followed by a
+    stream synchronisation (each allocation-free call then finds the stream
+    idle and pays its status check: a 4-byte copy and a synchronisation)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(torch.bfloat16) for _ in range(n)]
+    outs = [torch.empty_like(t) for t in ins]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def queued(fn):
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(calls):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / calls
+
+    def synced(fn, reps=500):
+        for _ in range(20):
+            fn()
+            torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+            torch.cuda.synchronize()
+        return (time.perf_counter() - t0) * 1e6 / reps
+
+    def noalloc():
+        llar.llar_allreduce_noalloc(ins, outs, count, n, "bf16")
+
+    def regular():
+        llar.llar_allreduce(ins, outs, count, "ll")
+
+    rows = {"noalloc_queued_us": round(queued(noalloc), 3),
+            "noalloc_sync_each_host_us": round(synced(noalloc), 3)}
+    llar.llar_init(n, "bf16", count * 2)
+    try:
+        rows["allreduce_queued_us"] = round(queued(regular), 3)
+        rows["allreduce_sync_each_host_us"] = round(synced(regular), 3)
+        if llar.llar_get_status()[0] != llar.OK:
+            raise RuntimeError("device status not ok")
+    finally:
+        llar.llar_destroy()
+    return rows
 
 
 def llbuffer_rows(llar, torch, dev, stream):
@@ -637,11 +754,19 @@ def run_ours(args, world, rank, local, pg):
                                    f"{args.iters} back-to-back per persistent launch",
                        "nranks": NRANKS, "count": COUNT, "iters_per_launch": args.iters,
                        "protocol": lat["proto"], "ctas_per_rank": lat["G"], "threads_per_cta": lat["T"]})
+        dep_us = max_over_ranks(pg, lat["dependent"]["us_per_ar"], dev)
         res["latency_roofline"] = {
             "kernel": f"k_{lat['proto']}<bf16>", "bound": "latency (L2 round trips)",
             "achieved_us": round(us, 4), "sol_us": round(sol_us, 4),
+            "achieved_kind": "per-AllReduce throughput: independent AllReduces back to back in one "
+                             "launch, the next one's lines leave before this one's reduction",
             "l2_round_trip_us": round(l2_us, 4), "write_us": round(write_us, 4),
             "frac": round(sol_us / us, 4), "within_2x_sol": bool(us <= 2 * sol_us),
+            "dependent": {"us_per_ar": round(dep_us, 4), "frac": round(sol_us / dep_us, 4),
+                          "within_2x_sol": bool(dep_us <= 2 * sol_us),
+                          "kernel": f"k_{lat['dependent']['proto']}<bf16> (chain)",
+                          "kind": f"latency: {args.iters} dependent AllReduces per launch, each input "
+                                  "= RNE(output of the previous one / 8)"},
             "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run",
             "probe_ns_min_median_max": {"l2_chase_per_sm": spread(detail["chase_ns"]),
                                         "pingpong_round_trip_per_pair": spread(detail["rt_ns"])}}
@@ -697,6 +822,49 @@ def time_oracle(seconds, count=COUNT, nranks=NRANKS):
             return el * 1e6 / n, n
 
 
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_partitioned(orc, xb, bounds, pool, out):
+    """The oracle's AllReduce on element ranges [bounds[i], bounds[i+1]),
+    one range per worker thread (numpy releases the GIL inside its loops);
+    the arithmetic per element is unchanged, so the bits are the same."""
+    def one(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        out[:, lo:hi] = orc.allreduce(xb[:, lo:hi], DTYPE)
+    list(pool.map(one, range(len(bounds) - 1)))
+    return out
+
+
+def time_oracle_all_cores(seconds, count=COUNT, nranks=NRANKS):
+    """The same AllReduces, element-partitioned over every host core the
+    process may use; returns (us per AllReduce, AllReduces, threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    from oracle import allreduce as orc
+    from tp_allreduce_persistent_b300 import inputs
+    cores = host_cores()
+    xb = inputs.bits_of(inputs.normal(nranks, count, DTYPE, seed=1, scale=0.02))
+    bounds = [count * i // cores for i in range(cores + 1)]
+    out = np.empty_like(xb)
+    with ThreadPoolExecutor(cores) as pool:
+        oracle_partitioned(orc, xb, bounds, pool, out)
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle_partitioned(orc, xb, bounds, pool, out)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return el * 1e6 / n, n, cores
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -735,9 +903,15 @@ def main():
     if rank == 0 and res is not None:  # the llbuffer and config legs print their own line
         if not args.no_cpu_baseline:
             us, n = time_oracle(10.0)
+            us_all, n_all, cores = time_oracle_all_cores(5.0)
             res["cpu_baseline"] = {"value": round(us, 3), "unit": "us", "cores": 1, "kind": "oracle",
                                    "sample": f"{n} oracle AllReduces of the latency workload in ~10 s "
-                                             "on one host core (numpy, single-threaded)"}
+                                             "on one host core (numpy, single-threaded)",
+                                   "nproc": os.cpu_count(),
+                                   "all_cores": {"value": round(us_all, 3), "unit": "us", "cores": cores,
+                                                 "sample": f"{n_all} oracle AllReduces of the latency "
+                                                           f"workload in ~5 s, elements split over "
+                                                           f"{cores} threads (same bits)"}}
         print(json.dumps(res), flush=True)
     if pg is not None:
         pg.destroy_process_group()

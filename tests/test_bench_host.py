@@ -84,3 +84,24 @@ def test_config_cases_parse_and_match_the_table_rows():
     assert bench.CONFIG_CASES["C3_ll128_1MiB"][:4] == (8, "bf16", 1 << 19, "ll128")
     with pytest.raises(SystemExit):
         bench.parse(["--leg", "config", "--case", "no_such_row"])
+
+
+def test_all_core_oracle_gives_the_same_bits():
+    # the element-partitioned timing of the CPU baseline computes exactly the
+    # single-threaded oracle's result, for ragged splits too
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    from oracle import allreduce as orc
+    from tp_allreduce_persistent_b300 import inputs
+    xb = inputs.bits_of(inputs.normal(8, 1003, "bf16", seed=1, scale=0.02))
+    want = orc.allreduce(xb, "bf16")
+    for parts in (1, 3, 7, 16):
+        bounds = [1003 * i // parts for i in range(parts + 1)]
+        out = np.zeros_like(xb)
+        with ThreadPoolExecutor(parts) as pool:
+            got = bench.oracle_partitioned(orc, xb, bounds, pool, out)
+        assert np.array_equal(got, want), parts
+    us, n, cores = bench.time_oracle_all_cores(0.05, count=512, nranks=4)
+    assert us > 0 and n >= 1 and cores == bench.host_cores()
