@@ -57,7 +57,7 @@ def parse(argv=None):
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
-    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer", "config"],
+    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer", "config", "polls"],
                     help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone; "
                          "config: one row of the per-configuration table (--case)")
     ap.add_argument("--case", default="C4_sentinel", choices=sorted(CONFIG_CASES) + sorted(FUSED_CASES),
@@ -239,9 +239,10 @@ def latency_leg(args, llar, inputs, torch, dev, stream, flush, pg, local):
     if code != llar.OK:
         raise RuntimeError(f"device status {code} during the latency leg")
     step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    placed = llar.llar_sol_probe_placed()  # over the CTAs a launch of this shape places
     dep = dependent_chain_us(args, llar, torch, ins, outs, stream, flush)
     return {"us_per_ar": step_ms * 1e3 / iters, "step_ms": step_ms, "proto": used_proto,
-            "G": g, "T": t, "wall_s": wall, "x": x, "dependent": dep}
+            "G": g, "T": t, "wall_s": wall, "x": x, "dependent": dep, "placed": placed}
 
 
 def dependent_chain_us(args, llar, torch, ins, outs, stream, flush):
@@ -662,6 +663,64 @@ def llbuffer_rows(llar, torch, dev, stream):
     return res
 
 
+# poll-count cases: (ranks, dtype, elements per rank, protocol, AllReduces
+# per launch, chain scale, sentinel chunk bytes)
+POLL_CASES = {
+    "ll_8ranks_16KiB_bf16": (8, "bf16", 8192, "ll", 1000, 0.0, None),
+    "ll_8ranks_16KiB_bf16_dependent": (8, "bf16", 8192, "ll", 1000, 1.0 / 8, None),
+    "sentinel_8ranks_16KiB_bf16": (8, "bf16", 8192, "sentinel", 1000, 0.0, None),
+    "sentinel_C4_8ranks_64KiB_fp16_8KiB_chunks": (8, "fp16", 32768, "sentinel", 200, 0.0, 8192),
+    "ll128_8ranks_16KiB_bf16": (8, "bf16", 8192, "ll128", 1000, 0.0, None),
+    "ll128_8ranks_1MiB_bf16": (8, "bf16", 1 << 19, "ll128", 100, 0.0, None),
+}
+
+
+def polls_leg(llar, torch, dev):
+    """Polling per AllReduce, counted by the poll-counting build (run with
+    LLAR_LIBRARY pointing at it): line loads per AllReduce (all ranks),
+    loads per awaited line (1 = the line was there at its first load) and
+    polling rounds per wait. Its timings are not the library's."""
+    from tp_allreduce_persistent_b300 import inputs
+    rows = {}
+    for name, (n, dtype, count, proto, iters, chain, chunk) in POLL_CASES.items():
+        llar.llar_init(n, dtype, count * inputs.ELEM_BYTES[dtype])
+        try:
+            if chunk:
+                llar.llar_set_sentinel_chunk(chunk)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(7)
+            td = inputs.TORCH_DTYPE[dtype]
+            ins = [(torch.randn(count, device=dev, generator=gen) * 0.02).to(td) for _ in range(n)]
+            outs = [torch.empty_like(t) for t in ins]
+            llar.llar_allreduce_iters(ins, outs, count, proto, min(iters, 20), 0, 0, chain)
+            llar.llar_debug_poll_stats(reset=True)
+            llar.llar_allreduce_iters(ins, outs, count, proto, iters, 0, 0, chain)
+            rounds, loads, waits, awaited = llar.llar_debug_poll_stats(reset=True)
+            if llar.llar_get_status()[0] != llar.OK:
+                raise RuntimeError("device status not ok")
+            rows[name] = {"line_loads_per_allreduce": round(loads / iters, 1),
+                          "lines_awaited_per_allreduce": round(awaited / iters, 1),
+                          "loads_per_awaited_line": round(loads / max(awaited, 1), 3),
+                          "rounds_per_wait": round(rounds / max(waits, 1), 3)}
+        finally:
+            llar.llar_destroy()
+    return rows
+
+
+def poll_counts_subprocess():
+    """Run the polls leg in a child process on the poll-counting build, if it
+    has been built; None otherwise."""
+    from tp_allreduce_persistent_b300 import build as b
+    if not os.path.exists(b.POLLS_LIB):
+        return None
+    env = dict(os.environ, LLAR_LIBRARY=b.POLLS_LIB)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--leg", "polls"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])["poll_counts"]
+
+
 def per_config_roofline(per_config, sol_us, hbm_gbs):
     """Each row against its roofline: latency rows (microseconds per
     operation) as speed of light / time, with the speed of light measured in
@@ -707,6 +766,11 @@ def run_ours(args, world, rank, local, pg):
         if rank == 0:
             print(json.dumps({"leg": "llbuffer", **llbuffer_rows(llar, torch, dev, stream)}))
         return
+    if args.leg == "polls":
+        if rank == 0:
+            print(json.dumps({"leg": "polls", "library": os.path.basename(llar.LIB_PATH),
+                              "poll_counts": polls_leg(llar, torch, dev)}))
+        return
     llar.llar_init(NRANKS, DTYPE, max(args.bw_mib << 20, COUNT * 2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peaks, peak_src = measured_peaks()
@@ -734,6 +798,8 @@ def run_ours(args, world, rank, local, pg):
     per_config = None
     if args.leg == "all" and not args.no_configs:
         per_config = configs_leg(llar, torch, dev, stream)
+        if rank == 0:
+            per_config["poll_counts"] = poll_counts_subprocess()
 
     res = {"metric": METRIC, "unit": "us", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
@@ -767,7 +833,14 @@ def run_ours(args, world, rank, local, pg):
                           "kernel": f"k_{lat['dependent']['proto']}<bf16> (chain)",
                           "kind": f"latency: {args.iters} dependent AllReduces per launch, each input "
                                   "= RNE(output of the previous one / 8)"},
-            "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run",
+            "placed_worst_pair": {
+                "l2_round_trip_us": round(lat["placed"][0], 4), "write_us": round(lat["placed"][1], 4),
+                "sol_us": round(lat["placed"][2], 4), "pairs": lat["placed"][3],
+                "frac": round(lat["placed"][2] / us, 4), "dependent_frac": round(lat["placed"][2] / dep_us, 4),
+                "definition": "the slowest chase among the SMs holding the launch's rank CTAs, and half the "
+                              "slowest round trip among the CTA pairs that exchange data"},
+            "definition": "SoL = 2 x L2 round trip + one remote write, both measured in this run (medians over "
+                          "all SMs and SM pairs; placed_worst_pair: the worst placed pair)",
             "probe_ns_min_median_max": {"l2_chase_per_sm": spread(detail["chase_ns"]),
                                         "pingpong_round_trip_per_pair": spread(detail["rt_ns"])}}
         res["device"] = {"name": props.name, "sms": props.multi_processor_count,

@@ -234,6 +234,18 @@ int llar_debug_inject(int rank, int mode);
  * different SMs; sol_us = 2 * l2_rt_us + write_us. Needs llar_init. */
 int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us);
 
+/* The same bound over the rank CTAs a launch actually places, at the
+ * worst pair. A probe grid shaped like the most recent AllReduce launch
+ * (N x G blocks, its threads, shared memory, cluster and cooperative
+ * attributes) records the SM of every block; block c of every two ranks
+ * (the blocks that exchange data) ping-pong in rounds of disjoint pairs.
+ * l2_rt_us: the slowest pointer-chase latency (as in llar_sol_probe) among
+ * the SMs that hold the blocks; write_us: half the slowest pair's round
+ * trip; sol_us = 2 * l2_rt_us + write_us; npairs: pairs measured. Needs
+ * llar_init and an AllReduce launched since (LLAR_ERR_INVALID otherwise).
+ * Synchronises the device. */
+int llar_sol_probe_placed(double* l2_rt_us, double* write_us, double* sol_us, int* npairs);
+
 /* The speed-of-light bound itself (host only): 2 * l2_rt_us + write_us. */
 double llar_sol_bound_us(double l2_rt_us, double write_us);
 
@@ -272,8 +284,9 @@ int llar_select_protocol(int nranks, int dtype, size_t count);
  * graph get fresh epochs on every replay. Synchronises the device to read it. */
 unsigned long long llar_epoch(void);
 
-/* Launch shape of the most recent launch: protocol used, CTAs per rank,
- * threads per CTA, iterations. Any pointer may be NULL. */
+/* Launch shape of the most recent launch of this context (llar_init clears
+ * it): protocol used, CTAs per rank, threads per CTA, iterations. Any
+ * pointer may be NULL. */
 int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters);
 
 /* Diagnostic, host arithmetic only (no GPU work, no llar_init needed; no
@@ -321,6 +334,20 @@ int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, i
  * captured. */
 int llar_allreduce_noalloc(const void* const* in, void* const* out, size_t count,
                            int nranks, int dtype, void* stream);
+
+/* Poll counts (diagnostic; no page describes it). In the poll-counting
+ * build of this library (libllar_polls.so, compiled with LLAR_POLL_STATS:
+ * python -m tp_allreduce_persistent_b300.build --poll-stats) the library's
+ * own AllReduce kernels count their polling: stats[0] thread polling rounds
+ * (one round loads every line the thread still awaits), stats[1] line loads
+ * issued in those rounds, stats[2] bounded waits started, stats[3] lines
+ * those waits awaited. stats[1] / stats[3] is the loads per awaited line (1
+ * = every line was there at its first load); stats[0] / stats[2] the rounds
+ * per wait. The counters add up across launches; reset != 0 zeroes them
+ * after the read. Synchronises the device. The regular build returns
+ * LLAR_ERR_UNSUPPORTED; timings of the counting build are not the
+ * library's. */
+int llar_debug_poll_stats(unsigned long long* stats, int reset);
 
 /* Static description of a status code. */
 const char* llar_strerror(int status);

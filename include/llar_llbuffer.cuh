@@ -35,6 +35,16 @@
 
 #include "llar_llbuffer.h"
 
+// Diagnostic hook: every bounded wait below calls it once per polling
+// round, with `first` (the wait's first round) and `pending` (one bit per
+// line still awaited; its population count is the loads the round issues).
+// It expands to nothing unless the includer defines LLB_ON_POLL_ROUND
+// before including this header (the library's poll-counting build does).
+#ifndef LLB_ON_POLL_ROUND
+__device__ __forceinline__ void llb_poll_round_unused(bool, unsigned) {}
+#define LLB_ON_POLL_ROUND(first, pending) llb_poll_round_unused((first), (pending))
+#endif
+
 namespace llb {
 
 typedef unsigned long long u64;
@@ -232,12 +242,14 @@ __device__ __forceinline__ bool ll_try(const llar_llbuffer& b, int q, u64 E, siz
 // timeout. False on timeout or abort.
 __device__ __forceinline__ bool ll_wait(const llar_llbuffer& b, int me, int q, u64 E, size_t w, u64& data) {
   Wait wt;
-  while (!ll_try(b, q, E, w, data))
+  for (bool first = true;; first = false) {
+    LLB_ON_POLL_ROUND(first, 1u);
+    if (ll_try(b, q, E, w, data)) return true;
     if (wt.expired(b)) {
       fail(b, me, E);
       return false;
     }
-  return true;
+  }
 }
 // Poll word w of every rank but `me` at once (one load per pending rank per
 // round); d[q] receives rank q's word, d[me] is left alone.
@@ -245,7 +257,8 @@ template <int N>
 __device__ __forceinline__ bool ll_wait_peers(const llar_llbuffer& b, int me, u64 E, size_t w, u64 (&d)[N]) {
   unsigned pend = ((1u << N) - 1u) & ~(1u << me);
   Wait wt;
-  while (true) {
+  for (bool first = true;; first = false) {
+    LLB_ON_POLL_ROUND(first, pend);
     u64 lo[N], hi[N];
 #pragma unroll
     for (int q = 0; q < N; ++q)
@@ -288,7 +301,8 @@ __device__ __forceinline__ u64 sum_words(const u64 (&d)[N]) {
 __device__ __forceinline__ bool ll_wait_ranks(const llar_llbuffer& b, int me, u64 E, size_t w, u64 (&d)[8]) {
   unsigned pend = ((1u << b.nranks) - 1u) & ~(1u << me);
   Wait wt;
-  while (true) {
+  for (bool first = true;; first = false) {
+    LLB_ON_POLL_ROUND(first, pend);
     u64 lo[8], hi[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -372,7 +386,8 @@ template <typename T>
 __device__ __forceinline__ bool sen_take(const llar_llbuffer& b, int d, int q, int s, size_t v, u64 E, uint4& x) {
   char* p = sen_vec(b, d, s, q, v);
   Wait wt;
-  while (true) {
+  for (bool first = true;; first = false) {
+    LLB_ON_POLL_ROUND(first, 1u);
     x = ld_relaxed_v4(p);
     if (!has_pattern<T>(x)) break;
     if (wt.expired(b)) {
@@ -465,12 +480,15 @@ __device__ __forceinline__ bool ll128_take(const llar_llbuffer& b, int o, int s,
   data = make_uint4(0u, 0u, 0u, 0u);
   if (active) {
     Wait wt;
-    while ((ld_acquire_u32(line) & Elem<T>::kMask) != want)
+    for (bool first = true;; first = false) {
+      LLB_ON_POLL_ROUND(first, 1u);
+      if ((ld_acquire_u32(line) & Elem<T>::kMask) == want) break;
       if (wt.expired(b)) {
         fail(b, o, E);
         ok = false;
         break;
       }
+    }
     if (ok) data = ld_relaxed_v4(line + lane * 16);
   }
   __syncwarp();  // every lane has its data before any lane zeroes

@@ -48,7 +48,8 @@ def test_layout_constants(dtype):
     assert lb == 128 and pl == oproto.ll128_payload_elems(dtype)
     assert st == 2 * oproto.ll128_round_staging_bytes(1 << 20, 8, dtype)
     lb, pl, st = llar.llar_layout("sentinel", dtype, 8, 32768)
-    assert lb == 16 and pl * e == 16 and st == 2 * 8 * 65536  # 2 slots x 8 sources x the 64 KiB default chunk
+    # published once per rank: a ring of 32 slots of the 64 KiB default chunk, one tail word per vector
+    assert lb == 16 and pl * e == 16 and st == 32 * 65536 + 65536 // 16 * 8
 
 
 @pytest.mark.parametrize("n", range(2, 9))

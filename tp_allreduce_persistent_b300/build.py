@@ -14,6 +14,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libllar.so")
+# diagnostic build: the same library with poll counting compiled in
+POLLS_LIB = os.path.join(HERE, "libllar_polls.so")
 SOURCES = ["llar_runtime.cu", "llar_kernels.cu", "llar_llbuffer.cu"]
 HEADERS = ["llar_internal.h", "llar_device.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,11 +36,18 @@ def _inputs():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
+
+
+def build_poll_stats(force=False):
+    """The poll-counting variant (LLAR_POLL_STATS), next to the library."""
+    if not force and up_to_date(POLLS_LIB):
+        return POLLS_LIB
+    return build(defines=["LLAR_POLL_STATS=1"], out=POLLS_LIB)
 
 
 def build(force=False, verbose=False, defines=(), out=None):
@@ -65,5 +74,8 @@ def build(force=False, verbose=False, defines=(), out=None):
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
-    print(LIB)
+    if "--poll-stats" in sys.argv:
+        print(build_poll_stats(force="--force" in sys.argv))
+    else:
+        build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+        print(LIB)

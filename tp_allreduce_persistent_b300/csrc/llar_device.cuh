@@ -21,6 +21,31 @@
 #include <cstdint>
 
 #include "llar_internal.h"
+
+#ifdef LLAR_POLL_STATS
+// Poll-counting build (diagnostic, a separate library): per warp and
+// polling round, the lowest active lane adds the active lanes (thread
+// rounds), the lines they load, the waits whose first round this is and
+// the lines those waits await. One reduction per warp and round, issued
+// without waiting for its result.
+static __device__ unsigned long long g_llar_poll_stats[4];
+static __device__ __forceinline__ void llar_poll_stat(bool first, unsigned pending) {
+  const unsigned m = __activemask();
+  const unsigned loads = __reduce_add_sync(m, (unsigned)__popc(pending));
+  const unsigned starts = __popc(__ballot_sync(m, first));
+  const unsigned awaited = __reduce_add_sync(m, first ? (unsigned)__popc(pending) : 0u);
+  if ((int)(threadIdx.x & 31u) == __ffs(m) - 1) {
+    atomicAdd(&g_llar_poll_stats[0], (unsigned long long)__popc(m));
+    atomicAdd(&g_llar_poll_stats[1], (unsigned long long)loads);
+    if (starts) {
+      atomicAdd(&g_llar_poll_stats[2], (unsigned long long)starts);
+      atomicAdd(&g_llar_poll_stats[3], (unsigned long long)awaited);
+    }
+  }
+}
+#define LLB_ON_POLL_ROUND(first, pending) llar_poll_stat((first), (pending))
+#endif
+
 #include "llar_llbuffer.cuh"
 
 namespace llar {
@@ -38,6 +63,11 @@ using llb::ld_relaxed_v4;
 using llb::st_relaxed_b128;
 using llb::st_relaxed_v4;
 
+__device__ __forceinline__ u64 ld_relaxed_u64(const void* p) {
+  u64 v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ u64 ld_acquire_u64(const void* p) {
   u64 v;
   asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

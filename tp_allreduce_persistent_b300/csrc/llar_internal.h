@@ -17,6 +17,33 @@ constexpr int kLL128Line = 128;    // bytes per LL128 line
 constexpr int kLL128Lanes = 8;     // 16-byte lanes (threads) per line
 constexpr int kLLLine = 16;        // bytes per LL line: 8 data + 8 flag
 constexpr int kAgLineBytes = 256;  // one LL128 line published again as 16 LL lines
+// Sentinel one-shot. From kSenPubMinN ranks (with at most one vector per
+// thread and chunk, and at least kSenPubMinSteps chunks in the launch) each
+// rank publishes its chunks once in its own ring of
+// kSenPubSlots = 4 kSenFencePeriod slots, fences every kSenFencePeriod
+// chunks and resets a slot 2 kSenFencePeriod chunks after publishing it;
+// its tail words (one u64 per vector of a chunk) follow the ring at
+// kSenPubSlots * kSenMaxChunkBytes. Otherwise chunks are pushed into two
+// slots per peer at the receivers, with the next chunk pushed as soon as
+// this one has arrived for up to kSenEarlyMaxN ranks.
+#ifndef LLAR_SEN_EARLY_MAX_N
+#define LLAR_SEN_EARLY_MAX_N 4
+#endif
+#ifndef LLAR_SEN_PUB_MIN_N
+#define LLAR_SEN_PUB_MIN_N 2
+#endif
+#ifndef LLAR_SEN_FENCE_PERIOD
+#define LLAR_SEN_FENCE_PERIOD 8  // measured against 4: 8 ranks x 64 KiB fp16 in 8 KiB chunks 10.4 -> 10.0 us
+#endif
+#ifndef LLAR_SEN_PUB_MIN_STEPS
+#define LLAR_SEN_PUB_MIN_STEPS 4
+#endif
+constexpr int kSenEarlyMaxN = LLAR_SEN_EARLY_MAX_N;
+constexpr int kSenPubMinN = LLAR_SEN_PUB_MIN_N;
+constexpr int kSenFencePeriod = LLAR_SEN_FENCE_PERIOD;
+constexpr int kSenPubMinSteps = LLAR_SEN_PUB_MIN_STEPS;  // chunks per launch (iterations x chunks)
+constexpr int kSenPubSlots = 4 * kSenFencePeriod;
+constexpr size_t kSenMaxChunkBytes = 64u << 10;  // largest sentinel chunk per rank
 // per (rank, CTA) signal words: 0 ready and 1 done epochs of the fixed-order
 // chains, 2 consumption acknowledgements of point-to-point transfers
 constexpr int kFlagKinds = 3;
@@ -127,5 +154,17 @@ struct SolResult {
 };
 // The probes use their own abort word, never the context's.
 cudaError_t run_sol(SolResult* res, unsigned long long timeout_ns);
+// The same two measurements over the CTAs of a launch of the given shape:
+// the slowest chase among the SMs holding its blocks, and the round trips
+// of every pair of blocks that exchange data (block c of two ranks).
+struct SolPlaced {
+  int npairs;
+  int distinct_sms;
+  double chase_worst_ns;
+  double rt_worst_ns;
+  double rt_median_ns;
+};
+cudaError_t run_sol_placed(int nranks, int G, int threads, int clustered, int spread_smem,
+                           unsigned long long timeout_ns, SolPlaced* out);
 
 }  // namespace llar

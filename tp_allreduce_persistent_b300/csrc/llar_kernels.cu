@@ -9,6 +9,7 @@
 // No kernel contains a grid-wide barrier; the only waits are per-line polls
 // (techniques 1, 2, 4) and, on the fixed-order chained paths, per-CTA-pair
 // epoch flags.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -323,6 +324,7 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
     from[q] = p.sen + (size_t)r * p.sen_stride + (size_t)q * src_stride;
   }
   const unsigned others = ((1u << N) - 1u) & ~(1u << r);
+  constexpr bool EARLY = N <= kSenEarlyMaxN;
   auto input = [&](int e) -> const char* {
     return CHAIN ? rank_input<DT>(p, r, e) : p.in[r] + (size_t)e * p.in_stride * EB;
   };
@@ -330,6 +332,11 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
     if (poison) return ones;
     if (full || v + 1 < NV) return CHAIN ? ld_cg_v4(src + (size_t)v * 16) : ld_stream_v4(src + (size_t)v * 16);
     return load_vec16<DT>(src, v, p.count, !CHAIN);
+  };
+  auto load_cg = [&](const char* src, unsigned v) -> uint4 {
+    if (poison) return ones;
+    if (full || v + 1 < NV) return ld_cg_v4(src + (size_t)v * 16);
+    return load_vec16<DT>(src, v, p.count, false);
   };
   // Push my vector j of chunk sequence number sq into every peer's slot
   // sq & 1. Credit (technique 3): peer q consumed and reset my vector j of
@@ -358,6 +365,192 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
     return true;
   };
 
+  // PUBLISH-ONCE (at least kSenPubMinN ranks, at most one vector per thread
+  // and chunk). As in the LL one-shot, each rank writes its vector j of
+  // chunk t once, into its own ring of S = kSenPubSlots slots (slot t % S,
+  // all-ones when idle), and every peer polls it there until no element is
+  // the sentinel. On one GPU a peer's load and a store into the peer's
+  // staging meet in the same L2, so one store replaces N - 1 pushes
+  // (measured with the pushes: 7 stores took 0.45 us of a 1.66 us step).
+  // The owner resets its slot D = 2F steps later (F = kSenFencePeriod), runs
+  // a fence every F steps, and S = 4F. Step t: fence if t is a positive
+  // multiple of F; publish chunk t; reset chunk t - D; store the output of
+  // chunk t - 1; load the next step's input; poll chunk t from every peer;
+  // reduce into registers. Credit (technique 3): (1) no reset before every
+  // reader has read: reader q polled my chunk u in its step u, fenced at
+  // g = the first multiple of F after u, and published chunk g (or g + 1,
+  // the steps without a vector being isolated); I received that before my
+  // fence at g + F <= u + D, which precedes my reset of u. (2) no stale read
+  // after reuse: my reset of chunk u - S, in step u - S + D = u - 2F,
+  // precedes my fence f <= u - F and my publication of chunk f (or f + 1);
+  // q received that before its fence at f + F <= u, which precedes its poll
+  // of chunk u. At the end of the launch each thread publishes the launch's
+  // last epoch in a tail word (after a fence), waits for its peers' tail
+  // words, fences and resets the slots still holding data, so the next
+  // launch finds every slot all-ones. That tail costs about one round trip
+  // and two fences per launch (8 ranks x 16 KiB bf16, one AllReduce per
+  // launch: 3.7 us on the push path, 5.4 us published once), so launches of
+  // fewer than kSenPubMinSteps chunks take the push path below.
+  if (N >= kSenPubMinN && per <= blockDim.x && (unsigned)p.iters * nchunks >= (unsigned)kSenPubMinSteps) {
+    const unsigned j = j0 + threadIdx.x;
+    if (j >= j1) return;
+    constexpr unsigned S = (unsigned)kSenPubSlots, F = (unsigned)kSenFencePeriod, D = 2 * F;
+    static_assert(S == 4 * F && F >= 2, "the credit chain needs S = 4F slots and F >= 2");
+    const size_t ring = (size_t)CV * 16;  // bytes per slot
+    auto cell = [&](int q, unsigned t) -> char* {
+      return p.sen + (size_t)q * p.sen_stride + (size_t)(t % S) * ring + (size_t)j * 16;
+    };
+    auto tail_word = [&](int q) -> u64* {
+      return reinterpret_cast<u64*>(p.sen + (size_t)q * p.sen_stride + (size_t)S * kSenMaxChunkBytes) + j;
+    };
+    auto has_at = [&](unsigned t) { return (t % nchunks) * CV + j < NV; };
+    bool lag = false;  // step t - 1 had my vector j: its output is still to be stored
+    char* lag_dst = nullptr;
+    char* lag_chain = nullptr;
+    unsigned lag_v = 0;
+    uint4 lag_y = ones, lag_nx = ones;
+    auto store_lagged = [&]() {
+      if (!lag) return;
+      if (full || lag_v + 1 < NV) st_v4(lag_dst + (size_t)lag_v * 16, lag_y);
+      else store_vec16<DT>(lag_dst, lag_v, p.count, lag_y);
+      if (CHAIN) store_vec16<DT>(lag_chain, lag_v, p.count, lag_nx);
+      lag = false;
+    };
+    // the chunk received last, reduced only after the next chunk has been
+    // published (the reduction is register work: the order of the memory
+    // operations, and so the credit argument, is unchanged)
+    bool pending = false;
+    uint4 pd[N];
+    uint4 p_own = ones;
+    char* p_dst = nullptr;
+    unsigned p_v = 0;
+    int p_e = 0;
+    auto reduce_pending = [&]() {
+      if (!pending) return;
+      float acc[PER16];
+#pragma unroll
+      for (int q = 0; q < N; ++q) {
+        const uint4 vq = (q == r) ? p_own : pd[q];
+        const unsigned w4[4] = {vq.x, vq.y, vq.z, vq.w};
+        acc_words<DT, 4>(acc, w4, q == 0);
+      }
+      unsigned y[4];
+      round_words<DT, 4>(acc, y);
+      lag_y = u4(y);
+      if (CHAIN) {
+        unsigned nx[4];
+        chain_words_fast<DT, 4>(acc, y, nx, p.chain_scale);
+        lag_nx = u4(nx);
+        lag_chain = chain_next_buf(p, r, p_e);
+      }
+      lag = true;
+      lag_dst = p_dst;
+      lag_v = p_v;
+      pending = false;
+    };
+    // The next step's input is loaded before this step's poll, with
+    // L2-coherent (.cg) loads: through the non-coherent read-only path the
+    // inputs took 2.5x longer per AllReduce here (8 ranks x 64 KiB fp16 in
+    // 8 KiB chunks: 25.3 against 10.4 us on one box; the push path below
+    // does not gain from .cg). A chain's next inputs are its own outputs of
+    // the previous iteration: loading them ahead measured slower (C5 chain,
+    // 8 ranks: 14.0 against 11.5 us per AllReduce), so a chain loads them
+    // at the publication.
+    const bool ahead = !CHAIN;
+    bool have_next = false;
+    uint4 next_own = ones;
+    unsigned t = 0;
+    u64 E = epoch0;
+    for (int e = 0; e < p.iters; ++e) {
+      E = epoch0 + (u64)e;
+      const char* src = input(e);
+      char* dst = rank_output<DT>(p, r, e);
+      for (unsigned k = 0; k < nchunks; ++k, ++t) {
+        if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+        // a chain reduces first: with one chunk per iteration its next input is
+        // that reduction's output, and otherwise the input load of the
+        // publication below then overlaps the reduction (C5 chain, 8 ranks:
+        // 11.5 against 13.0 us per AllReduce reducing after the publication)
+        if (CHAIN) reduce_pending();
+        if (t > 0 && t % F == 0) fence_gpu();
+        const unsigned v = k * CV + j;
+        const bool has = v < NV;
+        uint4 own = ones;
+        if (has) {
+          own = have_next ? next_own
+                          : ((CHAIN && e > 0 && nchunks == 1) ? (poison ? ones : lag_nx) : load_cg(src, v));
+          if (!skip) st_relaxed_v4(cell(r, t), own);
+        }
+        reduce_pending();
+        if (t >= D && has_at(t - D) && !skip) st_relaxed_v4(cell(r, t - D), ones);
+        store_lagged();
+        have_next = false;
+        if (ahead) {
+          const bool wrap = k + 1 == nchunks;
+          const unsigned nv = (wrap ? 0u : k + 1) * CV + j;
+          if ((!wrap || e + 1 < p.iters) && nv < NV) {
+            next_own = load_cg(wrap ? input(e + 1) : src, nv);
+            have_next = true;
+          }
+        }
+        if (!has) continue;
+        uint4 d[N];
+        unsigned pend = others;
+        Waiter wt;
+        for (bool first_round = true;; first_round = false) {
+          LLB_ON_POLL_ROUND(first_round, pend);
+          uint4 tv[N];
+#pragma unroll
+          for (int q = 0; q < N; ++q)
+            if ((pend >> q) & 1u) tv[q] = ld_relaxed_v4(cell(q, t));
+#pragma unroll
+          for (int q = 0; q < N; ++q)
+            if (((pend >> q) & 1u) && !has_sentinel<DT>(tv[q])) {
+              d[q] = tv[q];
+              pend &= ~(1u << q);
+            }
+          if (pend == 0u) break;
+          if (wt.expired(p)) {
+            report_timeout(p, r, c, E);
+            return;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < N; ++q) pd[q] = d[q];
+        p_own = own;
+        p_dst = dst;
+        p_v = v;
+        p_e = e;
+        pending = true;
+      }
+    }
+    reduce_pending();
+    store_lagged();
+    // tail: every peer has read my last chunks once it publishes the last
+    // epoch in its tail word, which it does after a fence that follows
+    // its polls; then my remaining slots can be reset
+    if (skip) return;
+    fence_gpu();
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(tail_word(r)), "l"(E) : "memory");
+    unsigned pend = others;
+    Waiter wt;
+    for (bool first_round = true;; first_round = false) {
+      LLB_ON_POLL_ROUND(first_round, pend);
+#pragma unroll
+      for (int q = 0; q < N; ++q)
+        if (((pend >> q) & 1u) && ld_relaxed_u64(tail_word(q)) == E) pend &= ~(1u << q);
+      if (pend == 0u) break;
+      if (wt.expired(p)) {
+        report_timeout(p, r, c, E);
+        return;
+      }
+    }
+    fence_gpu();
+    for (unsigned u = t > D ? t - D : 0u; u < t; ++u)
+      if (has_at(u)) st_relaxed_v4(cell(r, u), ones);
+    return;
+  }
+
   // EARLY (up to 4 ranks): chunk 0 of the first iteration goes out first;
   // afterwards the next chunk's vector j goes out as soon as vector j of
   // this chunk has arrived from every peer and been reset (a fence orders
@@ -369,7 +562,6 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
   // previous chunk's resets landed (measured, 8 ranks: 64 KiB in 8 KiB
   // chunks 15.7 us with this order, 20.0 us with early push; 4 ranks x
   // 16 KiB: 1.57 vs 1.49 us).
-  constexpr bool EARLY = N <= 4;
   if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
   if (EARLY)
     for (unsigned j = j0 + threadIdx.x; j < j1; j += blockDim.x)
@@ -411,7 +603,8 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
         unsigned pend = others;
         unsigned spins = 0;
         u64 deadline = 0;
-        while (true) {
+        for (bool first_round = true;; first_round = false) {
+          LLB_ON_POLL_ROUND(first_round, pend);
           uint4 t[N];
 #pragma unroll
           for (int q = 0; q < N; ++q)
@@ -740,7 +933,9 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
       if (own) {
         if (!failed) {
           Waiter wt;
-          while ((ld_acquire_u32(line) & flag_mask) != n_bits) {
+          for (bool first_round = true;; first_round = false) {
+            LLB_ON_POLL_ROUND(first_round, 1u);
+            if ((ld_acquire_u32(line) & flag_mask) == n_bits) break;
             if (wt.expired(p)) {
               report_timeout(p, r, c, E);
               failed = true;
@@ -783,7 +978,8 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
       if (!failed) {
         Waiter wt;
         bool got0 = false, got1 = false;
-        while (true) {
+        for (bool first_round = true;; first_round = false) {
+          LLB_ON_POLL_ROUND(first_round, (got0 ? 0u : 1u) | (got1 ? 0u : 2u));
           u64 a0, f0, a1, f1;
           if (!got0) ld_relaxed_b128(ag, a0, f0);
           if (!got1) ld_relaxed_b128(ag + 16, a1, f1);
@@ -2134,6 +2330,138 @@ done:
   return err;
 }
 
+// Speed of light over the CTAs a launch places. A grid of the launch's
+// shape (N x G blocks, its threads, dynamic shared memory, cluster and
+// cooperative attributes) records each block's SM; then block c of rank r
+// ping-pongs with block c of every other rank q (the blocks that exchange
+// data), in rounds of disjoint pairs (round-robin schedule over the ranks
+// plus a bye when N is odd). rt_ns[(c * M + k) * P + min(r, q)] receives
+// the pair's ns per round trip in round k (0 for a bye or a wait that ran
+// out). Waits are bounded by the timeout and the abort word.
+__global__ void k_sol_placed(int nranks, int reps, unsigned* flags, int* smid, unsigned long long* rt_ns,
+                             unsigned* abort_flag, unsigned long long timeout_ns) {
+  extern __shared__ char pad[];
+  if (threadIdx.x != 0) return;
+  const int r = blockIdx.x % nranks, c = blockIdx.x / nranks;
+  unsigned id;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+  smid[blockIdx.x] = (int)id;
+  const int P = nranks + (nranks & 1);  // players, with a bye for odd N
+  const int M = P - 1;                  // rounds
+  u64 deadline = 0;
+  auto wait_for = [&](const unsigned* w, unsigned v) -> bool {
+    unsigned spins = 0;
+    while (ld_relaxed_u32(w) != v)
+      if ((++spins & 1023u) == 0 && (globaltimer_ns() > deadline || ld_relaxed_u32(abort_flag) != 0)) {
+        atomicExch(abort_flag, 7u);
+        return false;
+      }
+    return true;
+  };
+  for (int k = 0; k < M; ++k) {
+    int q;
+    if (r == M) {
+      q = k;
+    } else {
+      q = ((2 * k - r) % M + M) % M;
+      if (q == r) q = M;
+    }
+    if (q >= nranks) continue;  // bye
+    deadline = globaltimer_ns() + timeout_ns;  // each round's waits have the full bound
+    const int lo = r < q ? r : q;
+    const size_t pair = ((size_t)c * M + k) * P + lo;
+    unsigned* to_a = flags + pair * 64;
+    unsigned* to_b = to_a + 32;
+    if (r == lo) {  // A: handshake 1, then reps timed round trips
+      asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" :: "l"(to_b), "r"(1u) : "memory");
+      if (!wait_for(to_a, 1u)) return;
+      const u64 t0 = globaltimer_ns();
+      for (int i = 2; i <= reps + 1; ++i) {
+        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" :: "l"(to_b), "r"((unsigned)i) : "memory");
+        if (!wait_for(to_a, (unsigned)i)) return;
+      }
+      rt_ns[pair] = (globaltimer_ns() - t0) / (u64)reps;
+    } else {  // B: answer every value
+      for (int i = 1; i <= reps + 1; ++i) {
+        if (!wait_for(to_b, (unsigned)i)) return;
+        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" :: "l"(to_a), "r"((unsigned)i) : "memory");
+      }
+    }
+  }
+  (void)pad;
+}
+
+cudaError_t run_sol_placed(int nranks, int G, int threads, int clustered, int spread_smem,
+                           unsigned long long timeout_ns, SolPlaced* out) {
+  cudaError_t err;
+  SolResult chase;
+  if ((err = run_sol(&chase, timeout_ns)) != cudaSuccess) return err;
+  const int P = nranks + (nranks & 1), M = P - 1, blocks = nranks * G;
+  const size_t npair_slots = (size_t)G * M * P;
+  const int reps = 2000;
+  unsigned *flags = nullptr, *abort_flag = nullptr;
+  int* smid = nullptr;
+  unsigned long long* rt = nullptr;
+  std::vector<int> h_smid(blocks);
+  std::vector<unsigned long long> h_rt(npair_slots);
+#define LLAR_TRY(x) do { if ((err = (x)) != cudaSuccess) goto done; } while (0)
+  LLAR_TRY(cudaMalloc(&flags, npair_slots * 64 * sizeof(unsigned)));
+  LLAR_TRY(cudaMalloc(&abort_flag, sizeof(unsigned)));
+  LLAR_TRY(cudaMalloc(&smid, blocks * sizeof(int)));
+  LLAR_TRY(cudaMalloc(&rt, npair_slots * sizeof(unsigned long long)));
+  LLAR_TRY(cudaMemset(flags, 0, npair_slots * 64 * sizeof(unsigned)));
+  LLAR_TRY(cudaMemset(abort_flag, 0, sizeof(unsigned)));
+  LLAR_TRY(cudaMemset(rt, 0, npair_slots * sizeof(unsigned long long)));
+  if (spread_smem > 0)
+    LLAR_TRY(cudaFuncSetAttribute(k_sol_placed, cudaFuncAttributeMaxDynamicSharedMemorySize, spread_smem));
+  {
+    Params shape;
+    memset(&shape, 0, sizeof(shape));
+    shape.nranks = nranks;
+    shape.G = G;
+    shape.clustered = clustered;
+    shape.spread_smem = spread_smem;
+    cudaLaunchAttribute at[3];
+    cudaLaunchConfig_t cfg = launch_config(shape, threads, 0, true, at);
+    int n_arg = nranks, reps_arg = reps;
+    void* args[] = {&n_arg, &reps_arg, &flags, &smid, &rt, &abort_flag, &timeout_ns};
+    LLAR_TRY(cudaLaunchKernelExC(&cfg, (const void*)k_sol_placed, args));
+  }
+  LLAR_TRY(cudaDeviceSynchronize());
+  LLAR_TRY(cudaMemcpy(h_smid.data(), smid, blocks * sizeof(int), cudaMemcpyDeviceToHost));
+  LLAR_TRY(cudaMemcpy(h_rt.data(), rt, npair_slots * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  {
+    // the slowest chase among the SMs that hold rank CTAs
+    double worst_chase = 0.0;
+    for (int b = 0; b < blocks; ++b)
+      for (int i = 0; i < chase.nchase; ++i)
+        if (chase.chase_smid[i] == h_smid[b] && chase.chase_ns[i] > worst_chase) worst_chase = chase.chase_ns[i];
+    std::vector<double> rts;
+    for (size_t i = 0; i < npair_slots; ++i)
+      if (h_rt[i] > 0) rts.push_back((double)h_rt[i]);
+    out->npairs = (int)rts.size();
+    out->chase_worst_ns = worst_chase;
+    out->rt_worst_ns = 0.0;
+    out->rt_median_ns = 0.0;
+    if (!rts.empty()) {
+      std::sort(rts.begin(), rts.end());
+      out->rt_worst_ns = rts.back();
+      out->rt_median_ns = rts[rts.size() / 2];
+    }
+    out->distinct_sms = 0;
+    std::vector<int> sorted_sm(h_smid);
+    std::sort(sorted_sm.begin(), sorted_sm.end());
+    out->distinct_sms = (int)(std::unique(sorted_sm.begin(), sorted_sm.end()) - sorted_sm.begin());
+  }
+#undef LLAR_TRY
+done:
+  cudaFree(flags);
+  cudaFree(abort_flag);
+  cudaFree(smid);
+  cudaFree(rt);
+  return err;
+}
+
 }  // namespace llar
 
 // ==================================================== allocation-free LL
@@ -2269,4 +2597,28 @@ extern "C" int llar_allreduce_noalloc(const void* const* in, void* const* out, s
     return err == cudaErrorCooperativeLaunchTooLarge ? LLAR_ERR_OCCUPANCY : LLAR_ERR_CUDA;
   }
   return LLAR_OK;
+}
+
+// =================================================== poll statistics
+extern "C" int llar_debug_poll_stats(unsigned long long* stats, int reset) {
+#ifdef LLAR_POLL_STATS
+  if (!stats) return LLAR_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(stats, g_llar_poll_stats, sizeof(g_llar_poll_stats)) != cudaSuccess) {
+    cudaGetLastError();
+    return LLAR_ERR_CUDA;
+  }
+  if (reset) {
+    const unsigned long long zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_llar_poll_stats, zero, sizeof(zero)) != cudaSuccess) {
+      cudaGetLastError();
+      return LLAR_ERR_CUDA;
+    }
+  }
+  return LLAR_OK;
+#else
+  (void)stats;
+  (void)reset;
+  return LLAR_ERR_UNSUPPORTED;
+#endif
 }

@@ -73,6 +73,7 @@ int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0, g_pdl = 1;  // LLAR_PDL=
 size_t g_bulk_min_bytes = 0;  // LLAR_BULK_MIN_BYTES: TMA two-shot threshold for every N (0: per N)
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
+int g_last_clustered = 0, g_last_spread = 0;  // of the last AllReduce launch
 
 // no error recorded; cta -1 until a wait that records its CTA runs out
 void clear_status(llar::DevStatus* st) {
@@ -84,6 +85,16 @@ int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return LLAR_OK;
   if (e == cudaErrorCooperativeLaunchTooLarge) return LLAR_ERR_OCCUPANCY;
   return LLAR_ERR_CUDA;
+}
+
+// Chunk-sized slots per rank region the sentinel one-shot keeps all-ones
+// between launches: the publish-once ring, or two slots per peer on the
+// push path (forced launch shapes); the publish-once tail words follow at
+// kSenPubSlots * kSenMaxChunkBytes.
+size_t sen_slots(int n) { return std::max<size_t>(llar::kSenPubSlots, 2 * (size_t)n); }
+size_t sen_region_bytes(int n) {
+  static_assert(llar::kSenMaxChunkBytes == kMaxChunk, "one largest chunk");
+  return std::max<size_t>(llar::kSenPubSlots, 2 * (size_t)n) * kMaxChunk + (kMaxChunk / 16) * 8;
 }
 
 size_t ll128_payload(int dtype) { return 128 / elem_bytes(dtype) - 1; }
@@ -520,6 +531,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   g_last_G = G;
   g_last_T = T;
   g_last_iters = iters;
+  g_last_clustered = p.clustered;
+  g_last_spread = p.spread_smem;
   return LLAR_OK;
 }
 
@@ -554,6 +567,8 @@ extern "C" {
 int llar_init(int nranks, int dtype, size_t max_bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (g) return LLAR_ERR_INVALID;
+  // the last-launch record belongs to the context
+  g_last_proto = g_last_G = g_last_T = g_last_iters = g_last_clustered = g_last_spread = 0;
   if (nranks < 2 || nranks > llar::kMaxRanks || !valid_dtype(dtype) || max_bytes == 0)
     return LLAR_ERR_INVALID;
   Ctx* c = new Ctx();
@@ -591,7 +606,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   };
   c->ll_words = (c->ll_cap + 7) / 8;
   region(2 * c->ll_words * llar::kLLLine, &c->ll_off, &c->ll_stride);  // [slot][word] published lines
-  region(2 * (size_t)n * kMaxChunk, &c->sen_off, &c->sen_stride);
+  region(sen_region_bytes(n), &c->sen_off, &c->sen_stride);
   c->l128_lines = ll128_lines_for(c->ll128_cap / c->esize, n, dtype);
   region(2 * c->l128_lines * llar::kLL128Line, &c->l128_off, &c->l128_stride);
   region(2 * c->l128_lines * llar::kAgLineBytes, &c->ag_off, &c->ag_stride);
@@ -884,6 +899,27 @@ int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us) {
   return LLAR_OK;
 }
 
+int llar_sol_probe_placed(double* l2_rt_us, double* write_us, double* sol_us, int* npairs) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (g_last_G <= 0 || g_last_T <= 0) return LLAR_ERR_INVALID;  // no AllReduce launched yet
+  llar::SolPlaced res;
+  const cudaError_t err = llar::run_sol_placed(g->n, g_last_G, g_last_T, g_last_clustered, g_last_spread,
+                                               g_timeout_ns, &res);
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(err);
+  }
+  if (res.npairs == 0 || res.chase_worst_ns <= 0.0) return LLAR_ERR_TIMEOUT;
+  const double l2 = res.chase_worst_ns * 1e-3;
+  const double wr = 0.5 * res.rt_worst_ns * 1e-3;
+  if (l2_rt_us) *l2_rt_us = l2;
+  if (write_us) *write_us = wr;
+  if (sol_us) *sol_us = llar_sol_bound_us(l2, wr);
+  if (npairs) *npairs = res.npairs;
+  return LLAR_OK;
+}
+
 int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes, size_t* rank_bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g) return LLAR_ERR_NOT_INIT;
@@ -891,7 +927,7 @@ int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes, size_t
   size_t off = 0, stride = 0, used = 0;
   switch (protocol) {
     case LLAR_PROTO_LL: off = c.ll_off; stride = c.ll_stride; used = 2 * c.ll_words * llar::kLLLine; break;
-    case LLAR_PROTO_SENTINEL: off = c.sen_off; stride = c.sen_stride; used = 2 * c.n * c.chunk_bytes; break;
+    case LLAR_PROTO_SENTINEL: off = c.sen_off; stride = c.sen_stride; used = sen_slots(c.n) * c.chunk_bytes; break;
     case LLAR_PROTO_LL128_ATOMIC: off = c.l128_off; stride = c.l128_stride; used = 2 * c.l128_lines * llar::kLL128Line; break;
     default: return LLAR_ERR_UNSUPPORTED;
   }
@@ -915,7 +951,9 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
       break;
     case LLAR_PROTO_SENTINEL: {
       const size_t chunk = g ? g->chunk_bytes : kDefaultChunk;
-      st = 2 * (size_t)nranks * chunk;
+      // the publish-once ring of kSenPubSlots chunks and a tail word per vector
+      st = nranks >= llar::kSenPubMinN ? (size_t)llar::kSenPubSlots * chunk + chunk / 16 * 8
+                                       : 2 * (size_t)nranks * chunk;
       break;
     }
     case LLAR_PROTO_LL128_ATOMIC:

@@ -89,12 +89,14 @@ def lib():
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
+        "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
         "llar_host_register": (c_int, [c_vp, c_size]),
         "llar_host_unregister": (c_int, [c_vp]),
         "llar_debug_launch_shape": (c_int, [c_int, c_int, c_size, c_int, c_int, c_int, c_size,
                                             ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
         "llar_strerror": (ctypes.c_char_p, [c_int]),
+        "llar_debug_poll_stats": (c_int, [ctypes.POINTER(c_ull), c_int]),
         "llar_llbuffer_create": (c_int, [c_int, c_size, ctypes.POINTER(LLBufferDesc)]),
         "llar_llbuffer_destroy": (c_int, [ctypes.POINTER(LLBufferDesc)]),
         "llar_llbuffer_get_status": (c_int, [ctypes.POINTER(LLBufferDesc), ctypes.POINTER(c_int),
@@ -236,6 +238,15 @@ def llar_allreduce_noalloc(ins, outs, count, nranks, dtype, stream=None):
            "llar_allreduce_noalloc")
 
 
+def llar_debug_poll_stats(reset=True):
+    """(thread polling rounds, line loads, waits, lines awaited) counted by
+    the poll-counting build since the last reset; raises LlarError
+    (ERR_UNSUPPORTED) in the regular build."""
+    out = (ctypes.c_ulonglong * 4)()
+    _check(lib().llar_debug_poll_stats(out, 1 if reset else 0), "llar_debug_poll_stats")
+    return tuple(int(v) for v in out)
+
+
 def llar_get_status():
     """(code, rank, cta, epoch) of the device status word."""
     r, c, e = ctypes.c_int(), ctypes.c_int(), ctypes.c_ulonglong()
@@ -268,6 +279,16 @@ def llar_sol_probe():
     a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
     _check(lib().llar_sol_probe(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "llar_sol_probe")
     return a.value, b.value, c.value
+
+
+def llar_sol_probe_placed():
+    """(l2_rt_us, write_us, sol_us, pairs) at the worst pair of the rank CTAs
+    placed by a launch shaped like the most recent AllReduce."""
+    a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    n = ctypes.c_int()
+    _check(lib().llar_sol_probe_placed(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), ctypes.byref(n)),
+           "llar_sol_probe_placed")
+    return a.value, b.value, c.value, n.value
 
 
 def llar_sol_bound_us(l2_rt_us, write_us):
