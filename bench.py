@@ -357,6 +357,8 @@ CONFIG_CASES = {
     "C3_ll128_16KiB": (8, "bf16", 16 * 512, "ll128", 1000, 0.0, None),
     "C4_sentinel": (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192),
     "C5_ll128_chain_N8": (8, "bf16", 65536, "ll128", 160, 0.5, None),
+    "C3_ll128_direct_1MiB": (8, "bf16", 1024 * 512, "ll128_direct", 200, 0.0, None),
+    "C3_ll128_direct_16KiB": (8, "bf16", 16 * 512, "ll128_direct", 1000, 0.0, None),
 }
 # fused decode layers for `--leg config --case NAME`: (ranks, tokens m, K, H), bf16
 FUSED_CASES = {
@@ -397,17 +399,24 @@ def configs_leg(llar, torch, dev, stream):
         "C2_4ranks_16KiB_bf16_us": {p: timed(4, "bf16", 8192, p, 10000, chunk=16384) for p in ("ll", "sentinel")},
         "C3_ll128_8ranks_bf16_us": {f"{kb}KiB": timed(8, "bf16", kb * 512, "ll128", 200 if kb > 64 else 1000)
                                     for kb in (4, 16, 64, 256, 1024)},
+        # the variant whose AllGather reads the owners' lines directly
+        "C3_ll128_direct_8ranks_bf16_us": {f"{kb}KiB": timed(8, "bf16", kb * 512, "ll128_direct",
+                                                             200 if kb > 64 else 1000)
+                                           for kb in (4, 16, 64, 256, 1024)},
+        "fixed_twoshot_8ranks_bf16_us": {f"{kb}KiB": timed(8, "bf16", kb * 512, "fixed_twoshot",
+                                                           200 if kb > 64 else 1000)
+                                         for kb in (4, 16, 64, 256, 1024)},
         "C4_sentinel_8ranks_64KiB_fp16_8KiB_chunks_us": timed(8, "fp16", 32768, "sentinel", 1000, chunk=8192),
         "C5_chain_160_layers_128KiB_bf16_us": {
             f"N{n}": {p: timed(n, "bf16", 65536, p, 160, chain=0.5, chunk=16384)
-                      for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")}
+                      for p in ("ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot")}
             for n in (4, 8)},
     }
     # the headline shape as a chain of dependent AllReduces (input of each =
     # RNE(previous output / 8)), every protocol
     out["dependent_chain_8ranks_16KiB_bf16_us"] = {
-        p: timed(8, "bf16", 8192, p, 2000, chain=1.0 / 8) for p in ("ll", "sentinel", "ll128", "fixed_oneshot",
-                                                                   "fixed_twoshot")}
+        p: timed(8, "bf16", 8192, p, 2000, chain=1.0 / 8) for p in ("ll", "sentinel", "ll128", "ll128_direct",
+                                                                   "fixed_oneshot", "fixed_twoshot")}
     out["C2_mode_b_graph_10000_launches_4ranks_16KiB_bf16_us"] = {
         p: mode_b_us(llar, torch, dev, stream, p) for p in ("ll", "sentinel")}
     out["noalloc_8ranks_16KiB_bf16"] = noalloc_rows(llar, torch, dev, stream)
@@ -447,7 +456,8 @@ def configs_leg(llar, torch, dev, stream):
             llar.llar_destroy()
 
     out["single_call_graph_8ranks_16KiB_bf16_us"] = {
-        "allreduce": {p: graph_call_us("allreduce", p) for p in ("ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot")},
+        "allreduce": {p: graph_call_us("allreduce", p) for p in ("ll", "sentinel", "ll128", "ll128_direct",
+                                                                 "fixed_oneshot", "fixed_twoshot")},
         "reduce_scatter": {p: graph_call_us("reduce_scatter", p) for p in ("ll", "sentinel", "ll128", "fixed_oneshot")},
         "all_gather": {p: graph_call_us("all_gather", p) for p in ("ll", "sentinel", "fixed_oneshot")},
     }
@@ -672,6 +682,8 @@ POLL_CASES = {
     "sentinel_C4_8ranks_64KiB_fp16_8KiB_chunks": (8, "fp16", 32768, "sentinel", 200, 0.0, 8192),
     "ll128_8ranks_16KiB_bf16": (8, "bf16", 8192, "ll128", 1000, 0.0, None),
     "ll128_8ranks_1MiB_bf16": (8, "bf16", 1 << 19, "ll128", 100, 0.0, None),
+    "ll128_direct_8ranks_16KiB_bf16": (8, "bf16", 8192, "ll128_direct", 1000, 0.0, None),
+    "ll128_direct_8ranks_1MiB_bf16": (8, "bf16", 1 << 19, "ll128_direct", 100, 0.0, None),
 }
 
 

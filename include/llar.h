@@ -69,8 +69,12 @@ typedef enum {
   LLAR_PROTO_LL128_ATOMIC = 3,  /* two-shot, atomic ReduceScatter into 128 B lines with a
                                    count flag, LL AllGather (technique 4); nondeterministic */
   LLAR_PROTO_FIXED_ONESHOT = 4, /* one-shot, every rank reads all inputs directly */
-  LLAR_PROTO_FIXED_TWOSHOT = 5  /* two-shot, owner of each segment reads all inputs
+  LLAR_PROTO_FIXED_TWOSHOT = 5, /* two-shot, owner of each segment reads all inputs
                                    directly and writes every rank's output */
+  LLAR_PROTO_LL128_DIRECT = 6   /* two-shot as LL128_ATOMIC, but every rank reads the
+                                   reduced data straight from the owners' 128 B lines once
+                                   their count reads N (three line slots in turn) instead
+                                   of an LL AllGather; nondeterministic, same bound */
 } llar_proto_t;
 
 typedef enum {

@@ -56,8 +56,9 @@ def test_c2_four_ranks_16k_bf16_10000_calls(proto):
     assert bad.size == 0, (bad[:8] // count).tolist()
 
 
+@pytest.mark.parametrize("proto", ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
-def test_c3_ll128_eight_ranks_4k_to_1m(dtype):
+def test_c3_ll128_eight_ranks_4k_to_1m(dtype, proto):
     n = 8
     e = fp.ELEM_BYTES[dtype]
     lo, hi = (-32, 32) if dtype == "bf16" else (-64, 64)
@@ -66,11 +67,11 @@ def test_c3_ll128_eight_ranks_4k_to_1m(dtype):
             count = (4096 << k) // e
             x = inputs.normal(n, count, dtype, seed=2)
             xb = inputs.bits_of(x)
-            got = allreduce(x, dtype, "ll128")
+            got = allreduce(x, dtype, proto)
             ok, err, rel = orc.compare_atomic(got, orc.allreduce(xb, dtype), xb, dtype)
             assert ok, (count, err, rel)
             xi = inputs.integers(n, count, dtype, seed=2, lo=lo, hi=hi)
-            assert np.array_equal(allreduce(xi, dtype, "ll128"), orc.allreduce(inputs.bits_of(xi), dtype))
+            assert np.array_equal(allreduce(xi, dtype, proto), orc.allreduce(inputs.bits_of(xi), dtype))
 
 
 def test_c4_sentinel_eight_ranks_64k_fp16_8k_chunks_100_calls():
@@ -88,7 +89,7 @@ def test_c4_sentinel_eight_ranks_64k_fp16_8k_chunks_100_calls():
 
 
 @pytest.mark.parametrize("n", [4, 8])
-@pytest.mark.parametrize("proto", ["ll", "sentinel", "fixed_oneshot", "fixed_twoshot", "ll128"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "fixed_oneshot", "fixed_twoshot", "ll128", "ll128_direct"])
 def test_c5_decode_chain_160_layers(n, proto):
     count, iters = 65536, 160
     x = inputs.normal(n, count, "bf16", seed=4, scale=0.02)
@@ -96,7 +97,7 @@ def test_c5_decode_chain_160_layers(n, proto):
     with context(n, "bf16", 1 << 20):
         for scale in (0.5, 1.0 / n):
             got = allreduce_iters(x, "bf16", proto, iters, chain_scale=scale)
-            if proto == "ll128":
+            if proto.startswith("ll128"):
                 # atomic order: the first step within the tolerance, every
                 # step the same on every rank (the exact chain is pinned in
                 # test_gpu_parity with inputs whose sums are all exact)

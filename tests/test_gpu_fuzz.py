@@ -17,7 +17,7 @@ from gpu_util import FILL, context, device_inputs, filled_outputs
 
 pytestmark = pytest.mark.gpu
 
-PROTOS = ["auto", "ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"]
+PROTOS = ["auto", "ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot"]
 
 
 def draw_cases(seed, k):
@@ -35,7 +35,7 @@ def draw_cases(seed, k):
 
 def check(got, xb, dtype, proto):
     want = orc.allreduce(xb, dtype)
-    if proto == "ll128":
+    if proto.startswith("ll128"):
         ok, err, rel = orc.compare_atomic(got, want, xb, dtype)
         assert ok, (err, rel)
     else:
@@ -96,7 +96,7 @@ def test_random_allreduce(case):
             got = np.stack([inputs.bits_of(o).reshape(iters, stride)[:, :count] for o in outs], axis=1)
             xb = inputs.bits_of(xi)
             if chain:
-                if proto == "ll128":  # atomic order: first step, then ranks agree
+                if proto.startswith("ll128"):  # atomic order: first step, then ranks agree
                     check(got[0], xb[0], dtype, proto)
                     for it in range(iters):
                         assert all(np.array_equal(got[it][0], got[it][q]) for q in range(n))
@@ -166,7 +166,8 @@ def test_random_segments_and_p2p(case):
 @pytest.mark.parametrize("case", draw_cases(314, 40))
 def test_random_llbuffer_allreduce(case):
     n, dtype, count, proto, kind, seed = case
-    proto = {"auto": "ll", "fixed_oneshot": "ll", "fixed_twoshot": "sentinel"}.get(proto, proto)
+    proto = {"auto": "ll", "fixed_oneshot": "ll", "fixed_twoshot": "sentinel",
+             "ll128_direct": "ll128"}.get(proto, proto)  # the LL buffer API's protocols
     e = inputs.ELEM_BYTES[dtype]
     count = max(count, 1)
     iters = [1, 2, 9, 40][kind]

@@ -18,7 +18,7 @@ from gpu_util import context, filled_outputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot"])
 def test_graph_replays_with_fresh_inputs(proto):
     n, dtype, count, calls = 8, "bf16", 8192, 6
     with context(n, dtype, 1 << 20):
@@ -42,7 +42,7 @@ def test_graph_replays_with_fresh_inputs(proto):
             want = orc.allreduce(xb, dtype)
             for k in range(calls):
                 got = np.stack([inputs.bits_of(o) for o in outs[k]])
-                if proto == "ll128":
+                if proto.startswith("ll128"):
                     assert orc.compare_atomic(got, want, xb, dtype)[0], (rep, k)
                 else:
                     assert np.array_equal(got, want), (rep, k)

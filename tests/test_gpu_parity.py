@@ -40,29 +40,31 @@ def test_fixed_order_bit_exact(proto, dtype, n):
             _ranks_identical(got)
 
 
+@pytest.mark.parametrize("proto", ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("n", [2, 3, 5, 8])
-def test_ll128_within_tolerance(dtype, n):
+def test_ll128_within_tolerance(proto, dtype, n):
     with context(n, dtype, 1 << 20):
         for i, count in enumerate(COUNTS):
             x = inputs.normal(n, count, dtype, seed=2000 + 17 * n + i)
-            got = allreduce(x, dtype, "ll128")
+            got = allreduce(x, dtype, proto)
             xb = inputs.bits_of(x)
             ok, err, rel = orc.compare_atomic(got, orc.allreduce(xb, dtype), xb, dtype)
             assert ok, (dtype, n, count, err, rel)
             _ranks_identical(got)
 
 
+@pytest.mark.parametrize("proto", ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype,lo,hi", [("fp32", -64, 64), ("fp16", -64, 64), ("bf16", -32, 32)])
-def test_ll128_exact_on_integers(dtype, lo, hi):
+def test_ll128_exact_on_integers(proto, dtype, lo, hi):
     with context(8, dtype, 1 << 20):
         for count in (63, 1000, 32768):
             x = inputs.integers(8, count, dtype, seed=count, lo=lo, hi=hi)
-            got = allreduce(x, dtype, "ll128")
+            got = allreduce(x, dtype, proto)
             assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
 
 
-@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128"])
+@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128", "ll128_direct"])
 def test_rank_id_inputs(proto):
     for n in (2, 8):
         with context(n, "bf16", 1 << 16):
@@ -75,6 +77,7 @@ def test_rank_id_inputs(proto):
     ("ll", [(1, 32), (3, 64), (7, 96), (18, 512)]),
     ("sentinel", [(1, 32), (2, 64), (5, 128), (16, 256)]),
     ("ll128", [(1, 32), (3, 64), (9, 256), (18, 512)]),
+    ("ll128_direct", [(1, 32), (3, 64), (9, 256), (18, 512)]),
     ("fixed_oneshot", [(1, 32), (4, 64), (37, 256)]),
     ("fixed_twoshot", [(1, 32), (4, 96), (74, 256)]),
 ])
@@ -89,7 +92,7 @@ def test_launch_shapes(proto, shapes):
                 got = allreduce(x, dtype, proto)
                 xb = inputs.bits_of(x)
                 want = orc.allreduce(xb, dtype)
-                if proto == "ll128":
+                if proto.startswith("ll128"):
                     assert orc.compare_atomic(got, want, xb, dtype)[0]
                 else:
                     assert np.array_equal(got, want), (g, t, count)
@@ -106,7 +109,7 @@ def test_sentinel_chunk_sizes(chunk):
             assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype))
 
 
-@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128"])
+@pytest.mark.parametrize("proto", FIXED_ORDER + ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_iters_fresh_inputs(proto, dtype):
     n, iters = 4, 9
@@ -116,7 +119,7 @@ def test_iters_fresh_inputs(proto, dtype):
             got = allreduce_iters(x, dtype, proto, iters)
             xb = inputs.bits_of(x)
             want = orc.allreduce_iters(xb, iters, dtype)
-            if proto == "ll128":
+            if proto.startswith("ll128"):
                 for e in range(iters):
                     assert orc.compare_atomic(got[e], want[e], xb[e], dtype)[0], e
             else:
@@ -136,9 +139,10 @@ def test_chain_bit_exact(proto, dtype, scale):
             assert np.array_equal(got, want), (proto, dtype, count)
 
 
+@pytest.mark.parametrize("proto", ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("n", [2, 4, 8])
-def test_chain_ll128_exact_fixed_point(n, dtype):
+def test_chain_ll128_exact_fixed_point(n, dtype, proto):
     # integers in [-2, 2] with scale 1/N (a power of two): every partial sum
     # of every step is exact in every element type, so the atomic chain must
     # equal the oracle's chain bit for bit (it settles on a fixed point after
@@ -147,12 +151,13 @@ def test_chain_ll128_exact_fixed_point(n, dtype):
     with context(n, dtype, 1 << 20):
         for count in (7, 8192, 20001):
             x = inputs.integers(n, count, dtype, seed=count + n, lo=-2, hi=2)
-            got = allreduce_iters(x, dtype, "ll128", iters, chain_scale=1.0 / n)
+            got = allreduce_iters(x, dtype, proto, iters, chain_scale=1.0 / n)
             assert np.array_equal(got, orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=1.0 / n))
 
 
+@pytest.mark.parametrize("proto", ["ll128", "ll128_direct"])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_chain_ll128_general_data(dtype):
+def test_chain_ll128_general_data(dtype, proto):
     # atomic sums may differ from the oracle in the last place, and a chain
     # carries that on: the first step is held to the atomic tolerance, every
     # step to what must hold whatever the order (every rank the same result,
@@ -161,7 +166,7 @@ def test_chain_ll128_general_data(dtype):
     with context(n, dtype, 1 << 20):
         count = 65536
         x = inputs.normal(n, count, dtype, seed=5, scale=0.02)
-        got = allreduce_iters(x, dtype, "ll128", iters, chain_scale=scale)
+        got = allreduce_iters(x, dtype, proto, iters, chain_scale=scale)
         xb = inputs.bits_of(x)
         ok, err, rel = orc.compare_atomic(got[0], orc.allreduce(xb, dtype), xb, dtype)
         assert ok, (err, rel)

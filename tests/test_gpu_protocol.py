@@ -62,6 +62,34 @@ def test_ll128_lines_clear_after_each_call(dtype):
                 assert oproto.ll128_lines_clear(buf)
 
 
+def test_ll128_direct_keeps_only_the_last_slot_after_each_call():
+    # three line slots in turn (sequence s uses slot s % 3, counted per
+    # context over direct AllReduces only); each AllReduce zeroes the slot
+    # before its own, so after a call only the last one holds data, whatever
+    # other protocols ran in between
+    n, dtype = 8, "bf16"
+    with context(n, dtype, 1 << 20):
+        seq = 0
+        for count, iters, other in ((100, 1, None), (65536, 1, "ll"), (70001, 4, "ll128"), (3000, 2, "sentinel")):
+            if other:
+                allreduce(inputs.normal(n, 1000, dtype, seed=count + 1, exclude_sentinel=True), dtype, other)
+            x = inputs.normal(n, count, dtype, seed=count, iters=iters)
+            got = allreduce_iters(x, dtype, "ll128_direct", iters)
+            xb = inputs.bits_of(x)
+            for e in range(iters):
+                assert orc.compare_atomic(got[e], orc.allreduce(xb[e], dtype), xb[e], dtype)[0], (count, e)
+            seq += iters
+            _, _, used = llar.llar_staging("ll128_direct")
+            per_slot = used // 3
+            for buf in staging_bytes("ll128_direct", n):
+                for slot in range(3):
+                    part = buf[slot * per_slot:(slot + 1) * per_slot]
+                    if slot != seq % 3:
+                        assert oproto.ll128_lines_clear(part), (count, slot)
+                    else:
+                        assert part.any()  # the last AllReduce's reduced lines
+
+
 def test_epochs_strictly_increase():
     with context(4, "bf16", 1 << 16):
         x = inputs.normal(4, 100, "bf16", seed=1)
@@ -107,7 +135,7 @@ def test_invalid_arguments_rejected():
     assert ei.value.code == llar.ERR_NOT_INIT
 
 
-@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "ll128_direct"])
 def test_dead_rank_times_out_then_recovers(proto):
     n, dtype, count = 4, "bf16", 4096
     with context(n, dtype, 1 << 20, timeout_ns=20_000_000):
@@ -119,7 +147,7 @@ def test_dead_rank_times_out_then_recovers(proto):
         torch.cuda.synchronize()
         code, rank, cta, epoch = llar.llar_get_status()
         assert code == llar.ERR_TIMEOUT and 0 <= rank < n and epoch >= 1
-        if proto != "ll128":  # in LL128 the silent rank also waits, as owner of its segment
+        if not proto.startswith("ll128"):  # in LL128 the silent rank also waits, as owner of its segment
             assert rank != 2
         with pytest.raises(llar.LlarError) as ei:  # sticky until reset
             llar.llar_allreduce(ins, outs, count, proto)
@@ -128,13 +156,13 @@ def test_dead_rank_times_out_then_recovers(proto):
         llar.llar_reset()
         got = allreduce(x, dtype, proto)
         want = orc.allreduce(inputs.bits_of(x), dtype)
-        if proto == "ll128":
+        if proto.startswith("ll128"):
             assert orc.compare_atomic(got, want, inputs.bits_of(x), dtype)[0]
         else:
             assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "ll128_direct"])
 def test_poisoned_rank_times_out(proto):
     n, dtype, count = 8, "fp16", 2048
     with context(n, dtype, 1 << 20, timeout_ns=20_000_000):
@@ -165,7 +193,7 @@ def test_fixed_chain_dead_rank_times_out(proto):
         llar.llar_reset()
 
 
-@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "fixed_oneshot", "fixed_twoshot"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot"])
 def test_delayed_rank_still_exact(proto):
     n, dtype, count, iters = 4, "bf16", 8192, 6
     with context(n, dtype, 1 << 20):
@@ -173,7 +201,7 @@ def test_delayed_rank_still_exact(proto):
         x = inputs.normal(n, count, dtype, seed=8, scale=0.02)
         got = allreduce_iters(x, dtype, proto, iters, chain_scale=0.5)
         want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=0.5)
-        if proto == "ll128":
+        if proto.startswith("ll128"):
             assert orc.compare_atomic(got[0], want[0], inputs.bits_of(x), dtype)[0]
         else:
             assert np.array_equal(got, want)

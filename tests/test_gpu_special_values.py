@@ -36,7 +36,7 @@ from tp_allreduce_persistent_b300 import inputs, llar
 
 from gpu_util import allreduce, context
 
-PROTOCOLS = ["ll", "sentinel", "fixed_oneshot", "fixed_twoshot", "ll128"]
+PROTOCOLS = ["ll", "sentinel", "fixed_oneshot", "fixed_twoshot", "ll128", "ll128_direct"]
 DTYPES = ["fp32", "fp16", "bf16"]
 KINDS = ["negzero", "zeromix", "subnormal", "subnormal_cancel", "posinf", "neginf", "infcancel",
          "qnan", "overflow_up", "overflow_below", "normal"]
@@ -148,7 +148,7 @@ def test_special_values_against_oracle(proto, dtype, n):
             got = allreduce(_torch_of(xb, dtype), dtype, proto)
             want = orc.allreduce(xb, dtype)
             assert all(np.array_equal(got[0], got[r]) for r in range(1, n))
-            if proto == "ll128":
+            if proto.startswith("ll128"):
                 # float32 atomic adds flush subnormal operands and results
                 ok, err, rel = orc.compare_atomic(got, want, xb, dtype, flush_subnormals=dtype == "fp32")
                 assert ok, (dtype, n, count, err, rel)

@@ -97,6 +97,9 @@ struct Params {
   char* l128;          size_t l128_stride;      // [2][L][128]
   char* l128ag;        size_t l128ag_stride;    // [2][L][256]: the owner's published AllGather lines
   size_t l128_lines;                            // L: lines per slot
+  char* l128d;         size_t l128d_stride;     // [3][L][128]: lines of the direct-AllGather variant
+  unsigned long long* l128d_seq;                // [0] its AllReduces so far (slot = sequence % 3),
+                                                // [1] lines per segment of its last launch
   char* chainbuf;      size_t chain_stride;     // [2][max_bytes] per rank
   size_t chain_slot_bytes;
   unsigned long long* flags;                    // [N][Gmax][kFlagKinds] signal words
@@ -121,6 +124,7 @@ void fault_settings(unsigned long long* timeout_ns, int* inject_rank, int* injec
 cudaError_t launch_ll(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s);
+cudaError_t launch_ll128d(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s);
 cudaError_t launch_fixed_twoshot(int dtype, const Params& p, int threads, cudaStream_t s);
 // ReduceScatter / AllGather: which = 0 RS over LL, 1 AG over LL, 2 RS fixed,

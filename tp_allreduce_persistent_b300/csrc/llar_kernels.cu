@@ -396,14 +396,14 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
     if (j >= j1) return;
     constexpr unsigned S = (unsigned)kSenPubSlots, F = (unsigned)kSenFencePeriod, D = 2 * F;
     static_assert(S == 4 * F && F >= 2, "the credit chain needs S = 4F slots and F >= 2");
+    static_assert(2 * F < 32, "the history mask keeps the last 2F steps");
     const size_t ring = (size_t)CV * 16;  // bytes per slot
-    auto cell = [&](int q, unsigned t) -> char* {
-      return p.sen + (size_t)q * p.sen_stride + (size_t)(t % S) * ring + (size_t)j * 16;
-    };
+    char* const col = p.sen + (size_t)j * 16;  // vector j's cell in slot 0 of rank 0's ring
+    auto cell = [&](int q, size_t slot_off) -> char* { return col + (size_t)q * p.sen_stride + slot_off; };
     auto tail_word = [&](int q) -> u64* {
       return reinterpret_cast<u64*>(p.sen + (size_t)q * p.sen_stride + (size_t)S * kSenMaxChunkBytes) + j;
     };
-    auto has_at = [&](unsigned t) { return (t % nchunks) * CV + j < NV; };
+    unsigned hist = 0;  // bit i: step t - i had vector j (after this step's bit is shifted in)
     bool lag = false;  // step t - 1 had my vector j: its output is still to be stored
     char* lag_dst = nullptr;
     char* lag_chain = nullptr;
@@ -460,12 +460,15 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
     bool have_next = false;
     uint4 next_own = ones;
     unsigned t = 0;
+    size_t slot_off = 0;                          // (t % S) * ring
+    size_t reset_off = (size_t)(S - D) * ring;    // ((t - D) % S) * ring
+    auto advance = [&](size_t off) { return off + ring == (size_t)S * ring ? (size_t)0 : off + ring; };
     u64 E = epoch0;
     for (int e = 0; e < p.iters; ++e) {
       E = epoch0 + (u64)e;
       const char* src = input(e);
       char* dst = rank_output<DT>(p, r, e);
-      for (unsigned k = 0; k < nchunks; ++k, ++t) {
+      for (unsigned k = 0; k < nchunks; ++k, ++t, slot_off = advance(slot_off), reset_off = advance(reset_off)) {
         if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
         // a chain reduces first: with one chunk per iteration its next input is
         // that reduction's output, and otherwise the input load of the
@@ -475,14 +478,15 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
         if (t > 0 && t % F == 0) fence_gpu();
         const unsigned v = k * CV + j;
         const bool has = v < NV;
+        hist = (hist << 1) | (has ? 1u : 0u);
         uint4 own = ones;
         if (has) {
           own = have_next ? next_own
                           : ((CHAIN && e > 0 && nchunks == 1) ? (poison ? ones : lag_nx) : load_cg(src, v));
-          if (!skip) st_relaxed_v4(cell(r, t), own);
+          if (!skip) st_relaxed_v4(cell(r, slot_off), own);
         }
         reduce_pending();
-        if (t >= D && has_at(t - D) && !skip) st_relaxed_v4(cell(r, t - D), ones);
+        if (t >= D && ((hist >> D) & 1u) && !skip) st_relaxed_v4(cell(r, reset_off), ones);
         store_lagged();
         have_next = false;
         if (ahead) {
@@ -502,7 +506,7 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
           uint4 tv[N];
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if ((pend >> q) & 1u) tv[q] = ld_relaxed_v4(cell(q, t));
+            if ((pend >> q) & 1u) tv[q] = ld_relaxed_v4(cell(q, slot_off));
 #pragma unroll
           for (int q = 0; q < N; ++q)
             if (((pend >> q) & 1u) && !has_sentinel<DT>(tv[q])) {
@@ -546,8 +550,12 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
       }
     }
     fence_gpu();
-    for (unsigned u = t > D ? t - D : 0u; u < t; ++u)
-      if (has_at(u)) st_relaxed_v4(cell(r, u), ones);
+    // chunks t - 1, t - 2, ..., t - D (those that exist), newest first
+    size_t off = slot_off;
+    for (unsigned i = 0; i < D && i < t; ++i) {
+      off = off == 0 ? (size_t)(S - 1) * ring : off - ring;
+      if ((hist >> i) & 1u) st_relaxed_v4(cell(r, off), ones);
+    }
     return;
   }
 
@@ -1002,6 +1010,156 @@ __device__ __forceinline__ void body_ll128(const Params& p, const u64 epoch0) {
       }
     }
     if (__any_sync(0xFFFFFFFFu, failed)) return;
+  }
+}
+
+// Technique 4 with the AllGather read straight from the owners' lines (a
+// variant beside the pages' LL AllGather): the ReduceScatter is the same
+// (data reductions into owner s's line, a fence, the count), but instead of
+// the owner reading its lines and publishing them again as LL lines, every
+// rank polls each owner's line until the count reads N (acquire) and reads
+// the reduced data there. That removes one store -> load hop and the LL
+// copy of every segment. Lines then stay read for an AllReduce after their
+// count completes, so each owner keeps three slots in turn: sequence
+// number s (a per-context counter of these AllReduces, advanced like the
+// epoch) uses slot s % 3, and when the owner sees the count of its line in
+// slot s % 3 reach N it zeroes the same line in slot (s - 1) % 3. That is
+// safe: each contributor added to slot s % 3 after (program order, then the
+// fence before its count) it had read every line of s - 1. The zeroed slot
+// is next used by s + 2, whose additions each contributor makes only after
+// it saw the count N of s + 1 on that owner's line, which includes the
+// owner's own count, added after a fence that follows the zeroing. After a
+// launch only the last slot holds data, in the lines that launch used (its
+// line count is kept beside the sequence counter); the next launch's first
+// AllReduce zeroes all of them at once (the launch boundary orders every
+// read of that slot before), since its own, possibly fewer, lines would
+// leave the rest.
+template <int DT>
+__device__ __forceinline__ void body_ll128d(const Params& p, const u64 epoch0, const u64 seq0,
+                                            const size_t lines_prev) {
+  constexpr int EB = Fmt<DT>::kBytes;
+  constexpr int EL = 128 / EB;  // elements per line
+  constexpr int P = EL - 1;     // data elements per line
+  const int N = p.nranks;
+  const int r = rank_of_block(p);
+  const int c = cta_of_block(p);
+  const size_t count = p.count;
+  const size_t seg = (count + N - 1) / N;
+  const size_t L = (seg + P - 1) / P;
+  const size_t Lc = (L + p.G - 1) / p.G;
+  const size_t l0 = min(L, (size_t)c * Lc);
+  const size_t nl = min(L, l0 + Lc) - l0;
+  const unsigned per_seg = (unsigned)(nl * kLL128Lanes);  // fewer than 2^32 items, as in body_ll128
+  const unsigned items = (unsigned)N * per_seg;
+  const unsigned T = blockDim.x;
+  const unsigned one_bits = Fmt<DT>::from_f(1.0f);
+  const unsigned n_bits = Fmt<DT>::from_f((float)N);
+  const unsigned flag_mask = (EB == 4) ? 0xFFFFFFFFu : 0xFFFFu;
+  const bool injected = (p.inject_rank == r);
+  const bool skip = injected && p.inject_mode == LLAR_INJECT_SKIP_;
+  const bool poison = injected && p.inject_mode == LLAR_INJECT_POISON_;
+  const size_t line_slot = p.l128_lines * (size_t)kLL128Line;
+  char* const my_lines = p.l128d + (size_t)r * p.l128d_stride;
+  bool failed = false;
+  {
+    // the previous launch's last slot, every line it used, my segment:
+    // this CTA's share of (line, lane) items
+    const size_t Lp = min(lines_prev, (size_t)p.l128_lines);
+    const size_t Lpc = (Lp + p.G - 1) / p.G;
+    const size_t lp0 = min(Lp, (size_t)c * Lpc), lp1 = min(Lp, lp0 + Lpc);
+    char* const last = my_lines + (size_t)(seq0 % 3) * line_slot;
+    for (size_t i = lp0 * kLL128Lanes + threadIdx.x; i < lp1 * kLL128Lanes; i += T)
+      st_relaxed_v4(last + i * 16, make_uint4(0, 0, 0, 0));
+  }
+
+  for (int e = 0; e < p.iters; ++e) {
+    const u64 E = epoch0 + (u64)e;
+    const u64 sq = seq0 + 1 + (u64)e;
+    const size_t slot = (size_t)(sq % 3), prev = (size_t)((sq + 2) % 3);
+    const char* src = rank_input<DT>(p, r, e);
+    char* dst = rank_output<DT>(p, r, e);
+    if (injected && p.inject_mode == LLAR_INJECT_DELAY_) injected_delay();
+
+    // ---- ReduceScatter: add my data into every owner's lines
+    if (!skip) {
+      for (unsigned i = threadIdx.x; i < items; i += T) {
+        const int s = (int)(i / per_seg);
+        const unsigned rem = i - (unsigned)s * per_seg;
+        const size_t l = l0 + rem / kLL128Lanes;
+        const int j = (int)(rem % kLL128Lanes);
+        unsigned w[4];
+        if (ll128_gather<DT>(src, count, seg, s, l, j, w))
+          red_add_v4<DT>(p.l128d + (size_t)s * p.l128d_stride + slot * line_slot + l * kLL128Line + j * 16, w);
+      }
+    }
+    __syncwarp();
+    fence_gpu();  // every data reduction (and zeroing) of this warp before its counts
+    if (!skip) {
+      for (unsigned i = threadIdx.x; i < items; i += T) {
+        if ((i % kLL128Lanes) != 0) continue;
+        const int s = (int)(i / per_seg);
+        const size_t l = l0 + (i - (unsigned)s * per_seg) / kLL128Lanes;
+        red_add_flag<DT>(p.l128d + (size_t)s * p.l128d_stride + slot * line_slot + l * kLL128Line,
+                         poison ? 0u : one_bits);
+      }
+    }
+
+    // ---- AllGather: every owner's line, once its count reads N
+    for (unsigned i = threadIdx.x; i < items; i += T) {
+      const int s = (int)(i / per_seg);
+      const unsigned rem = i - (unsigned)s * per_seg;
+      const size_t l = l0 + rem / kLL128Lanes;
+      const int j = (int)(rem % kLL128Lanes);
+      const char* line = p.l128d + (size_t)s * p.l128d_stride + slot * line_slot + l * kLL128Line;
+      if (!failed) {
+        Waiter wt;
+        for (bool first_round = true;; first_round = false) {
+          LLB_ON_POLL_ROUND(first_round, 1u);
+          if ((ld_acquire_u32(line) & flag_mask) == n_bits) break;
+          if (wt.expired(p)) {
+            report_timeout(p, r, c, E);
+            failed = true;
+            break;
+          }
+        }
+      }
+      if (failed) continue;
+      const uint4 v = ld_relaxed_v4(line + j * 16);
+      const unsigned w[4] = {v.x, v.y, v.z, v.w};
+      ll128_scatter<DT>(dst, 0, count, seg, s, l, j, w);
+      if (p.chain) {
+        unsigned nx[4];
+        chain_words<DT, 4>(w, nx, p.chain_scale);
+        ll128_scatter<DT>(chain_next_buf(p, r, e), 0, count, seg, s, l, j, nx);
+      }
+      // the owner: every contributor has read this line's previous slot
+      if (s == r) st_relaxed_v4(my_lines + prev * line_slot + l * kLL128Line + j * 16, make_uint4(0, 0, 0, 0));
+    }
+    if (__any_sync(0xFFFFFFFFu, failed)) return;
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_ll128d(const Params p) {
+  const u64 epoch0 = launch_epoch(p);
+  const u64 seq0 = *reinterpret_cast<volatile const u64*>(p.l128d_seq);
+  const u64 lines_prev = *reinterpret_cast<volatile const u64*>(p.l128d_seq + 1);
+  body_ll128d<DT>(p, epoch0, seq0, (size_t)lines_prev);
+  // as k_ll128: rank 0's CTA c waited for every contribution to every line
+  // of its range, each made after its CTA read both counters; the last of
+  // rank 0's CTAs advances the sequence counter with the epoch
+  __syncthreads();
+  if (threadIdx.x == 0 && rank_of_block(p) == 0) {
+    if (atomicAdd(p.done_count, 1u) == (unsigned)p.G - 1) {
+      *reinterpret_cast<volatile unsigned*>(p.done_count) = 0u;
+      volatile u64* ep = p.epoch_dev;
+      *ep = *ep + (u64)p.iters;
+      volatile u64* sp = p.l128d_seq;
+      *sp = *sp + (u64)p.iters;
+      // the lines of every segment this launch used (the same in every AllReduce)
+      const size_t seg = (p.count + p.nranks - 1) / p.nranks;
+      sp[1] = (u64)((seg + (128 / Fmt<DT>::kBytes - 1) - 1) / (128 / Fmt<DT>::kBytes - 1));
+    }
   }
 }
 
@@ -2099,6 +2257,9 @@ cudaError_t launch_sentinel(int dtype, const Params& p, int threads, cudaStream_
 cudaError_t launch_ll128(int dtype, const Params& p, int threads, cudaStream_t s) {
   LLAR_DISPATCH(k_ll128, true)
 }
+cudaError_t launch_ll128d(int dtype, const Params& p, int threads, cudaStream_t s) {
+  LLAR_DISPATCH(k_ll128d, true)
+}
 cudaError_t launch_fixed_oneshot(int dtype, const Params& p, int threads, cudaStream_t s) {
   LLAR_DISPATCH(k_fixed_oneshot, p.chain != 0)
 }
@@ -2146,6 +2307,7 @@ template <int DT>
 static const void* kernel_for(int proto) {
   switch (proto) {
     case 3: return (const void*)k_ll128<DT>;
+    case 6: return (const void*)k_ll128d<DT>;
     case 4: return (const void*)k_fixed_oneshot<DT>;
     case 5: return (const void*)k_fixed_twoshot<DT>;
     default: return nullptr;

@@ -46,6 +46,7 @@ struct Ctx {
   size_t sen_off = 0, sen_stride = 0;
   size_t l128_off = 0, l128_stride = 0, l128_lines = 0;
   size_t ag_off = 0, ag_stride = 0;
+  size_t l128d_off = 0, l128d_stride = 0;  // [3 slots][lines][128 B] of LLAR_PROTO_LL128_DIRECT
   size_t chain_off = 0, chain_stride = 0, chain_slot = 0;
   size_t flags_off = 0, abort_off = 0;
   llar::DevStatus* status_host = nullptr;
@@ -105,7 +106,9 @@ size_t ll128_lines_for(size_t count, int n, int dtype) {
 }
 
 bool valid_dtype(int d) { return d == LLAR_F32 || d == LLAR_F16 || d == LLAR_BF16; }
-bool valid_proto(int p) { return p >= LLAR_PROTO_AUTO && p <= LLAR_PROTO_FIXED_TWOSHOT; }
+bool valid_proto(int p) { return p >= LLAR_PROTO_AUTO && p <= LLAR_PROTO_LL128_DIRECT; }
+// the two-shot LL128 atomic protocols: the pages' LL AllGather, or reads from the owners' lines
+bool is_ll128(int p) { return p == LLAR_PROTO_LL128_ATOMIC || p == LLAR_PROTO_LL128_DIRECT; }
 
 // AUTO, per rank count. Measured on a B300 (bf16, one call per launch,
 // replayed from a CUDA graph, 2 KiB .. 4 MiB per rank): LL is fastest up
@@ -134,7 +137,7 @@ int select_protocol(int n, int dtype, size_t count) {
   const char* force = std::getenv("LLAR_PROTO");
   if (force && *force) {
     const int f = std::atoi(force);
-    if (f >= LLAR_PROTO_LL && f <= LLAR_PROTO_FIXED_TWOSHOT) return f;
+    if (f >= LLAR_PROTO_LL && f <= LLAR_PROTO_LL128_DIRECT) return f;
   }
   const size_t bytes = count * elem_bytes(dtype);
   const AutoRule rule = auto_rule(n);
@@ -153,7 +156,8 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
   switch (proto) {
     case LLAR_PROTO_LL: units = (count * e + 7) / 8; break;
     case LLAR_PROTO_SENTINEL: units = std::min(c.chunk_bytes, round_up(count * e, 16)) / 16; break;
-    case LLAR_PROTO_LL128_ATOMIC: units = ll128_lines_for(count, n, c.dtype) * n * llar::kLL128Lanes; break;
+    case LLAR_PROTO_LL128_ATOMIC:
+    case LLAR_PROTO_LL128_DIRECT: units = ll128_lines_for(count, n, c.dtype) * n * llar::kLL128Lanes; break;
     default: units = (count * e + 15) / 16; break;
   }
   int g = 1;
@@ -172,7 +176,7 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
     const size_t want = std::max<size_t>((units + t - 1) / t, 16);
     g = (int)std::min<size_t>(want, (size_t)std::max(1, 2 * c.sms / n));
     if (want > (size_t)g) t = (int)std::min<size_t>(llar::kMaxThreads, round_up((units + g - 1) / g, 32));
-  } else if (proto == LLAR_PROTO_LL128_ATOMIC && units > (size_t)one_per_sm * llar::kMaxThreads) {
+  } else if (is_ll128(proto) && units > (size_t)one_per_sm * llar::kMaxThreads) {
     // more (segment, line, lane) items than one CTA of 512 threads per SM
     // covers: as many resident CTAs of 256 threads as fit (the capacity
     // check clamps G); 8 ranks x 1 MiB bf16, one call: 23.1 -> 20.9 us
@@ -187,7 +191,7 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
       const size_t per_cta = (units + g - 1) / g;
       t = (int)std::min<size_t>(llar::kMaxThreads, round_up(per_cta, 32));
     }
-    if (proto == LLAR_PROTO_LL128_ATOMIC) {
+    if (is_ll128(proto)) {
       // a CTA takes whole lines, ceil(L / g) of every segment: threads for
       // all of its items in one pass (8 ranks x 128 KiB bf16 chain: 480
       // threads left 32 of 512 items for a second pass, 5.17 us per layer;
@@ -259,6 +263,9 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
   p.l128ag = c.base + c.ag_off;
   p.l128ag_stride = c.ag_stride;
   p.l128_lines = c.l128_lines;
+  p.l128d = c.base + c.l128d_off;
+  p.l128d_stride = c.l128d_stride;
+  p.l128d_seq = reinterpret_cast<unsigned long long*>(c.base + c.abort_off + 192);
   p.chainbuf = c.base + c.chain_off;
   p.chain_stride = c.chain_stride;
   p.chain_slot_bytes = c.chain_slot;
@@ -452,7 +459,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   if (proto == LLAR_PROTO_AUTO) proto = select_protocol(c.n, c.dtype, count);
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
-  if (proto == LLAR_PROTO_LL128_ATOMIC && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
+  if (is_ll128(proto) && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
   int st = check_ptrs(in, out, c.n, in_span, out_span);
   if (st != LLAR_OK) return st;
   if (c.status_host->code != 0) return LLAR_ERR_TIMEOUT;
@@ -469,7 +476,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   int G = 1, T = 128;
   choose_shape(c, proto, count, chain, &G, &T);
   const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
-                    proto == LLAR_PROTO_LL128_ATOMIC || chain;
+                    is_ll128(proto) || chain;
   // Thread-block clusters put the N CTAs that serve one range on one GPC.
   // Measured on B300 (8 ranks, bf16, CTAs per rank as chosen above): they
   // help the sentinel protocol (64 KiB in 8 KiB chunks: 18.0 -> 15.1 us)
@@ -509,6 +516,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
     case LLAR_PROTO_LL: err = llar::launch_ll(c.dtype, p, T, stream); break;
     case LLAR_PROTO_SENTINEL: err = llar::launch_sentinel(c.dtype, p, T, stream); break;
     case LLAR_PROTO_LL128_ATOMIC: err = llar::launch_ll128(c.dtype, p, T, stream); break;
+    case LLAR_PROTO_LL128_DIRECT: err = llar::launch_ll128d(c.dtype, p, T, stream); break;
     case LLAR_PROTO_FIXED_ONESHOT: err = llar::launch_fixed_oneshot(c.dtype, p, T, stream); break;
     default:
       if (!chain && g_bulk && bytes >= bulk_min_bytes(c.n) && g_force_G == 0) {
@@ -543,6 +551,8 @@ int fill_staging(Ctx& c, cudaStream_t s) {
   ok(cudaMemsetAsync(c.base + c.sen_off, 0xFF, c.sen_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.l128_off, 0, c.l128_stride * c.n, s));
   ok(cudaMemsetAsync(c.base + c.ag_off, 0, c.ag_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.l128d_off, 0, c.l128d_stride * c.n, s));
+  ok(cudaMemsetAsync(c.base + c.abort_off + 192, 0, 16, s));  // direct LL128 sequence and last line count
   ok(cudaMemsetAsync(c.base + c.flags_off, 0, (size_t)c.n * kFlagsGmax * llar::kFlagKinds * 8, s));
   // abort word only: the epoch counter at +128 keeps counting across resets
   ok(cudaMemsetAsync(c.base + c.abort_off, 0, 4, s));
@@ -610,6 +620,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   c->l128_lines = ll128_lines_for(c->ll128_cap / c->esize, n, dtype);
   region(2 * c->l128_lines * llar::kLL128Line, &c->l128_off, &c->l128_stride);
   region(2 * c->l128_lines * llar::kAgLineBytes, &c->ag_off, &c->ag_stride);
+  region(3 * c->l128_lines * llar::kLL128Line, &c->l128d_off, &c->l128d_stride);
   c->chain_slot = round_up(c->max_bytes, kAlign);
   region(2 * c->chain_slot, &c->chain_off, &c->chain_stride);
   c->flags_off = off;
@@ -929,6 +940,7 @@ int llar_staging(int protocol, void** dev_ptr, size_t* rank_stride_bytes, size_t
     case LLAR_PROTO_LL: off = c.ll_off; stride = c.ll_stride; used = 2 * c.ll_words * llar::kLLLine; break;
     case LLAR_PROTO_SENTINEL: off = c.sen_off; stride = c.sen_stride; used = sen_slots(c.n) * c.chunk_bytes; break;
     case LLAR_PROTO_LL128_ATOMIC: off = c.l128_off; stride = c.l128_stride; used = 2 * c.l128_lines * llar::kLL128Line; break;
+    case LLAR_PROTO_LL128_DIRECT: off = c.l128d_off; stride = c.l128d_stride; used = 3 * c.l128_lines * llar::kLL128Line; break;
     default: return LLAR_ERR_UNSUPPORTED;
   }
   if (dev_ptr) *dev_ptr = c.base + off;
@@ -957,9 +969,11 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
       break;
     }
     case LLAR_PROTO_LL128_ATOMIC:
+    case LLAR_PROTO_LL128_DIRECT:
       lb = llar::kLL128Line;
       pl = ll128_payload(dtype);
-      st = 2 * ll128_lines_for(count, nranks, dtype) * llar::kLL128Line;
+      // two slots (LL AllGather) or three (AllGather read from the lines)
+      st = (protocol == LLAR_PROTO_LL128_DIRECT ? 3 : 2) * ll128_lines_for(count, nranks, dtype) * llar::kLL128Line;
       break;
     default: st = 0; break;
   }
@@ -997,7 +1011,7 @@ int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters
 int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, int chained, int sms,
                             size_t chunk_bytes, int* ctas_per_rank, int* threads) {
   if (nranks < 2 || nranks > llar::kMaxRanks || !valid_dtype(dtype) || count == 0 || sms < 1) return LLAR_ERR_INVALID;
-  if (protocol < LLAR_PROTO_LL || protocol > LLAR_PROTO_FIXED_TWOSHOT) return LLAR_ERR_INVALID;
+  if (protocol < LLAR_PROTO_LL || protocol > LLAR_PROTO_LL128_DIRECT) return LLAR_ERR_INVALID;
   if (chunk_bytes == 0 || chunk_bytes % 16 || chunk_bytes > kMaxChunk) return LLAR_ERR_INVALID;
   Ctx c;  // host arithmetic only: no device memory behind it
   c.n = nranks;

@@ -15,7 +15,7 @@ LIB_PATH = os.environ.get("LLAR_LIBRARY") or os.path.join(HERE, "libllar.so")
 
 DTYPES = {"fp32": 0, "fp16": 1, "bf16": 2}
 PROTOCOLS = {"auto": 0, "ll": 1, "sentinel": 2, "ll128": 3,
-             "fixed_oneshot": 4, "fixed_twoshot": 5}
+             "fixed_oneshot": 4, "fixed_twoshot": 5, "ll128_direct": 6}
 PROTOCOL_NAMES = {v: k for k, v in PROTOCOLS.items()}
 INJECT = {"none": 0, "skip": 1, "poison": 2, "delay": 3}
 OK, ERR_INVALID, ERR_NOT_INIT, ERR_TOO_LARGE, ERR_UNSUPPORTED, ERR_OCCUPANCY, ERR_CUDA, ERR_TIMEOUT = range(8)
