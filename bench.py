@@ -358,6 +358,7 @@ CONFIG_CASES = {
     "C4_sentinel": (8, "fp16", 32768, "sentinel", 1000, 0.0, 8192),
     "C5_ll128_chain_N8": (8, "bf16", 65536, "ll128", 160, 0.5, None),
     "C3_ll128_direct_1MiB": (8, "bf16", 1024 * 512, "ll128_direct", 200, 0.0, None),
+    "headline_dependent_ll": (8, "bf16", 8192, "ll", 10000, 1.0 / 8, None),
     "C3_ll128_direct_16KiB": (8, "bf16", 16 * 512, "ll128_direct", 1000, 0.0, None),
 }
 # fused decode layers for `--leg config --case NAME`: (ranks, tokens m, K, H), bf16

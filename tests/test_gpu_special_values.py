@@ -222,3 +222,53 @@ def test_ll128_fp32_flushes_subnormals_and_16bit_keeps_them(n):
             ok, err, rel = orc.compare_atomic(got, orc.allreduce(xb, dtype), xb, dtype)
             assert ok, (dtype, err, rel)
             assert np.any(got != 0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("proto", ["ll", "fixed_oneshot", "sentinel", "ll128"])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [3, 8])
+def test_special_values_reduce_scatter(proto, dtype, n):
+    # the first half of the two-shot on the same special columns
+    count = 4099
+    xb = special_inputs(n, count, dtype, seed=40 + n)
+    seg = -(-count // n)
+    with context(n, dtype, 1 << 20):
+        ins = [_torch_of(xb[r], dtype).cuda() for r in range(n)]
+        outs = [torch.empty(seg, dtype=inputs.TORCH_DTYPE[dtype], device="cuda") for _ in range(n)]
+        llar.llar_reduce_scatter(ins, outs, count, proto)
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.OK
+    want = orc.reduce_scatter(xb, dtype)
+    for s in range(n):
+        got = inputs.bits_of(outs[s])[: len(want[s])]
+        if proto == "ll128":
+            lo, hi = orc.shard_bounds(count, n, s)
+            ok, err, rel = orc.compare_atomic(got[None], want[s][None], xb[:, lo:hi], dtype,
+                                              flush_subnormals=dtype == "fp32")
+            assert ok, (s, err, rel)
+        else:
+            assert_same_up_to_nan_payload(got[None], want[s], dtype, (proto, dtype, n, s))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "ll128"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_special_values_llbuffer_allreduce(proto, dtype):
+    # the AllReduces written on the public device primitives
+    n, count = 8, 4099
+    xb = special_inputs(n, count, dtype, seed=50)
+    with llar.LLBuffer(n, count * inputs.ELEM_BYTES[dtype]) as buf:
+        ins = [_torch_of(xb[r], dtype).cuda() for r in range(n)]
+        outs = [torch.empty_like(t) for t in ins]
+        buf.allreduce(ins, outs, count, dtype, proto)
+        torch.cuda.synchronize()
+        assert buf.status()[0] == llar.OK
+    got = np.stack([inputs.bits_of(o) for o in outs])
+    want = orc.allreduce(xb, dtype)
+    assert all(np.array_equal(got[0], got[r]) for r in range(1, n))
+    if proto == "ll128":
+        ok, err, rel = orc.compare_atomic(got, want, xb, dtype, flush_subnormals=dtype == "fp32")
+        assert ok, (err, rel)
+    else:
+        assert_same_up_to_nan_payload(got, want[0], dtype, (proto, dtype))
