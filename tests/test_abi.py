@@ -47,6 +47,10 @@ def test_layout_constants(dtype):
     lb, pl, st = llar.llar_layout("ll128", dtype, 8, 1 << 20)
     assert lb == 128 and pl == oproto.ll128_payload_elems(dtype)
     assert st == 2 * oproto.ll128_round_staging_bytes(1 << 20, 8, dtype)
+    # the direct-AllGather variant: the same lines, three slots, no LL copy
+    lb, pl, st = llar.llar_layout("ll128_direct", dtype, 8, 1 << 20)
+    assert lb == 128 and pl == oproto.ll128_payload_elems(dtype)
+    assert st == 3 * oproto.ll128_round_staging_bytes(1 << 20, 8, dtype)
     lb, pl, st = llar.llar_layout("sentinel", dtype, 8, 32768)
     # published once per rank: a ring of 32 slots of the 64 KiB default chunk, one tail word per vector
     assert lb == 16 and pl * e == 16 and st == 32 * 65536 + 65536 // 16 * 8
@@ -106,6 +110,14 @@ def test_argument_checks_without_device():
         with pytest.raises(llar.LlarError) as ei:
             call()
         assert ei.value.code == llar.ERR_NOT_INIT
+    # so does the placed speed-of-light probe (it takes the last launch's shape)
+    with pytest.raises(llar.LlarError) as ei:
+        llar.llar_sol_probe_placed()
+    assert ei.value.code == llar.ERR_NOT_INIT
+    # an unknown protocol value
+    with pytest.raises(llar.LlarError) as ei:
+        llar.llar_debug_launch_shape(8, "bf16", 8192, 7)
+    assert ei.value.code == llar.ERR_INVALID
     assert llar.strerror(llar.ERR_TIMEOUT) == "a device-side wait timed out"
 
 

@@ -88,3 +88,14 @@ def test_forced_shape_is_reported_and_arguments_are_checked():
         assert ei.value.code == llar.ERR_INVALID
     with pytest.raises(llar.LlarError):
         llar.llar_debug_launch_shape(8, "bf16", 8, "sentinel", False, SMS, 24)  # chunk not a multiple of 16
+
+
+def test_ll128_direct_takes_the_ll128_shapes():
+    # the direct-AllGather variant runs the same (segment, line, lane) items
+    rng = random.Random(5)
+    for _ in range(200):
+        n = rng.randint(2, 8)
+        dtype = rng.choice(["fp32", "fp16", "bf16"])
+        count = rng.choice([1, 63, 500, rng.randint(1, 1 << 20)])
+        chained = rng.random() < 0.3
+        assert shape(n, dtype, count, "ll128_direct", chained) == shape(n, dtype, count, "ll128", chained)
