@@ -483,7 +483,9 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
         if (has) {
           own = have_next ? next_own
                           : ((CHAIN && e > 0 && nchunks == 1) ? (poison ? ones : lag_nx) : load_cg(src, v));
-          if (!skip) st_relaxed_v4(cell(r, slot_off), own);
+          // one 128-bit access: a poller sees all of it or none of it
+          if (!skip)
+            st_relaxed_b128(cell(r, slot_off), (u64)own.x | ((u64)own.y << 32), (u64)own.z | ((u64)own.w << 32));
         }
         reduce_pending();
         if (t >= D && ((hist >> D) & 1u) && !skip) st_relaxed_v4(cell(r, reset_off), ones);
@@ -501,16 +503,20 @@ __device__ __forceinline__ void body_sentinel(const Params& p, const u64 epoch0)
         uint4 d[N];
         unsigned pend = others;
         Waiter wt;
+        // each vector is read as one 128-bit access (published as one): it
+        // is either still all-ones or entirely the new data, which holds no
+        // all-ones element, so one test of all 128 bits replaces a test of
+        // every element
         for (bool first_round = true;; first_round = false) {
           LLB_ON_POLL_ROUND(first_round, pend);
-          uint4 tv[N];
+          u64 lo[N], hi[N];
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if ((pend >> q) & 1u) tv[q] = ld_relaxed_v4(cell(q, slot_off));
+            if ((pend >> q) & 1u) ld_relaxed_b128(cell(q, slot_off), lo[q], hi[q]);
 #pragma unroll
           for (int q = 0; q < N; ++q)
-            if (((pend >> q) & 1u) && !has_sentinel<DT>(tv[q])) {
-              d[q] = tv[q];
+            if (((pend >> q) & 1u) && (lo[q] & hi[q]) != ~0ull) {
+              d[q] = make_uint4((unsigned)lo[q], (unsigned)(lo[q] >> 32), (unsigned)hi[q], (unsigned)(hi[q] >> 32));
               pend &= ~(1u << q);
             }
           if (pend == 0u) break;
