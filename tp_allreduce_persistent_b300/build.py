@@ -61,7 +61,7 @@ def build(force=False, verbose=False, defines=(), out=None):
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
     target = out or LIB
     tmp = target + ".tmp"
-    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
+    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "--threads", "3",
            "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
            "-cudart", "shared", "-Xlinker", "-rpath=" + cuda_lib,
            "-o", tmp] + ["-D" + d for d in defines] + [os.path.join(CSRC, f) for f in SOURCES]
