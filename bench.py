@@ -789,6 +789,7 @@ def run_ours(args, world, rank, local, pg):
     peaks, peak_src = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
 
+    ll_clustered = llar.llar_ll_placement()  # chosen by timing both placements at llar_init
     l2_us, write_us, sol_us = llar.llar_sol_probe()
     detail = llar.llar_sol_probe_detail()
     props = torch.cuda.get_device_properties(local)
@@ -832,7 +833,8 @@ def run_ours(args, world, rank, local, pg):
         config.update({"workload": f"8 virtual ranks x 16 KiB bf16 (8192 elements) AllReduce, "
                                    f"{args.iters} back-to-back per persistent launch",
                        "nranks": NRANKS, "count": COUNT, "iters_per_launch": args.iters,
-                       "protocol": lat["proto"], "ctas_per_rank": lat["G"], "threads_per_cta": lat["T"]})
+                       "protocol": lat["proto"], "ctas_per_rank": lat["G"], "threads_per_cta": lat["T"],
+                       "ll_clusters_of_n_blocks": bool(ll_clustered)})
         dep_us = max_over_ranks(pg, lat["dependent"]["us_per_ar"], dev)
         res["latency_roofline"] = {
             "kernel": f"k_{lat['proto']}<bf16>", "bound": "latency (L2 round trips)",

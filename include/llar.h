@@ -250,6 +250,16 @@ int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us);
  * Synchronises the device. */
 int llar_sol_probe_placed(double* l2_rt_us, double* write_us, double* sol_us, int* npairs);
 
+/* LL placement chosen for this context (diagnostic; no page describes
+ * it): *clustered = 1 if LL launches of 16 or more AllReduces run in
+ * clusters of N blocks (the CTAs that exchange a word range on one GPC),
+ * 0 if not. llar_init times both on this GPU (a few hundred 16 KiB
+ * AllReduces each, a few milliseconds) and keeps clusters only if they are
+ * at least 3 % faster: which placement is faster differs between GPUs of
+ * the same model. LLAR_TUNE=0 skips the timing (no clusters); LLAR_CLUSTER
+ * = 0 or 2 forces it. Results are identical either way. */
+int llar_ll_placement(int* clustered);
+
 /* The speed-of-light bound itself (host only): 2 * l2_rt_us + write_us. */
 double llar_sol_bound_us(double l2_rt_us, double write_us);
 

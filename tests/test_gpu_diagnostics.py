@@ -15,6 +15,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch
 
@@ -100,3 +101,26 @@ def test_poll_counting_build_counts_every_awaited_line():
     assert loads >= awaited and rounds >= waits
     rounds, loads, waits, awaited = counts["ll128"]
     assert waits > 0 and loads >= awaited > 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("force", ["0", "2", None])
+def test_ll_placement_either_way_gives_the_oracle(force, monkeypatch):
+    # llar_init times LL with and without clusters of N blocks and keeps the
+    # faster for long launches; LLAR_CLUSTER forces either. The sums are
+    # fixed-order, so every placement must give the oracle's bits.
+    from oracle import allreduce as orc
+    if force is None:
+        monkeypatch.delenv("LLAR_CLUSTER", raising=False)
+    else:
+        monkeypatch.setenv("LLAR_CLUSTER", force)
+    n, count, iters = 8, 8192, 20
+    x = inputs.normal(n, count, "bf16", seed=11, scale=0.02, iters=iters)
+    with context(n, "bf16", count * 2):
+        placed = llar.llar_ll_placement()
+        assert placed in (0, 1)
+        if force is not None:
+            assert placed == (1 if force == "2" else 0)
+        from gpu_util import allreduce_iters
+        got = allreduce_iters(x, "bf16", "ll", iters)
+    assert np.array_equal(got, orc.allreduce_iters(inputs.bits_of(x), iters, "bf16"))

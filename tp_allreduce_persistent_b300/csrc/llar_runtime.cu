@@ -25,6 +25,7 @@ constexpr size_t kMaxHostRegs = 64;               // registered host buffers per
 constexpr size_t kDefaultChunk = 64u << 10;     // sentinel chunk per rank: every chunk costs a round trip and a fence
 constexpr size_t kMaxChunk = 64u << 10;         // largest sentinel chunk
 constexpr int kFlagsGmax = 1024;                // CTAs per rank the chain flags can address
+constexpr int kLLTuneMinIters = 16;             // LL launches the calibrated placement applies to
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t elem_bytes(int dtype) { return dtype == LLAR_F32 ? 4 : 2; }
@@ -64,6 +65,9 @@ struct Ctx {
   // resident-CTA capacity per (protocol, chain, threads, clustered): the
   // occupancy queries cost microseconds, so each is made once
   std::map<long long, int> capacity;
+  // LL launches of many AllReduces in clusters of N blocks (chosen by
+  // calibrate_ll on this GPU)
+  int ll_cluster = 0;
 };
 
 std::mutex g_mu;
@@ -484,7 +488,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   // and hurt LL (16 KiB: 0.79 -> 0.87 us) and LL128 (1 MiB: 21 -> 31 us).
   // LLAR_CLUSTER: 0 never, 1 per protocol (default), 2 always.
   const bool cluster_helps = proto == LLAR_PROTO_SENTINEL || proto == LLAR_PROTO_FIXED_ONESHOT ||
-                             proto == LLAR_PROTO_FIXED_TWOSHOT;
+                             proto == LLAR_PROTO_FIXED_TWOSHOT ||
+                             (proto == LLAR_PROTO_LL && c.ll_cluster && iters >= kLLTuneMinIters);
   p.clustered = (coop && (g_cluster == 2 || (g_cluster == 1 && cluster_helps))) ? 1 : 0;
   p.spread_smem = (coop && (proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL)) ? g_spread : 0;
   if (coop) {
@@ -562,6 +567,61 @@ int fill_staging(Ctx& c, cudaStream_t s) {
 }
 
 }  // namespace
+
+// LL placement. Launched in clusters of N blocks, the N CTAs that exchange
+// each word range sit on one GPC; whether that is faster depends on the
+// GPU. Measured on B300s, 8 ranks x 16 KiB bf16 back to back: without
+// clusters 0.65 us per AllReduce on some GPUs and 0.84-0.85 on others,
+// with clusters 0.72-0.73 on both (dependent chains 0.81 / 0.97 against
+// 0.93). llar_init times both here, on this GPU (300 AllReduces of up to
+// 16 KiB per rank, twice each), and keeps clusters for LL launches of
+// many AllReduces if they are at least 3 % faster. LLAR_TUNE=0 skips it;
+// LLAR_CLUSTER (0 or 2) forces either way. Results are identical either
+// way (the sums are fixed-order); only the timing differs.
+static void calibrate_ll(Ctx& c) {
+  c.ll_cluster = 0;
+  if (env_size("LLAR_TUNE", 1) == 0 || g_cluster != 1) return;
+  const size_t bytes = std::min<size_t>(std::min(c.max_bytes, c.ll_cap), 16u << 10) / 16 * 16;
+  const size_t count = bytes / c.esize;
+  if (count == 0) return;
+  char* buf = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaMalloc(&buf, 2 * (size_t)c.n * bytes) != cudaSuccess || cudaMemset(buf, 0, 2 * (size_t)c.n * bytes) != cudaSuccess ||
+      cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
+    if (buf) cudaFree(buf);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    return;
+  }
+  const void* in[llar::kMaxRanks];
+  void* out[llar::kMaxRanks];
+  for (int r = 0; r < c.n; ++r) {
+    in[r] = buf + (size_t)r * bytes;
+    out[r] = buf + (size_t)(c.n + r) * bytes;
+  }
+  float best[2] = {1e30f, 1e30f};
+  bool ok = true;
+  for (int rep = 0; rep < 3 && ok; ++rep) {
+    for (int pref = 0; pref < 2 && ok; ++pref) {
+      c.ll_cluster = pref;
+      ok = cudaEventRecord(e0, 0) == cudaSuccess &&
+           run(in, out, count, LLAR_PROTO_LL, 300, 0, 0, 0.0f, 0) == LLAR_OK &&
+           cudaEventRecord(e1, 0) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
+      float ms = 0.f;
+      if (ok && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) best[pref] = std::min(best[pref], ms);
+    }
+  }
+  cudaGetLastError();
+  c.ll_cluster = (ok && c.status_host->code == 0 && best[1] < 0.97f * best[0]) ? 1 : 0;
+  if (g_log)
+    std::fprintf(stderr, "llar: LL placement %s (%.3f ms unclustered, %.3f ms clustered, 300 AllReduces)\n",
+                 c.ll_cluster ? "clustered" : "unclustered", best[0], best[1]);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(buf);
+  if (c.status_host->code != 0) fill_staging(c, 0);  // a wait ran out: start the context clean
+}
 
 namespace llar {
 void fault_settings(unsigned long long* timeout_ns, int* inject_rank, int* inject_mode) {
@@ -653,6 +713,8 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
     return st;
   }
   g = c;
+  calibrate_ll(*c);
+  g_last_proto = g_last_G = g_last_T = g_last_iters = g_last_clustered = g_last_spread = 0;  // the user's launches only
   return LLAR_OK;
 }
 
@@ -907,6 +969,13 @@ int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us) {
   if (l2_rt_us) *l2_rt_us = l2;
   if (write_us) *write_us = wr;
   if (sol_us) *sol_us = llar_sol_bound_us(l2, wr);
+  return LLAR_OK;
+}
+
+int llar_ll_placement(int* clustered) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (clustered) *clustered = (g_cluster == 2 || (g_cluster == 1 && g->ll_cluster)) ? 1 : 0;
   return LLAR_OK;
 }
 

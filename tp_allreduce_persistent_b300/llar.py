@@ -90,6 +90,7 @@ def lib():
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
+        "llar_ll_placement": (c_int, [ctypes.POINTER(c_int)]),
         "llar_last_launch": (c_int, [ctypes.POINTER(c_int)] * 4),
         "llar_host_register": (c_int, [c_vp, c_size]),
         "llar_host_unregister": (c_int, [c_vp]),
@@ -279,6 +280,14 @@ def llar_sol_probe():
     a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
     _check(lib().llar_sol_probe(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "llar_sol_probe")
     return a.value, b.value, c.value
+
+
+def llar_ll_placement():
+    """1 if this context runs long LL launches in clusters of N blocks (chosen
+    by timing both at llar_init), else 0."""
+    v = ctypes.c_int()
+    _check(lib().llar_ll_placement(ctypes.byref(v)), "llar_ll_placement")
+    return v.value
 
 
 def llar_sol_probe_placed():
