@@ -917,40 +917,49 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def oracle_partitioned(orc, xb, bounds, pool, out):
-    """The oracle's AllReduce on element ranges [bounds[i], bounds[i+1]),
-    one range per worker thread (numpy releases the GIL inside its loops);
-    the arithmetic per element is unchanged, so the bits are the same."""
-    def one(i):
-        lo, hi = bounds[i], bounds[i + 1]
-        out[:, lo:hi] = orc.allreduce(xb[:, lo:hi], DTYPE)
-    list(pool.map(one, range(len(bounds) - 1)))
-    return out
+def _oracle_slice_worker(job):
+    """One worker process of the all-core CPU baseline: the oracle's
+    AllReduce on one element slice, repeated from a common start time for
+    `seconds`; returns (AllReduces done, seconds taken, the slice's result)."""
+    xs, start_at, seconds = job
+    from oracle import allreduce as orc
+    y = orc.allreduce(xs, DTYPE)
+    time.sleep(max(0.0, start_at - time.time()))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        y = orc.allreduce(xs, DTYPE)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return n, el, y
 
 
-def time_oracle_all_cores(seconds, count=COUNT, nranks=NRANKS):
+def time_oracle_all_cores(seconds, count=COUNT, nranks=NRANKS, parts=None):
     """The same AllReduces, element-partitioned over every host core the
-    process may use; returns (us per AllReduce, AllReduces, threads)."""
-    from concurrent.futures import ThreadPoolExecutor
+    process may use: one spawned worker process per slice, all running at
+    once from a common start (threads would take turns on the interpreter
+    lock, which numpy holds between its small calls). The arithmetic per
+    element is the oracle's, so the joined slices are its bits. An
+    AllReduce is done when every slice is, so its time is the slowest
+    worker's. Returns (us per AllReduce, AllReduces of the slowest worker,
+    processes, inputs, joined outputs)."""
+    import multiprocessing
+    from concurrent.futures import ProcessPoolExecutor
 
     import numpy as np
 
-    from oracle import allreduce as orc
     from tp_allreduce_persistent_b300 import inputs
-    cores = host_cores()
+    parts = parts or host_cores()
     xb = inputs.bits_of(inputs.normal(nranks, count, DTYPE, seed=1, scale=0.02))
-    bounds = [count * i // cores for i in range(cores + 1)]
-    out = np.empty_like(xb)
-    with ThreadPoolExecutor(cores) as pool:
-        oracle_partitioned(orc, xb, bounds, pool, out)
-        n = 0
-        t0 = time.perf_counter()
-        while True:
-            oracle_partitioned(orc, xb, bounds, pool, out)
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= seconds:
-                return el * 1e6 / n, n, cores
+    bounds = [count * i // parts for i in range(parts + 1)]
+    # a worker that fails to start raises here (BrokenProcessPool), it does not hang
+    with ProcessPoolExecutor(parts, mp_context=multiprocessing.get_context("spawn")) as pool:
+        start_at = time.time() + 1.0 + 0.1 * parts  # every worker started and warm
+        jobs = [(xb[:, bounds[i]:bounds[i + 1]].copy(), start_at, seconds) for i in range(parts)]
+        res = list(pool.map(_oracle_slice_worker, jobs))
+    us = max(el / n for n, el, _ in res) * 1e6
+    out = np.concatenate([y for _, _, y in res], axis=1)
+    return us, min(n for n, _, _ in res), parts, xb, out
 
 
 def run_reference(args, world, rank):
@@ -991,7 +1000,7 @@ def main():
     if rank == 0 and res is not None:  # the llbuffer and config legs print their own line
         if not args.no_cpu_baseline:
             us, n = time_oracle(10.0)
-            us_all, n_all, cores = time_oracle_all_cores(5.0)
+            us_all, n_all, cores, _, _ = time_oracle_all_cores(5.0)
             res["cpu_baseline"] = {"value": round(us, 3), "unit": "us", "cores": 1, "kind": "oracle",
                                    "sample": f"{n} oracle AllReduces of the latency workload in ~10 s "
                                              "on one host core (numpy, single-threaded)",
@@ -999,7 +1008,8 @@ def main():
                                    "all_cores": {"value": round(us_all, 3), "unit": "us", "cores": cores,
                                                  "sample": f"{n_all} oracle AllReduces of the latency "
                                                            f"workload in ~5 s, elements split over "
-                                                           f"{cores} threads (same bits)"}}
+                                                           f"{cores} worker processes running at "
+                                                           "once (same bits)"}}
         print(json.dumps(res), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -87,21 +87,13 @@ def test_config_cases_parse_and_match_the_table_rows():
 
 
 def test_all_core_oracle_gives_the_same_bits():
-    # the element-partitioned timing of the CPU baseline computes exactly the
-    # single-threaded oracle's result, for ragged splits too
-    from concurrent.futures import ThreadPoolExecutor
-
+    # the element-partitioned timing of the CPU baseline (worker processes)
+    # computes exactly the single-threaded oracle's result, ragged splits too
     import numpy as np
 
     from oracle import allreduce as orc
-    from tp_allreduce_persistent_b300 import inputs
-    xb = inputs.bits_of(inputs.normal(8, 1003, "bf16", seed=1, scale=0.02))
-    want = orc.allreduce(xb, "bf16")
-    for parts in (1, 3, 7, 16):
-        bounds = [1003 * i // parts for i in range(parts + 1)]
-        out = np.zeros_like(xb)
-        with ThreadPoolExecutor(parts) as pool:
-            got = bench.oracle_partitioned(orc, xb, bounds, pool, out)
-        assert np.array_equal(got, want), parts
-    us, n, cores = bench.time_oracle_all_cores(0.05, count=512, nranks=4)
-    assert us > 0 and n >= 1 and cores == bench.host_cores()
+    for parts in (1, 3, 7):
+        us, n, used, xb, out = bench.time_oracle_all_cores(0.05, count=1003, nranks=8, parts=parts)
+        assert us > 0 and n >= 1 and used == parts
+        assert np.array_equal(out, orc.allreduce(xb, "bf16")), parts
+    assert bench.time_oracle_all_cores(0.02, count=64, nranks=2)[2] == bench.host_cores()
