@@ -177,10 +177,11 @@ int llar_sendrecv(const void* const* send, void* const* recv, const int* dst, si
  * device-addressable (cudaHostAlloc / cudaHostRegister memory under
  * unified addressing) and count * element size is a multiple of 16, the
  * kernel reads the inputs and writes the outputs across the bus directly
- * (one launch, no staging copies). Otherwise the call copies in, runs and
- * copies out on `stream` through device buffers the library allocates on
- * first use. Returns once the work is queued (synchronise the stream
- * before reading out_host). */
+ * (one launch, no staging copies); there LLAR_PROTO_AUTO follows
+ * llar_select_protocol_host, not llar_select_protocol. Otherwise the call
+ * copies in, runs and copies out on `stream` through device buffers the
+ * library allocates on first use. Returns once the work is queued
+ * (synchronise the stream before reading out_host). */
 int llar_allreduce_host(const void* in_host, void* out_host, size_t count,
                         int protocol, void* stream);
 
@@ -291,6 +292,15 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
  * with TMA bulk copies from 1 MiB (3-4), 512 KiB (5) or 32 KiB (6-8), and
  * never for 2 ranks. LLAR_PROTO (environment) forces a protocol. */
 int llar_select_protocol(int nranks, int dtype, size_t count);
+
+/* The protocol LLAR_PROTO_AUTO picks when llar_allreduce_host reads and
+ * writes host memory directly (host-only). (No page describes it.) The
+ * bus sets the cost there: LL up to 4 KiB per rank (a single call answers
+ * ~1 us sooner), the direct-read two-shot above (8 x 16 KiB bf16: 7.1-7.4
+ * us per call back to back against 8.3-10.1 for LL). LLAR_PROTO
+ * (environment) forces a protocol. LLAR_PROTO_AUTO for an invalid rank
+ * count or dtype. */
+int llar_select_protocol_host(int nranks, int dtype, size_t count);
 
 /* Epoch the next launch will use for its first AllReduce; strictly
  * increasing, never reset. The counter lives in device memory (each launch

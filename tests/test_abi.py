@@ -85,6 +85,19 @@ def test_protocol_selection_is_monotone_in_size():
     assert llar.llar_select_protocol(8, "bf16", 8192) == "ll"
 
 
+def test_host_memory_protocol_selection():
+    # host buffers read across the bus: LL up to 4 KiB per rank, the
+    # direct-read two-shot above, for every rank count and dtype (in bytes)
+    for n in range(2, 9):
+        for dtype, e in (("bf16", 2), ("fp16", 2), ("fp32", 4)):
+            assert llar.llar_select_protocol_host(n, dtype, 16 // e) == "ll"
+            assert llar.llar_select_protocol_host(n, dtype, 4096 // e) == "ll"
+            assert llar.llar_select_protocol_host(n, dtype, 4096 // e + 1) == "fixed_twoshot"
+            assert llar.llar_select_protocol_host(n, dtype, (1 << 20) // e) == "fixed_twoshot"
+    assert llar.llar_select_protocol_host(1, "bf16", 8192) == "auto"
+    assert llar.lib().llar_select_protocol_host(8, 7, 8192) == llar.PROTOCOLS["auto"]  # no such dtype
+
+
 def test_argument_checks_without_device():
     with pytest.raises(llar.LlarError) as ei:
         llar.llar_init(1, "bf16", 1024)

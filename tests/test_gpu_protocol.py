@@ -255,6 +255,29 @@ def test_host_buffer_registration():
         assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype))
 
 
+@pytest.mark.parametrize("n,dtype", [(8, "bf16"), (3, "fp32"), (6, "fp16")])
+def test_host_buffer_auto_follows_the_host_rule(n, dtype):
+    # AUTO on host memory takes the host rule (LL for a few KiB, the direct
+    # two-shot above, which from 32 KiB with 6-8 ranks streams the host
+    # inputs through shared memory with TMA bulk copies); bits as the oracle
+    e = inputs.ELEM_BYTES[dtype]
+    with context(n, dtype, 1 << 20):
+        for nbytes in (64, 4096, 16384 + 16, 65536, 262144 + 32):
+            count = nbytes // e
+            x = inputs.normal(n, count, dtype, seed=nbytes + n).pin_memory()
+            out = torch.empty_like(x).pin_memory()
+            llar.llar_host_register(x)
+            llar.llar_host_register(out)
+            try:
+                llar.llar_allreduce_host(x, out, count, "auto")
+                torch.cuda.synchronize()
+                assert llar.llar_last_launch()[0] == llar.llar_select_protocol_host(n, dtype, count)
+                assert np.array_equal(inputs.bits_of(out), orc.allreduce(inputs.bits_of(x), dtype)), nbytes
+            finally:
+                llar.llar_host_unregister(x)
+                llar.llar_host_unregister(out)
+
+
 def test_host_buffer_entry_point_pageable_and_ragged():
     # pageable host memory (and a row size that is not a multiple of 16
     # bytes) takes the staged-copy path

@@ -137,17 +137,40 @@ size_t bulk_min_bytes(int n) {
   return g_bulk_min_bytes ? g_bulk_min_bytes : auto_rule(n).bulk_min;
 }
 
-int select_protocol(int n, int dtype, size_t count) {
+int forced_protocol() {
   const char* force = std::getenv("LLAR_PROTO");
   if (force && *force) {
     const int f = std::atoi(force);
     if (f >= LLAR_PROTO_LL && f <= LLAR_PROTO_LL128_DIRECT) return f;
   }
+  return LLAR_PROTO_AUTO;
+}
+
+int select_protocol(int n, int dtype, size_t count) {
+  if (const int f = forced_protocol()) return f;
   const size_t bytes = count * elem_bytes(dtype);
   const AutoRule rule = auto_rule(n);
   if (bytes <= rule.ll_max) return LLAR_PROTO_LL;
   if (bytes <= rule.oneshot_max) return LLAR_PROTO_FIXED_ONESHOT;
   return LLAR_PROTO_FIXED_TWOSHOT;
+}
+
+// AUTO when the inputs and outputs are host memory that the kernel reads
+// and writes across the bus (the host-buffer entry's direct path). The bus
+// sets the cost there, and every path moves the same bytes across it; what
+// differs is how many reads are in flight and when the writes start.
+// Measured on a B300 (bf16, pinned registered buffers, 2..8 ranks, 64 B ..
+// 1 MiB per rank): LL answers a single call ~1 us sooner up to a few KiB
+// per rank (13.0-13.3 against 14.0-14.2 us, idle GPU); from 16 KiB the
+// direct-read two-shot is fastest or within a few percent (8 x 16 KiB:
+// 7.1-7.4 us back to back against 8.3-10.1 for LL; 4 x 1 MiB: 128 us
+// against 170), except 8 ranks from 256 KiB, where a sentinel launch with
+// 16 KiB chunks is ~10-25 % faster (the chunk is the caller's setting, so
+// AUTO does not take it).
+int select_protocol_host(int n, int dtype, size_t count) {
+  if (const int f = forced_protocol()) return f;
+  (void)n;
+  return count * elem_bytes(dtype) <= 4096 ? LLAR_PROTO_LL : LLAR_PROTO_FIXED_TWOSHOT;
 }
 
 // CTAs per rank and threads per CTA for one launch.
@@ -784,6 +807,7 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
       }
       return nullptr;
     };
+    const int proto = protocol == LLAR_PROTO_AUTO ? select_protocol_host(c.n, c.dtype, count) : protocol;
     char* rin = registered(in_host, bytes * c.n);
     char* rout = registered(out_host, bytes * c.n);
     if (rin && rout && ((((uintptr_t)rin) | ((uintptr_t)rout)) & 15u) == 0) {
@@ -793,7 +817,7 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
         ins[r] = rin + r * bytes;
         outs[r] = rout + r * bytes;
       }
-      return run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
+      return run(ins, outs, count, proto, 1, 0, 0, 0.0f, s);
     }
     cudaPointerAttributes ai, ao;
     if (cudaPointerGetAttributes(&ai, in_host) == cudaSuccess && cudaPointerGetAttributes(&ao, out_host) == cudaSuccess &&
@@ -805,7 +829,7 @@ int llar_allreduce_host(const void* in_host, void* out_host, size_t count, int p
         ins[r] = static_cast<const char*>(ai.devicePointer) + r * bytes;
         outs[r] = static_cast<char*>(ao.devicePointer) + r * bytes;
       }
-      return run(ins, outs, count, protocol, 1, 0, 0, 0.0f, s);
+      return run(ins, outs, count, proto, 1, 0, 0, 0.0f, s);
     }
     cudaGetLastError();  // pageable memory: not an error, take the copy path
   }
@@ -1055,6 +1079,11 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
 int llar_select_protocol(int nranks, int dtype, size_t count) {
   if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
   return select_protocol(nranks, dtype, count);
+}
+
+int llar_select_protocol_host(int nranks, int dtype, size_t count) {
+  if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
+  return select_protocol_host(nranks, dtype, count);
 }
 
 unsigned long long llar_epoch(void) {

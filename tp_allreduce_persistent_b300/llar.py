@@ -87,6 +87,7 @@ def lib():
         "llar_layout": (c_int, [c_int, c_int, c_int, c_size, ctypes.POINTER(c_size),
                                 ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
+        "llar_select_protocol_host": (c_int, [c_int, c_int, c_size]),
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
@@ -338,6 +339,11 @@ def llar_layout(protocol, dtype, nranks, count):
 
 def llar_select_protocol(nranks, dtype, count):
     return PROTOCOL_NAMES[lib().llar_select_protocol(int(nranks), _enum(DTYPES, dtype), int(count))]
+
+
+def llar_select_protocol_host(nranks, dtype, count):
+    """AUTO's choice for llar_allreduce_host on pinned, device-addressable buffers."""
+    return PROTOCOL_NAMES[lib().llar_select_protocol_host(int(nranks), _enum(DTYPES, dtype), int(count))]
 
 
 def llar_epoch():
