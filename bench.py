@@ -407,7 +407,7 @@ def configs_leg(llar, torch, dev, stream):
         "fixed_twoshot_8ranks_bf16_us": {f"{kb}KiB": timed(8, "bf16", kb * 512, "fixed_twoshot",
                                                            200 if kb > 64 else 1000)
                                          for kb in (4, 16, 64, 256, 1024)},
-        "C4_sentinel_8ranks_64KiB_fp16_8KiB_chunks_us": timed(8, "fp16", 32768, "sentinel", 1000, chunk=8192),
+        C4_KEY: timed(8, "fp16", 32768, "sentinel", 1000, chunk=8192),
         "C5_chain_160_layers_128KiB_bf16_us": {
             f"N{n}": {p: timed(n, "bf16", 65536, p, 160, chain=0.5, chunk=16384)
                       for p in ("ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot")}
@@ -734,11 +734,27 @@ def poll_counts_subprocess():
     return json.loads(r.stdout.strip().splitlines()[-1])["poll_counts"]
 
 
-def per_config_roofline(per_config, sol_us, hbm_gbs):
+C4_KEY = "C4_sentinel_8ranks_64KiB_fp16_8KiB_chunks_us"
+C4_CHUNKS = 8  # 64 KiB in 8 KiB chunks
+
+
+def chunked_floor_us(chunks, l2_us, write_us):
+    """Latency floor of an AllReduce carried in `chunks` dependent steps:
+    by the credit rule chunk t + 1 leaves only after chunk t has arrived
+    from every peer, and each step needs a publication to become visible
+    (one write) and a poll that sees it (one L2 round trip); the first
+    input read adds one more round trip. With one chunk this is the speed
+    of light, 2 x L2 round trip + one write."""
+    return l2_us + chunks * (write_us + l2_us)
+
+
+def per_config_roofline(per_config, sol_us, hbm_gbs, l2_us=None, write_us=None):
     """Each row against its roofline: latency rows (microseconds per
     operation) as speed of light / time, with the speed of light measured in
     this run (2 x L2 round trip + one write: a per-operation floor whatever
-    the size); bandwidth rows as GB/s / the measured HBM copy bandwidth."""
+    the size); bandwidth rows as GB/s / the measured HBM copy bandwidth.
+    The chunked sentinel row is also given against the floor of its
+    dependent chunk steps (chunked_floor_us)."""
     def lat(v):
         if isinstance(v, dict):
             return {k: lat(x) for k, x in v.items()}
@@ -755,6 +771,13 @@ def per_config_roofline(per_config, sol_us, hbm_gbs):
             out[key] = {k: round(v["GB/s"] / hbm_gbs, 4) for k, v in val.items()}
         elif key.startswith("fused_linear"):
             out[key] = {k: v["fused_frac_of_measured_hbm"] for k, v in val.items()}
+    c4 = per_config.get(C4_KEY)
+    if l2_us is not None and write_us is not None and isinstance(c4, (int, float)) and c4 > 0:
+        floor = chunked_floor_us(C4_CHUNKS, l2_us, write_us)
+        out["C4_chunked_floor"] = {
+            "floor_us": round(floor, 4), "frac": round(floor / c4, 4), "chunks": C4_CHUNKS,
+            "definition": "L2 round trip + chunks x (one write + one L2 round trip): the chunks are "
+                          "dependent steps (chunk t + 1 leaves after chunk t arrived from every peer)"}
     return out
 
 
@@ -890,7 +913,7 @@ def run_ours(args, world, rank, local, pg):
     res["config"] = config
     if per_config is not None:
         res["per_config"] = per_config
-        res["per_config_roofline"] = per_config_roofline(per_config, sol_us, hbm_peak)
+        res["per_config_roofline"] = per_config_roofline(per_config, sol_us, hbm_peak, l2_us, write_us)
     return res
 
 

@@ -97,3 +97,16 @@ def test_all_core_oracle_gives_the_same_bits():
         assert us > 0 and n >= 1 and used == parts
         assert np.array_equal(out, orc.allreduce(xb, "bf16")), parts
     assert bench.time_oracle_all_cores(0.02, count=64, nranks=2)[2] == bench.host_cores()
+
+
+def test_chunked_floor_reduces_to_the_speed_of_light():
+    # one chunk: 2 x L2 round trip + one write, the pages' speed of light
+    assert abs(bench.chunked_floor_us(1, 0.306, 0.792) - 1.404) < 1e-12
+    # the chunked sentinel row gets its own floor beside the per-operation one
+    per = {bench.C4_KEY: 8.0, "C1_2ranks_128B_fp32_us": {"ll": 0.5}}
+    out = bench.per_config_roofline(per, 0.6, 6000.0, 0.15, 0.3)
+    floor = 0.15 + 8 * (0.3 + 0.15)
+    assert abs(out["C4_chunked_floor"]["floor_us"] - floor) < 1e-4
+    assert abs(out["C4_chunked_floor"]["frac"] - floor / 8.0) < 1e-4
+    assert out[bench.C4_KEY] == round(0.6 / 8.0, 4)
+    assert "C4_chunked_floor" not in bench.per_config_roofline(per, 0.6, 6000.0)
