@@ -99,8 +99,15 @@ typedef enum {
  * (llar_dtype_t), messages up to `max_bytes` per rank. Allocates and
  * initialises all staging (LL lines zeroed, sentinel slots filled with the
  * all-ones -NaN pattern, LL128 lines zeroed), the epoch counter and the
- * status word. Returns LLAR_ERR_INVALID for a second init without
- * llar_destroy, LLAR_ERR_CUDA if no device or memory is available. */
+ * status word, and chooses the LL placement (llar_ll_placement). Tuning
+ * variables of the environment (LLAR_CTAS_PER_RANK, LLAR_THREADS,
+ * LLAR_CLUSTER, LLAR_BULK, LLAR_BULK_MIN_BYTES, LLAR_PDL, LLAR_SPREAD_SMEM,
+ * LLAR_CHUNK_BYTES, LLAR_LL_MAX_BYTES, LLAR_LL128_MAX_BYTES, LLAR_LOG,
+ * LLAR_TUNE) are read
+ * here: each context sees the environment as it is at its init, an unset
+ * variable meaning the built-in default. Returns LLAR_ERR_INVALID for a
+ * second init without llar_destroy, LLAR_ERR_CUDA if no device or memory
+ * is available. */
 int llar_init(int nranks, int dtype, size_t max_bytes);
 
 /* Free everything llar_init allocated. Synchronises the device first. */
@@ -257,8 +264,9 @@ int llar_sol_probe_placed(double* l2_rt_us, double* write_us, double* sol_us, in
  * 0 if not. llar_init times both on this GPU (a few hundred 16 KiB
  * AllReduces each, a few milliseconds) and keeps clusters only if they are
  * at least 3 % faster: which placement is faster differs between GPUs of
- * the same model. LLAR_TUNE=0 skips the timing (no clusters); LLAR_CLUSTER
- * = 0 or 2 forces it. Results are identical either way. */
+ * the same model. LLAR_TUNE=0, or a fault injection (llar_debug_inject)
+ * active at llar_init, skips the timing (no clusters); LLAR_CLUSTER = 0 or
+ * 2 forces it. Results are identical either way. */
 int llar_ll_placement(int* clustered);
 
 /* The speed-of-light bound itself (host only): 2 * l2_rt_us + write_us. */

@@ -603,7 +603,8 @@ int fill_staging(Ctx& c, cudaStream_t s) {
 // way (the sums are fixed-order); only the timing differs.
 static void calibrate_ll(Ctx& c) {
   c.ll_cluster = 0;
-  if (env_size("LLAR_TUNE", 1) == 0 || g_cluster != 1) return;
+  // injected faults would time the injection (or wait out its timeouts)
+  if (env_size("LLAR_TUNE", 1) == 0 || g_cluster != 1 || g_inject_mode != LLAR_INJECT_NONE) return;
   const size_t bytes = std::min<size_t>(std::min(c.max_bytes, c.ll_cap), 16u << 10) / 16 * 16;
   const size_t count = bytes / c.esize;
   if (count == 0) return;
@@ -674,14 +675,16 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
                            std::min(kMaxLL128Cap, round_up(env_size("LLAR_LL128_MAX_BYTES", kDefaultLL128Cap), 16)));
   c->chunk_bytes = round_up(std::min(env_size("LLAR_CHUNK_BYTES", kDefaultChunk), kMaxChunk), 16);
   g_timeout_ns = env_size("LLAR_TIMEOUT_NS", g_timeout_ns);
-  g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", (size_t)g_force_G);
-  g_force_T = (int)env_size("LLAR_THREADS", (size_t)g_force_T);
-  g_cluster = (int)env_size("LLAR_CLUSTER", (size_t)g_cluster);
-  g_log = (int)env_size("LLAR_LOG", (size_t)g_log);
-  g_bulk = (int)env_size("LLAR_BULK", (size_t)g_bulk);
-  g_pdl = (int)env_size("LLAR_PDL", (size_t)g_pdl);
-  g_bulk_min_bytes = env_size("LLAR_BULK_MIN_BYTES", g_bulk_min_bytes);
-  g_spread = (int)env_size("LLAR_SPREAD_SMEM", (size_t)g_spread);
+  // tuning knobs: each context takes the environment as it is at its
+  // llar_init (an unset variable means the built-in default)
+  g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", 0);
+  g_force_T = (int)env_size("LLAR_THREADS", 0);
+  g_cluster = (int)env_size("LLAR_CLUSTER", 1);
+  g_log = (int)env_size("LLAR_LOG", 0);
+  g_bulk = (int)env_size("LLAR_BULK", 1);
+  g_pdl = (int)env_size("LLAR_PDL", 1);
+  g_bulk_min_bytes = env_size("LLAR_BULK_MIN_BYTES", 0);
+  g_spread = (int)env_size("LLAR_SPREAD_SMEM", 0);
 
   cudaError_t err = cudaGetDevice(&c->dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->dev);
