@@ -940,14 +940,23 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+_START = None  # a worker process's start barrier
+
+
+def _oracle_worker_init(barrier):
+    global _START
+    _START = barrier
+
+
 def _oracle_slice_worker(job):
     """One worker process of the all-core CPU baseline: the oracle's
-    AllReduce on one element slice, repeated from a common start time for
-    `seconds`; returns (AllReduces done, seconds taken, the slice's result)."""
-    xs, start_at, seconds = job
+    AllReduce on one element slice, repeated for `seconds` once every
+    worker is ready; returns (AllReduces done, seconds taken, the slice's
+    result)."""
+    xs, seconds = job
     from oracle import allreduce as orc
     y = orc.allreduce(xs, DTYPE)
-    time.sleep(max(0.0, start_at - time.time()))
+    _START.wait(timeout=300)  # a worker that never arrives breaks the barrier: an error, not a hang
     n, t0 = 0, time.perf_counter()
     while True:
         y = orc.allreduce(xs, DTYPE)
@@ -959,8 +968,8 @@ def _oracle_slice_worker(job):
 
 def time_oracle_all_cores(seconds, count=COUNT, nranks=NRANKS, parts=None):
     """The same AllReduces, element-partitioned over every host core the
-    process may use: one spawned worker process per slice, all running at
-    once from a common start (threads would take turns on the interpreter
+    process may use: one spawned worker process per slice, all starting
+    together at a barrier (threads would take turns on the interpreter
     lock, which numpy holds between its small calls). The arithmetic per
     element is the oracle's, so the joined slices are its bits. An
     AllReduce is done when every slice is, so its time is the slowest
@@ -975,10 +984,12 @@ def time_oracle_all_cores(seconds, count=COUNT, nranks=NRANKS, parts=None):
     parts = parts or host_cores()
     xb = inputs.bits_of(inputs.normal(nranks, count, DTYPE, seed=1, scale=0.02))
     bounds = [count * i // parts for i in range(parts + 1)]
-    # a worker that fails to start raises here (BrokenProcessPool), it does not hang
-    with ProcessPoolExecutor(parts, mp_context=multiprocessing.get_context("spawn")) as pool:
-        start_at = time.time() + 1.0 + 0.1 * parts  # every worker started and warm
-        jobs = [(xb[:, bounds[i]:bounds[i + 1]].copy(), start_at, seconds) for i in range(parts)]
+    ctx = multiprocessing.get_context("spawn")
+    # each worker blocks at the barrier with its task, so every task lands on
+    # its own worker; a worker that fails to start raises (BrokenProcessPool)
+    with ProcessPoolExecutor(parts, mp_context=ctx, initializer=_oracle_worker_init,
+                             initargs=(ctx.Barrier(parts),)) as pool:
+        jobs = [(xb[:, bounds[i]:bounds[i + 1]].copy(), seconds) for i in range(parts)]
         res = list(pool.map(_oracle_slice_worker, jobs))
     us = max(el / n for n, el, _ in res) * 1e6
     out = np.concatenate([y for _, _, y in res], axis=1)
