@@ -15,8 +15,9 @@
 // Epochs. An exchange is named by a 64-bit epoch E that every rank agrees
 // on. llb::begin() returns the first epoch of a launch (the descriptor's
 // device counter + 1, so a launch replayed from a CUDA graph still gets
-// fresh epochs); a launch that used `n` epochs calls llb::end(b, n) in every
-// thread of every CTA as its last step.
+// fresh epochs); a launch that used `n` epochs calls llb::end(b, n, E) in
+// every thread of every CTA as its last step, E being what begin() returned
+// (llb::end(b, n) does the same but reads the counter once more).
 //
 // Waits. Every wait is bounded by b.timeout_ns. A wait that runs out
 // records the rank and epoch (llar_llbuffer_get_status on the host), raises
@@ -210,6 +211,20 @@ __device__ __forceinline__ void end(const llar_llbuffer& b, unsigned n) {
       *reinterpret_cast<volatile unsigned*>(b.done_count) = 0u;
       volatile u64* ep = b.epoch;
       *ep = *ep + (u64)n;
+    }
+  }
+}
+// The same with `first`, the value begin() returned: the counter every CTA
+// read is first - 1 and nobody has written it since, so the last CTA
+// writes first - 1 + n without reading it again (one round trip less at
+// the end of the launch).
+__device__ __forceinline__ void end(const llar_llbuffer& b, unsigned n, u64 first) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    if (atomicAdd(b.done_count, 1u) == total - 1) {
+      *reinterpret_cast<volatile unsigned*>(b.done_count) = 0u;
+      *reinterpret_cast<volatile u64*>(b.epoch) = first - 1 + (u64)n;
     }
   }
 }

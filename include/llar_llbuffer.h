@@ -109,7 +109,8 @@ int llar_llbuffer_reset(llar_llbuffer* b, void* stream);
 int llar_llbuffer_set_timeout_ns(llar_llbuffer* b, unsigned long long ns);
 
 /* Exchanges completed so far: the device epoch counter (every launch of a
- * kernel that called llb::end(b, n) added n). Synchronises the device. */
+ * kernel that called llb::end(b, n[, E]) added n). Synchronises the
+ * device. */
 int llar_llbuffer_epoch(const llar_llbuffer* b, unsigned long long* epoch);
 
 /* Diagnostic: one thread of one CTA waits (llb::ll_wait) as rank `rank`

@@ -106,17 +106,23 @@ __device__ __forceinline__ u64 launch_epoch(const Params& p) {
 // consumes, in its last iteration, data that every CTA of column c produced
 // after reading the counter may count rank 0's CTAs alone (G atomics on
 // the counter word instead of N x G).
-__device__ __forceinline__ void finish_launch(const Params& p, bool counted, unsigned participants) {
+// `epoch0` is what launch_epoch returned: the counter every CTA read is
+// epoch0 - 1, and only the last CTA to count writes it, so the new value
+// needs no second read of the counter (a round trip at the end of every
+// launch: 8 x 16 KiB bf16 LL, one AllReduce per launch replayed from a
+// graph, 2.79 -> 2.46 us per launch).
+__device__ __forceinline__ void finish_launch(const Params& p, u64 epoch0, bool counted, unsigned participants) {
   __syncthreads();
   if (threadIdx.x == 0 && counted) {
     if (atomicAdd(p.done_count, 1u) == participants - 1) {
       *reinterpret_cast<volatile unsigned*>(p.done_count) = 0u;
-      volatile u64* ep = p.epoch_dev;
-      *ep = *ep + (u64)p.iters;
+      *reinterpret_cast<volatile u64*>(p.epoch_dev) = epoch0 - 1 + (u64)p.iters;
     }
   }
 }
-__device__ __forceinline__ void finish_launch(const Params& p) { finish_launch(p, true, gridDim.x); }
+__device__ __forceinline__ void finish_launch(const Params& p, u64 epoch0) {
+  finish_launch(p, epoch0, true, gridDim.x);
+}
 
 // One thread per unit (an 8-byte LL word or a 16-byte sentinel vector):
 // the thread sends its unit of my data (LL: publishes it once in my own
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll(const Params p) {
   // every thread of rank 0's CTA c read, in the last iteration, a line that
   // the same thread of each peer CTA c published after reading the counter
   // (peer threads without words do nothing with it)
-  finish_launch(p, r == 0, (unsigned)p.G);
+  finish_launch(p, E0, r == 0, (unsigned)p.G);
 }
 
 // ====================================================== sentinel one-shot
@@ -683,7 +689,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_sentinel(const Params p) {
   body_sentinel<DT, N, CHAIN, INJ>(p, epoch0);
   // rank 0's thread j took, in the last chunk it handled, the vector that
   // thread j of each peer CTA pushed after reading the counter
-  finish_launch(p, rank_of_block(p) == 0, (unsigned)p.G);
+  finish_launch(p, epoch0, rank_of_block(p) == 0, (unsigned)p.G);
 }
 
 // ======================================================= LL128 two-shot
@@ -1158,10 +1164,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128d(const Params p) {
   if (threadIdx.x == 0 && rank_of_block(p) == 0) {
     if (atomicAdd(p.done_count, 1u) == (unsigned)p.G - 1) {
       *reinterpret_cast<volatile unsigned*>(p.done_count) = 0u;
-      volatile u64* ep = p.epoch_dev;
-      *ep = *ep + (u64)p.iters;
+      *reinterpret_cast<volatile u64*>(p.epoch_dev) = epoch0 - 1 + (u64)p.iters;
       volatile u64* sp = p.l128d_seq;
-      *sp = *sp + (u64)p.iters;
+      *sp = seq0 + (u64)p.iters;
       // the lines of every segment this launch used (the same in every AllReduce)
       const size_t seg = (p.count + p.nranks - 1) / p.nranks;
       sp[1] = (u64)((seg + (128 / Fmt<DT>::kBytes - 1) - 1) / (128 / Fmt<DT>::kBytes - 1));
@@ -1177,7 +1182,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_ll128(const Params p) {
   // every other owner's AllGather lines of its range, which each owner sent
   // only after all contributions to them: every working thread of column c
   // had read the counter
-  finish_launch(p, rank_of_block(p) == 0, (unsigned)p.G);
+  finish_launch(p, epoch0, rank_of_block(p) == 0, (unsigned)p.G);
 }
 
 // ==================================================== fixed-order paths
@@ -1330,7 +1335,7 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_fixed_oneshot(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_fixed_oneshot<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 
 // Two-shot: rank s owns vectors [s*ceil(NV/N), ...) of the message; CTA c
@@ -1376,7 +1381,7 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_fixed_twoshot<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 
 // Large two-shot without a chain: the owner's CTAs stream their sub-range
@@ -1501,7 +1506,7 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_fixed_twoshot_bulk(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_fixed_twoshot_bulk<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 
 // ============================================ ReduceScatter / AllGather
@@ -1918,44 +1923,44 @@ template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_rs_ll128(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_rs_ll128<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_rs_sentinel(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_rs_sentinel<DT, N>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_ag_sentinel(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_ag_sentinel<DT, N>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 
 template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_rs_ll(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_rs_ll<DT, N>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 template <int DT, int N>
 __global__ void __launch_bounds__(kMaxThreads) k_ag_ll(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_ag_ll<DT, N>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_rs_fixed(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_rs_fixed<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_ag_fixed(const Params p) {
   const u64 epoch0 = launch_epoch(p);
   body_ag_fixed<DT>(p, epoch0);
-  finish_launch(p);
+  finish_launch(p, epoch0);
 }
 
 // ========================================================= point to point
@@ -2050,7 +2055,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
       if (ok && !silent) unacked = E;
     }
   }
-  finish_launch(p);
+  finish_launch(p, E0);
 }
 
 // Sentinel: the sender pushes raw 16-byte vectors into the receiver's slot
@@ -2122,7 +2127,7 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_sentinel(const Params p) {
       }
     }
   }
-  finish_launch(p);
+  finish_launch(p, E0);
 }
 
 // ============================================================ launchers

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(512) kb_ll(const llar_llbuffer b, const Ptrs i
       store_word(io.out[r], w, nbytes, llb::sum_words<T, N>(d));
     }
   }
-  llb::end(b, (unsigned)iters);
+  llb::end(b, (unsigned)iters, E0);
 }
 
 // ====================================================== sentinel one-shot
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(512) kb_sentinel(const llar_llbuffer b, const 
       store_vec(io.out[r], v, nbytes, make_uint4(y[0], y[1], y[2], y[3]));
     }
   }
-  llb::end(b, (unsigned)iters);
+  llb::end(b, (unsigned)iters, E0);
 }
 
 // ======================================================= LL128 two-shot
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(512) kb_ll128(const llar_llbuffer b, const Ptr
     }
     if (__syncthreads_or(!ok)) break;
   }
-  llb::end(b, (unsigned)iters);
+  llb::end(b, (unsigned)iters, E0);
 }
 
 // ================================================= fused linear + AllReduce
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kLinearThreads, 2) kb_linear(const llar_llbuff
         }
         *reinterpret_cast<u64*>(out + wid * 8) = llb::sum_words_ranks<T>(d, n);
       }
-    llb::end(b, 1u);
+    llb::end(b, 1u, E);
   }
 }
 
@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(32 * kTcWarps, 2) kb_linear_tc(const llar_llbu
           if ((valid >> (8 * u)) & 0xFFu) *reinterpret_cast<u64*>(out + wid[u] * 8) = llb::sum_words_ranks<T>(dd[u], n);
       }
     }
-    llb::end(b, 1u);
+    llb::end(b, 1u, E);
   }
 }
 
