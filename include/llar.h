@@ -259,12 +259,12 @@ int llar_sol_probe(double* l2_rt_us, double* write_us, double* sol_us);
 int llar_sol_probe_placed(double* l2_rt_us, double* write_us, double* sol_us, int* npairs);
 
 /* LL placement chosen for this context (diagnostic; no page describes
- * it): *clustered = 1 if LL launches of 16 or more AllReduces run in
- * clusters of N blocks (the CTAs that exchange a word range on one GPC),
- * 0 if not. llar_init times both on this GPU (a few hundred 16 KiB
- * AllReduces each, a few milliseconds) and keeps clusters only if they are
- * at least 3 % faster: which placement is faster differs between GPUs of
- * the same model. LLAR_TUNE=0, or a fault injection (llar_debug_inject)
+ * it): *clustered = 1 if LL launches of 16 or more AllReduces of up to
+ * 16 KiB per rank (the size timed) run in clusters of N blocks (the CTAs
+ * that exchange a word range on one GPC), 0 if not. llar_init times both
+ * on this GPU (a few hundred 16 KiB AllReduces each, a few milliseconds)
+ * and keeps clusters only if they are at least 3 % faster: which placement
+ * is faster differs between GPUs of the same model. LLAR_TUNE=0, or a fault injection (llar_debug_inject)
  * active at llar_init, skips the timing (no clusters); LLAR_CLUSTER = 0 or
  * 2 forces it. Results are identical either way. */
 int llar_ll_placement(int* clustered);

@@ -67,7 +67,8 @@ struct Ctx {
   std::map<long long, int> capacity;
   // LL launches of many AllReduces in clusters of N blocks (chosen by
   // calibrate_ll on this GPU)
-  int ll_cluster = 0;
+  int ll_cluster = 0;       // LL launches of many AllReduces up to ll_cal_bytes run in clusters
+  size_t ll_cal_bytes = 0;  // bytes per rank the placement was timed at
 };
 
 std::mutex g_mu;
@@ -512,7 +513,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   // LLAR_CLUSTER: 0 never, 1 per protocol (default), 2 always.
   const bool cluster_helps = proto == LLAR_PROTO_SENTINEL || proto == LLAR_PROTO_FIXED_ONESHOT ||
                              proto == LLAR_PROTO_FIXED_TWOSHOT ||
-                             (proto == LLAR_PROTO_LL && c.ll_cluster && iters >= kLLTuneMinIters);
+                             (proto == LLAR_PROTO_LL && c.ll_cluster && iters >= kLLTuneMinIters &&
+                              count * e <= c.ll_cal_bytes);
   p.clustered = (coop && (g_cluster == 2 || (g_cluster == 1 && cluster_helps))) ? 1 : 0;
   p.spread_smem = (coop && (proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL)) ? g_spread : 0;
   if (coop) {
@@ -598,7 +600,10 @@ int fill_staging(Ctx& c, cudaStream_t s) {
 // with clusters 0.72-0.73 on both (dependent chains 0.81 / 0.97 against
 // 0.93). llar_init times both here, on this GPU (300 AllReduces of up to
 // 16 KiB per rank, twice each), and keeps clusters for LL launches of
-// many AllReduces if they are at least 3 % faster. LLAR_TUNE=0 skips it;
+// many AllReduces no larger than that if they are at least 3 % faster
+// (larger messages stay unclustered: 4 ranks x 128 KiB bf16 chained took
+// 1.60 us per AllReduce in clusters against 1.21 without, on a GPU where
+// 16 KiB ran faster in them). LLAR_TUNE=0 skips it;
 // LLAR_CLUSTER (0 or 2) forces either way. Results are identical either
 // way (the sums are fixed-order); only the timing differs.
 static void calibrate_ll(Ctx& c) {
@@ -608,6 +613,7 @@ static void calibrate_ll(Ctx& c) {
   const size_t bytes = std::min<size_t>(std::min(c.max_bytes, c.ll_cap), 16u << 10) / 16 * 16;
   const size_t count = bytes / c.esize;
   if (count == 0) return;
+  c.ll_cal_bytes = bytes;
   char* buf = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (cudaMalloc(&buf, 2 * (size_t)c.n * bytes) != cudaSuccess || cudaMemset(buf, 0, 2 * (size_t)c.n * bytes) != cudaSuccess ||
