@@ -144,8 +144,8 @@ int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
  * (direct reads), LLAR_PROTO_LL128_ATOMIC (technique 4's atomic
  * reductions into 128-byte lines with a count flag: element-type
  * additions in arrival order, within (N-1) ulp of the sum of |x|) or
- * LLAR_PROTO_AUTO; others give LLAR_ERR_UNSUPPORTED. One collective per
- * launch. */
+ * LLAR_PROTO_AUTO (llar_select_protocol_segment); others give
+ * LLAR_ERR_UNSUPPORTED. One collective per launch. */
 int llar_reduce_scatter(const void* const* in, void* const* out, size_t count,
                         int protocol, void* stream);
 
@@ -300,6 +300,15 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
  * with TMA bulk copies from 1 MiB (3-4), 512 KiB (5) or 32 KiB (6-8), and
  * never for 2 ranks. LLAR_PROTO (environment) forces a protocol. */
 int llar_select_protocol(int nranks, int dtype, size_t count);
+
+/* The protocol LLAR_PROTO_AUTO picks for llar_reduce_scatter
+ * (reduce_scatter != 0) or llar_all_gather of `count` elements (host-only).
+ * Measured per rank count on a B300 (one call per launch): the direct-read
+ * ReduceScatter at every size (8 x 16 KiB bf16: 2.3 us against 4.1 for
+ * LL); for AllGather LL up to 64 KiB per rank with 7-8 ranks, the direct
+ * reads otherwise. LLAR_PROTO (environment) forces a protocol.
+ * LLAR_PROTO_AUTO for an invalid rank count or dtype. */
+int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count);
 
 /* The protocol LLAR_PROTO_AUTO picks when llar_allreduce_host reads and
  * writes host memory directly (host-only). (No page describes it.) The

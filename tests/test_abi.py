@@ -98,6 +98,19 @@ def test_host_memory_protocol_selection():
     assert llar.lib().llar_select_protocol_host(8, 7, 8192) == llar.PROTOCOLS["auto"]  # no such dtype
 
 
+def test_segment_protocol_selection():
+    # ReduceScatter: direct reads at every size; AllGather: LL up to 64 KiB
+    # per rank with 7-8 ranks, direct reads otherwise (rule in bytes)
+    for n in range(2, 9):
+        for kib in (1, 16, 64, 65, 1024):
+            for dtype, e in (("bf16", 2), ("fp32", 4)):
+                count = kib * 1024 // e
+                assert llar.llar_select_protocol_segment(True, n, dtype, count) == "fixed_oneshot"
+                want = "ll" if n >= 7 and kib <= 64 else "fixed_oneshot"
+                assert llar.llar_select_protocol_segment(False, n, dtype, count) == want, (n, kib, dtype)
+    assert llar.llar_select_protocol_segment(True, 9, "bf16", 8) == "auto"
+
+
 def test_argument_checks_without_device():
     with pytest.raises(llar.LlarError) as ei:
         llar.llar_init(1, "bf16", 1024)

@@ -101,6 +101,27 @@ def test_all_gather(proto, dtype, n):
             assert np.array_equal(got, want), count
 
 
+@pytest.mark.parametrize("n", [2, 7, 8])
+def test_auto_follows_the_segment_rule(n):
+    # AUTO takes llar_select_protocol_segment's choice (direct reads for the
+    # ReduceScatter; LL for small AllGathers of 7-8 ranks) and the oracle's bits
+    dtype = "bf16"
+    with context(n, dtype, 1 << 20):
+        for count in (512, 32768, 32768 + 8 * 7):  # 1 KiB, 64 KiB, just above 64 KiB per rank
+            x = inputs.normal(n, count, dtype, seed=count + n, scale=0.02)
+            ins = device_inputs(x)
+            mid = filled_outputs(n, _seg_len(count, n), dtype)
+            outs = filled_outputs(n, count, dtype)
+            llar.llar_reduce_scatter(ins, mid, count, "auto")
+            assert llar.llar_last_launch()[0] == llar.llar_select_protocol_segment(True, n, dtype, count)
+            llar.llar_all_gather(mid, outs, count, "auto")
+            assert llar.llar_last_launch()[0] == llar.llar_select_protocol_segment(False, n, dtype, count)
+            torch.cuda.synchronize()
+            assert llar.llar_get_status()[0] == llar.OK
+            got = np.stack([inputs.bits_of(o) for o in outs])
+            assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype)), count
+
+
 @pytest.mark.parametrize("rs,ag", [("ll", "ll"), ("fixed_oneshot", "fixed_oneshot"), ("sentinel", "sentinel"),
                                    ("ll128", "ll"), ("sentinel", "ll"), ("ll", "sentinel")])
 def test_all_gather_of_reduce_scatter_is_allreduce(rs, ag):

@@ -307,6 +307,18 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
   p.pdl = g_pdl;
 }
 
+// AUTO for the standalone halves. Measured on a B300 (bf16, one call per
+// launch replayed from a graph, 2..8 ranks, 1 KiB .. 1 MiB per rank):
+// the direct-read ReduceScatter is the fastest at every point (8 x 16 KiB:
+// 2.3 us against 4.1 for LL and 3.8 for LL128); for AllGather LL is faster
+// up to 64 KiB with 7 or 8 ranks (8 x 16 KiB: 2.8 against 3.4 us), the
+// direct reads everywhere else (4 x 16 KiB: 2.2 against 2.8).
+int select_segment_protocol(bool rs, int n, size_t bytes) {
+  if (const int f = forced_protocol()) return f;
+  if (!rs && n >= 7 && bytes <= (64u << 10)) return LLAR_PROTO_LL;
+  return LLAR_PROTO_FIXED_ONESHOT;
+}
+
 // ReduceScatter (rs) or AllGather over segments of a count-element vector.
 int run_segment(bool rs, const void* const* in, void* const* out, size_t count, int proto, cudaStream_t stream) {
   if (!g) return LLAR_ERR_NOT_INIT;
@@ -314,7 +326,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   const size_t e = c.esize;
   const size_t bytes = count * e;
   const size_t seg_bytes = (count + c.n - 1) / c.n * e;
-  if (proto == LLAR_PROTO_AUTO) proto = bytes <= (64u << 10) ? LLAR_PROTO_LL : LLAR_PROTO_FIXED_ONESHOT;
+  if (proto == LLAR_PROTO_AUTO) proto = select_segment_protocol(rs, c.n, bytes);
   // AllGather adds nothing, so the atomic LL128 protocol has no AllGather
   // of its own (its second half is LL)
   const bool ok_proto = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_FIXED_ONESHOT ||
@@ -1088,6 +1100,11 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
 int llar_select_protocol(int nranks, int dtype, size_t count) {
   if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
   return select_protocol(nranks, dtype, count);
+}
+
+int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count) {
+  if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
+  return select_segment_protocol(reduce_scatter != 0, nranks, count * elem_bytes(dtype));
 }
 
 int llar_select_protocol_host(int nranks, int dtype, size_t count) {

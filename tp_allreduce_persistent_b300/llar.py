@@ -88,6 +88,7 @@ def lib():
                                 ctypes.POINTER(c_size), ctypes.POINTER(c_size)]),
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
         "llar_select_protocol_host": (c_int, [c_int, c_int, c_size]),
+        "llar_select_protocol_segment": (c_int, [c_int, c_int, c_int, c_size]),
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
@@ -339,6 +340,12 @@ def llar_layout(protocol, dtype, nranks, count):
 
 def llar_select_protocol(nranks, dtype, count):
     return PROTOCOL_NAMES[lib().llar_select_protocol(int(nranks), _enum(DTYPES, dtype), int(count))]
+
+
+def llar_select_protocol_segment(reduce_scatter, nranks, dtype, count):
+    """AUTO's choice for llar_reduce_scatter (True) or llar_all_gather (False)."""
+    return PROTOCOL_NAMES[lib().llar_select_protocol_segment(int(bool(reduce_scatter)), int(nranks),
+                                                             _enum(DTYPES, dtype), int(count))]
 
 
 def llar_select_protocol_host(nranks, dtype, count):
