@@ -410,7 +410,11 @@ int run_p2p(const void* const* send, void* const* recv, const int* dst, size_t c
       src[d] = r;
     }
   }
-  if (proto == LLAR_PROTO_AUTO) proto = bytes <= (64u << 10) ? LLAR_PROTO_LL : LLAR_PROTO_SENTINEL;
+  // AUTO: LL wherever it fits. Measured on a B300 (bf16 ring, one call per
+  // launch replayed from a graph / 100 per launch): LL is ahead at every
+  // size up to its capacity, by 0.1-0.7 us up to 64 KiB and by far above
+  // (2 ranks x 1 MiB: 4.2 against 29.7 us; 8 x 256 KiB: 4.5 against 9.2)
+  if (proto == LLAR_PROTO_AUTO) proto = bytes <= c.ll_cap ? LLAR_PROTO_LL : LLAR_PROTO_SENTINEL;
   if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_SENTINEL) return LLAR_ERR_UNSUPPORTED;
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
