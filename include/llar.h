@@ -127,7 +127,8 @@ int llar_allreduce(const void* const* in, void* const* out, size_t count,
  * when chain_scale != 0 (a chain of dependent AllReduces, as across the
  * layers of one decode step), in[r] for e == 0 and afterwards
  * roundTiesToEven(chain_scale * output of e-1), kept in library memory.
- * The output of iteration e is identical to llar_allreduce on that input. */
+ * The output of iteration e is identical to llar_allreduce on that input.
+ * LLAR_PROTO_AUTO follows llar_select_protocol_iters. */
 int llar_allreduce_iters(const void* const* in, void* const* out, size_t count,
                          int protocol, int iters, size_t in_stride_elems,
                          size_t out_stride_elems, float chain_scale, void* stream);
@@ -300,6 +301,18 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
  * with TMA bulk copies from 1 MiB (3-4), 512 KiB (5) or 32 KiB (6-8), and
  * never for 2 ranks. LLAR_PROTO (environment) forces a protocol. */
 int llar_select_protocol(int nranks, int dtype, size_t count);
+
+/* The protocol LLAR_PROTO_AUTO picks for llar_allreduce_iters (host-only;
+ * with the default 1 MiB LL capacity, the context's own in a call). With
+ * iters == 1, llar_select_protocol. A chain (`chained` != 0) takes LL up to
+ * the LL capacity, with 6-8 ranks up to 512 KiB per rank, and the
+ * direct-read two-shot beyond (8 x 64 KiB bf16 chained: LL 1.34 us per
+ * AllReduce against 14.9 for the two-shot); independent AllReduces take
+ * llar_select_protocol's choice, except LL up to 64 KiB with 6-8 ranks.
+ * Deterministic protocols only: the LL128 forms, faster in 8-rank chains
+ * from 256 KiB, are the caller's choice. LLAR_PROTO (environment) forces a
+ * protocol. LLAR_PROTO_AUTO for invalid arguments. */
+int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained);
 
 /* The protocol LLAR_PROTO_AUTO picks for llar_reduce_scatter
  * (reduce_scatter != 0) or llar_all_gather of `count` elements (host-only).

@@ -98,6 +98,31 @@ def test_host_memory_protocol_selection():
     assert llar.lib().llar_select_protocol_host(8, 7, 8192) == llar.PROTOCOLS["auto"]  # no such dtype
 
 
+def test_persistent_protocol_selection():
+    # one AllReduce per launch: the single-call rule
+    for n in range(2, 9):
+        for kib in (4, 64, 512, 1024):
+            count = kib * 512
+            assert llar.llar_select_protocol_iters(n, "bf16", count, 1) == llar.llar_select_protocol(n, "bf16", count)
+    # chains: LL up to the 1 MiB LL capacity (6-8 ranks: up to 512 KiB), then the two-shot
+    for n in range(2, 9):
+        for kib in (1, 64, 256, 512, 513, 1024, 1025, 4096):
+            count = kib * 512
+            ll = kib <= 1024 and (n <= 5 or kib <= 512)
+            want = "ll" if ll else "fixed_twoshot"
+            assert llar.llar_select_protocol_iters(n, "bf16", count, 160, True) == want, (n, kib)
+    # independent back to back: LL up to 64 KiB with 6-8 ranks, else the single-call rule
+    for n in range(2, 9):
+        for kib in (16, 33, 64, 65, 256):
+            count = kib * 512
+            got = llar.llar_select_protocol_iters(n, "bf16", count, 200, False)
+            if n >= 6 and kib <= 64:
+                assert got == "ll", (n, kib)
+            else:
+                assert got == llar.llar_select_protocol(n, "bf16", count), (n, kib)
+    assert llar.llar_select_protocol_iters(8, "bf16", 8192, 0) == "auto"
+
+
 def test_segment_protocol_selection():
     # ReduceScatter: direct reads at every size; AllGather: LL up to 64 KiB
     # per rank with 7-8 ranks, direct reads otherwise (rule in bytes)

@@ -191,3 +191,24 @@ def test_two_shot_tma_path_at_small_sizes(n, dtype):
             assert np.array_equal(got, orc.allreduce(inputs.bits_of(x), dtype)), count
             got_auto = allreduce(x, dtype, "auto")
             assert np.array_equal(got_auto, orc.allreduce(inputs.bits_of(x), dtype)), count
+
+
+@pytest.mark.parametrize("n,kib,chain", [(8, 64, True), (8, 1024, True), (4, 1024, True),
+                                         (8, 64, False), (8, 256, False), (2, 16, True)])
+def test_persistent_auto_follows_its_rule(n, kib, chain):
+    # llar_allreduce_iters with AUTO takes llar_select_protocol_iters' choice
+    # (LL for chains up to the LL capacity, the two-shot for 6-8 ranks from
+    # 1 MiB; LL up to 64 KiB back to back with 6-8 ranks); bits as the oracle
+    dtype, iters = "bf16", 6
+    count = kib * 512
+    with context(n, dtype, 1 << 20):
+        if chain:
+            x = inputs.normal(n, count, dtype, seed=kib + n, scale=0.02)
+            got = allreduce_iters(x, dtype, "auto", iters, chain_scale=1.0 / n)
+            want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=1.0 / n)
+        else:
+            x = inputs.uniform(n, count, dtype, seed=kib + n, iters=iters)
+            got = allreduce_iters(x, dtype, "auto", iters)
+            want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype)
+        assert llar.llar_last_launch()[0] == llar.llar_select_protocol_iters(n, dtype, count, iters, chain)
+        assert np.array_equal(got, want)

@@ -156,6 +156,28 @@ int select_protocol(int n, int dtype, size_t count) {
   return LLAR_PROTO_FIXED_TWOSHOT;
 }
 
+// AUTO for a persistent launch of `iters` > 1 AllReduces. Measured on a
+// B300 (bf16, 2/4/8 ranks, 16 KiB .. 1 MiB per rank, us per AllReduce):
+// * chains (each input = scale x the previous output): LL is the fastest
+//   deterministic path nearly everywhere, by far (8 x 64 KiB: 1.34 against
+//   14.9 for the two-shot, whose chained form pays a flag round per step),
+//   except 6-8 ranks at 1 MiB (two-shot 16.1 against LL 19.5). The LL128
+//   direct form is faster still at 8 ranks from 256 KiB (4.0 against 5.4)
+//   but its atomic sums are not bit-reproducible, so AUTO leaves it to the
+//   caller;
+// * independent AllReduces back to back: the single-call rule, except that
+//   LL stays ahead up to 64 KiB with 6-8 ranks (8 x 64 KiB: 1.22 against
+//   1.67).
+// LL only up to the context's LL capacity (ll_cap).
+int select_protocol_iters(int n, int dtype, size_t count, int iters, bool chain, size_t ll_cap) {
+  if (const int f = forced_protocol()) return f;
+  const size_t bytes = count * elem_bytes(dtype);
+  if (iters > 1 && chain && bytes <= ll_cap && (n <= 5 || bytes <= (512u << 10))) return LLAR_PROTO_LL;
+  if (iters > 1 && chain) return LLAR_PROTO_FIXED_TWOSHOT;
+  if (iters > 1 && n >= 6 && bytes <= std::min<size_t>(ll_cap, 64u << 10)) return LLAR_PROTO_LL;
+  return select_protocol(n, dtype, count);
+}
+
 // AUTO when the inputs and outputs are host memory that the kernel reads
 // and writes across the bus (the host-buffer entry's direct path). The bus
 // sets the cost there, and every path moves the same bytes across it; what
@@ -500,7 +522,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   const size_t bytes = count * e;
   const size_t in_span = (size_t)(iters - 1) * in_stride * e + bytes;
   const size_t out_span = (size_t)(iters - 1) * out_stride * e + bytes;
-  if (proto == LLAR_PROTO_AUTO) proto = select_protocol(c.n, c.dtype, count);
+  if (proto == LLAR_PROTO_AUTO) proto = select_protocol_iters(c.n, c.dtype, count, iters, chain, c.ll_cap);
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
   if (is_ll128(proto) && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
@@ -1104,6 +1126,11 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count, size_t* line_
 int llar_select_protocol(int nranks, int dtype, size_t count) {
   if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
   return select_protocol(nranks, dtype, count);
+}
+
+int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained) {
+  if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks || iters < 1) return LLAR_PROTO_AUTO;
+  return select_protocol_iters(nranks, dtype, count, iters, chained != 0, kDefaultLLCap);
 }
 
 int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count) {

@@ -89,6 +89,7 @@ def lib():
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
         "llar_select_protocol_host": (c_int, [c_int, c_int, c_size]),
         "llar_select_protocol_segment": (c_int, [c_int, c_int, c_int, c_size]),
+        "llar_select_protocol_iters": (c_int, [c_int, c_int, c_size, c_int, c_int]),
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
@@ -340,6 +341,12 @@ def llar_layout(protocol, dtype, nranks, count):
 
 def llar_select_protocol(nranks, dtype, count):
     return PROTOCOL_NAMES[lib().llar_select_protocol(int(nranks), _enum(DTYPES, dtype), int(count))]
+
+
+def llar_select_protocol_iters(nranks, dtype, count, iters, chained=False):
+    """AUTO's choice for llar_allreduce_iters (default LL capacity)."""
+    return PROTOCOL_NAMES[lib().llar_select_protocol_iters(int(nranks), _enum(DTYPES, dtype), int(count),
+                                                           int(iters), int(bool(chained)))]
 
 
 def llar_select_protocol_segment(reduce_scatter, nranks, dtype, count):
