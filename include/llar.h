@@ -305,9 +305,9 @@ int llar_select_protocol(int nranks, int dtype, size_t count);
 /* The protocol LLAR_PROTO_AUTO picks for llar_allreduce_iters (host-only;
  * with the default 1 MiB LL capacity, the context's own in a call). With
  * iters == 1, llar_select_protocol. A chain (`chained` != 0) takes LL up to
- * the LL capacity, with 6-8 ranks up to 512 KiB per rank, and the
- * direct-read two-shot beyond (8 x 64 KiB bf16 chained: LL 1.34 us per
- * AllReduce against 14.9 for the two-shot); independent AllReduces take
+ * the LL capacity, with 7-8 ranks up to 512 KiB per rank, and the
+ * direct-read two-shot beyond (8 x 64 KiB bf16 chained: LL 1.41 us per
+ * AllReduce against 11.7 for the two-shot); independent AllReduces take
  * llar_select_protocol's choice, except LL up to 64 KiB with 6-8 ranks.
  * Deterministic protocols only: the LL128 forms, faster in 8-rank chains
  * from 256 KiB, are the caller's choice. LLAR_PROTO (environment) forces a

@@ -104,11 +104,11 @@ def test_persistent_protocol_selection():
         for kib in (4, 64, 512, 1024):
             count = kib * 512
             assert llar.llar_select_protocol_iters(n, "bf16", count, 1) == llar.llar_select_protocol(n, "bf16", count)
-    # chains: LL up to the 1 MiB LL capacity (6-8 ranks: up to 512 KiB), then the two-shot
+    # chains: LL up to the 1 MiB LL capacity (7-8 ranks: up to 512 KiB), then the two-shot
     for n in range(2, 9):
         for kib in (1, 64, 256, 512, 513, 1024, 1025, 4096):
             count = kib * 512
-            ll = kib <= 1024 and (n <= 5 or kib <= 512)
+            ll = kib <= 1024 and (n <= 6 or kib <= 512)
             want = "ll" if ll else "fixed_twoshot"
             assert llar.llar_select_protocol_iters(n, "bf16", count, 160, True) == want, (n, kib)
     # independent back to back: LL up to 64 KiB with 6-8 ranks, else the single-call rule

@@ -197,8 +197,8 @@ def test_two_shot_tma_path_at_small_sizes(n, dtype):
                                          (8, 64, False), (8, 256, False), (2, 16, True)])
 def test_persistent_auto_follows_its_rule(n, kib, chain):
     # llar_allreduce_iters with AUTO takes llar_select_protocol_iters' choice
-    # (LL for chains up to the LL capacity, the two-shot for 6-8 ranks from
-    # 1 MiB; LL up to 64 KiB back to back with 6-8 ranks); bits as the oracle
+    # (LL for chains up to the LL capacity, the two-shot for 7-8 ranks above
+    # 512 KiB; LL up to 64 KiB back to back with 6-8 ranks); bits as the oracle
     dtype, iters = "bf16", 6
     count = kib * 512
     with context(n, dtype, 1 << 20):

@@ -159,12 +159,12 @@ int select_protocol(int n, int dtype, size_t count) {
 // AUTO for a persistent launch of `iters` > 1 AllReduces. Measured on a
 // B300 (bf16, 2/4/8 ranks, 16 KiB .. 1 MiB per rank, us per AllReduce):
 // * chains (each input = scale x the previous output): LL is the fastest
-//   deterministic path nearly everywhere, by far (8 x 64 KiB: 1.34 against
-//   14.9 for the two-shot, whose chained form pays a flag round per step),
-//   except 6-8 ranks at 1 MiB (two-shot 16.1 against LL 19.5). The LL128
-//   direct form is faster still at 8 ranks from 256 KiB (4.0 against 5.4)
-//   but its atomic sums are not bit-reproducible, so AUTO leaves it to the
-//   caller;
+//   deterministic path nearly everywhere, by far (8 x 64 KiB: 1.41 against
+//   11.7 for the two-shot, whose chained form pays two flag rounds per
+//   step), except 7-8 ranks at 1 MiB (8 ranks: two-shot 13.3 against LL
+//   19.9). The LL128 direct form is faster still at 8 ranks from 256 KiB
+//   (4.2 against 5.6) but its atomic sums are not bit-reproducible, so
+//   AUTO leaves it to the caller;
 // * independent AllReduces back to back: the single-call rule, except that
 //   LL stays ahead up to 64 KiB with 6-8 ranks (8 x 64 KiB: 1.22 against
 //   1.67).
@@ -172,7 +172,7 @@ int select_protocol(int n, int dtype, size_t count) {
 int select_protocol_iters(int n, int dtype, size_t count, int iters, bool chain, size_t ll_cap) {
   if (const int f = forced_protocol()) return f;
   const size_t bytes = count * elem_bytes(dtype);
-  if (iters > 1 && chain && bytes <= ll_cap && (n <= 5 || bytes <= (512u << 10))) return LLAR_PROTO_LL;
+  if (iters > 1 && chain && bytes <= ll_cap && (n <= 6 || bytes <= (512u << 10))) return LLAR_PROTO_LL;
   if (iters > 1 && chain) return LLAR_PROTO_FIXED_TWOSHOT;
   if (iters > 1 && n >= 6 && bytes <= std::min<size_t>(ll_cap, 64u << 10)) return LLAR_PROTO_LL;
   return select_protocol(n, dtype, count);
@@ -723,6 +723,9 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   // llar_init (an unset variable means the built-in default)
   g_force_G = (int)env_size("LLAR_CTAS_PER_RANK", 0);
   g_force_T = (int)env_size("LLAR_THREADS", 0);
+  // the same limits as llar_set_launch: whole warps, at most the kernels' bound
+  if (g_force_G < 0 || g_force_G > kFlagsGmax) g_force_G = 0;
+  if (g_force_T < 0 || g_force_T % 32 || g_force_T > llar::kMaxThreads) g_force_T = 0;
   g_cluster = (int)env_size("LLAR_CLUSTER", 1);
   g_log = (int)env_size("LLAR_LOG", 0);
   g_bulk = (int)env_size("LLAR_BULK", 1);
