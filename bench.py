@@ -304,7 +304,9 @@ def e2e_leg(args, llar, torch, stream, x, pg, local):
     llar.llar_host_register(hx)  # pinned buffers declared once, as a serving loop would
     llar.llar_host_register(hy)
     try:
-        for _ in range(args.warmup):
+        # warm-up steps of E2E_CALLS calls each, as timed (the host's own
+        # submission rate takes a few hundred calls to settle)
+        for _ in range(args.warmup * E2E_CALLS):
             llar.llar_allreduce_host(hx, hy, COUNT, proto)
         torch.cuda.synchronize()
         calls = max(3, args.steps // 5) * E2E_CALLS
