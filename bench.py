@@ -44,6 +44,7 @@ ITERS = 10000              # AllReduces per persistent launch in the latency leg
 BW_COUNT = 32 << 20        # 64 MiB bf16 per rank
 BW_REPS = 10               # AllReduces per step in the bandwidth leg
 E2E_CALLS = 200            # host-buffer calls per step in the end-to-end leg
+E2E_WARMUP_S = 0.5         # seconds of host-buffer calls before the end-to-end leg is timed
 FLUSH_BYTES = 256 << 20    # > 126 MB L2
 FALLBACK_HBM_GBS = 6400.0
 
@@ -304,10 +305,14 @@ def e2e_leg(args, llar, torch, stream, x, pg, local):
     llar.llar_host_register(hx)  # pinned buffers declared once, as a serving loop would
     llar.llar_host_register(hy)
     try:
-        # warm-up steps of E2E_CALLS calls each, as timed (the host's own
-        # submission rate takes a few hundred calls to settle)
-        for _ in range(args.warmup * E2E_CALLS):
+        # warm-up: W steps of E2E_CALLS calls each, as timed, and at least
+        # E2E_WARMUP_S of calls: on a fresh box the host link takes a few
+        # tenths of a second of traffic to settle (one box: 15 -> 7.3 us per
+        # call over the first 0.26 s)
+        done, t0 = 0, time.perf_counter()
+        while done < args.warmup * E2E_CALLS or time.perf_counter() - t0 < E2E_WARMUP_S:
             llar.llar_allreduce_host(hx, hy, COUNT, proto)
+            done += 1
         torch.cuda.synchronize()
         calls = max(3, args.steps // 5) * E2E_CALLS
         e0, e1 = _events(1)[0]
