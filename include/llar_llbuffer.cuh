@@ -413,6 +413,35 @@ __device__ __forceinline__ bool sen_take(const llar_llbuffer& b, int d, int q, i
   st_relaxed_v4(p, make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu));
   return true;
 }
+// Receiver d takes vector v of slot s from every source but itself at once
+// (one load per pending source per round, so the waits overlap), resetting
+// each slot as its vector arrives; x[q] receives source q's vector, x[d] is
+// left alone. False on timeout or abort.
+template <typename T, int N>
+__device__ __forceinline__ bool sen_take_peers(const llar_llbuffer& b, int d, int s, size_t v, u64 E, uint4 (&x)[N]) {
+  const uint4 ones = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  unsigned pend = ((1u << N) - 1u) & ~(1u << d);
+  Wait wt;
+  for (bool first = true;; first = false) {
+    LLB_ON_POLL_ROUND(first, pend);
+    uint4 t[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+      if ((pend >> q) & 1u) t[q] = ld_relaxed_v4(sen_vec(b, d, s, q, v));
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+      if (((pend >> q) & 1u) && !has_pattern<T>(t[q])) {
+        x[q] = t[q];
+        pend &= ~(1u << q);
+        st_relaxed_v4(sen_vec(b, d, s, q, v), ones);
+      }
+    if (pend == 0u) return true;
+    if (wt.expired(b)) {
+      fail(b, d, E);
+      return false;
+    }
+  }
+}
 
 // ============================================================ LL128 lines
 // Technique 4: a 128-byte line is 8 lanes x 16 bytes; element 0 of lane 0

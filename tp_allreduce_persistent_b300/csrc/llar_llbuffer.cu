@@ -134,23 +134,23 @@ __global__ void __launch_bounds__(512) kb_sentinel(const llar_llbuffer b, const 
         if (q != r) llb::sen_put(b, q, r, s, v, x);
     }
     for (size_t v = v0 + threadIdx.x; v < v1 && ok; v += blockDim.x) {
+      const uint4 own = load_vec(io.in[r], v, nbytes);
+      uint4 x[N];
+      if (!llb::sen_take_peers<T, N>(b, r, s, v, E, x)) {
+        ok = false;
+        break;
+      }
       float acc[PER];
 #pragma unroll
       for (int q = 0; q < N; ++q) {
-        uint4 x;
-        if (q == r) x = load_vec(io.in[r], v, nbytes);
-        else if (!llb::sen_take<T>(b, r, q, s, v, E, x)) {
-          ok = false;
-          break;
-        }
-        const unsigned w[4] = {x.x, x.y, x.z, x.w};
+        const uint4 xq = q == r ? own : x[q];
+        const unsigned w[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
           const float f = llb::Elem<T>::to_f(llb::elem_get<T>(w, i));
           acc[i] = (q == 0) ? f : __fadd_rn(acc[i], f);
         }
       }
-      if (!ok) break;
       unsigned y[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int i = 0; i < PER; ++i) llb::elem_set<T>(y, i, llb::Elem<T>::from_f(acc[i]));
