@@ -221,11 +221,20 @@ __global__ void __launch_bounds__(512) kb_ll128(const llar_llbuffer b, const Ptr
       if (s == r) continue;
       const size_t l = l0 + (i % (nl * 8)) / 8;
       const int j = (int)(i & 7);
-      u64 lo, hi;
-      if (!llb::ll_wait(b, r, s, E, (l * 8 + j) * 2, lo) || !llb::ll_wait(b, r, s, E, (l * 8 + j) * 2 + 1, hi)) {
-        ok = false;
-        break;
+      // the lane's two words, polled in the same round
+      u64 lo = 0, hi = 0;
+      bool got_lo = false, got_hi = false;
+      llb::Wait wt;
+      while (!(got_lo && got_hi)) {
+        if (!got_lo) got_lo = llb::ll_try(b, s, E, (l * 8 + j) * 2, lo);
+        if (!got_hi) got_hi = llb::ll_try(b, s, E, (l * 8 + j) * 2 + 1, hi);
+        if (!(got_lo && got_hi) && wt.expired(b)) {
+          llb::fail(b, r, E);
+          ok = false;
+          break;
+        }
       }
+      if (!ok) break;
       llb::ll128_unpack<T>(out + (size_t)s * seg, seg_len(s), l, j,
                            make_uint4((unsigned)lo, (unsigned)(lo >> 32), (unsigned)hi, (unsigned)(hi >> 32)));
     }
