@@ -62,7 +62,9 @@ extern "C" {
 typedef enum { LLAR_F32 = 0, LLAR_F16 = 1, LLAR_BF16 = 2 } llar_dtype_t;
 
 typedef enum {
-  LLAR_PROTO_AUTO = 0,          /* pick by size, see llar_select_protocol */
+  LLAR_PROTO_AUTO = 0,          /* measured choice per call kind, rank count and size:
+                                   llar_select_protocol (and _iters, _segment, _host);
+                                   never a nondeterministic protocol */
   LLAR_PROTO_LL = 1,            /* one-shot, 8 B data + 8 B flag per 16 B line (technique 1) */
   LLAR_PROTO_SENTINEL = 2,      /* one-shot, -NaN prefilled staging, chunked and
                                    double-buffered with implicit credits (techniques 2, 3) */
@@ -117,7 +119,8 @@ int llar_destroy(void);
  * at call time) are rank r's input and output, each `count` elements,
  * 16-byte aligned, owned by the caller. out[r] must not alias any in[q].
  * On return the work is queued on `stream`; out[r] holds the sum of all
- * in[q] once the stream reaches it. count == 0 is a no-op. */
+ * in[q] once the stream reaches it. count == 0 is a no-op. protocol: an
+ * llar_proto_t; LLAR_PROTO_AUTO follows llar_select_protocol. */
 int llar_allreduce(const void* const* in, void* const* out, size_t count,
                    int protocol, void* stream);
 
