@@ -64,7 +64,8 @@ typedef enum { LLAR_F32 = 0, LLAR_F16 = 1, LLAR_BF16 = 2 } llar_dtype_t;
 typedef enum {
   LLAR_PROTO_AUTO = 0,          /* measured choice per call kind, rank count and size:
                                    llar_select_protocol (and _iters, _segment, _host);
-                                   never a nondeterministic protocol */
+                                   a nondeterministic protocol only after
+                                   llar_set_auto_nondeterministic(1) */
   LLAR_PROTO_LL = 1,            /* one-shot, 8 B data + 8 B flag per 16 B line (technique 1) */
   LLAR_PROTO_SENTINEL = 2,      /* one-shot, -NaN prefilled staging, chunked and
                                    double-buffered with implicit credits (techniques 2, 3) */
@@ -312,10 +313,24 @@ int llar_select_protocol(int nranks, int dtype, size_t count);
  * direct-read two-shot beyond (8 x 64 KiB bf16 chained: LL 1.41 us per
  * AllReduce against 11.7 for the two-shot); independent AllReduces take
  * llar_select_protocol's choice, except LL up to 64 KiB with 6-8 ranks.
- * Deterministic protocols only: the LL128 forms, faster in 8-rank chains
- * from 256 KiB, are the caller's choice. LLAR_PROTO (environment) forces a
- * protocol. LLAR_PROTO_AUTO for invalid arguments. */
-int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained);
+ * Deterministic protocols only, unless `nondeterministic` != 0 (what
+ * llar_set_auto_nondeterministic(1) gives a context): then chains take the
+ * LL128 direct form where it measured fastest, 5-8 ranks at 512 KiB per
+ * rank, 8 ranks from 256 KiB, 5-6 ranks above 512 KiB (8 x 256 KiB bf16
+ * chained: 4.2 us per AllReduce against 5.6 for LL, 11.9 for the
+ * two-shot). LLAR_PROTO (environment) forces a protocol. LLAR_PROTO_AUTO
+ * for invalid arguments. */
+int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained,
+                               int nondeterministic);
+
+/* Let LLAR_PROTO_AUTO pick the LL128 direct protocol where it measured
+ * fastest (llar_select_protocol_iters with nondeterministic = 1): its
+ * atomic additions make the result depend on arrival order, within the
+ * (N-1)-ulp bound of the LL128 protocols instead of bit-exact. allow: 0
+ * (the default at llar_init) or 1; LLAR_ERR_NOT_INIT without a context,
+ * LLAR_ERR_INVALID otherwise. (The pages name the atomic protocol's
+ * nondeterminism; the switch is this library's.) */
+int llar_set_auto_nondeterministic(int allow);
 
 /* The protocol LLAR_PROTO_AUTO picks for llar_reduce_scatter
  * (reduce_scatter != 0) or llar_all_gather of `count` elements (host-only).

@@ -121,6 +121,19 @@ def test_persistent_protocol_selection():
             else:
                 assert got == llar.llar_select_protocol(n, "bf16", count), (n, kib)
     assert llar.llar_select_protocol_iters(8, "bf16", 8192, 0) == "auto"
+    # with nondeterministic protocols allowed, chains take LL128 direct where measured fastest
+    for n in range(2, 9):
+        for kib in (128, 256, 512, 1024):
+            count = kib * 512
+            got = llar.llar_select_protocol_iters(n, "bf16", count, 160, True, True)
+            atomic = n >= 5 and (kib >= 512 or (n == 8 and kib >= 256)) and (n <= 6 or kib <= 512)
+            want = "ll128_direct" if atomic else llar.llar_select_protocol_iters(n, "bf16", count, 160, True)
+            assert got == want, (n, kib)
+            # never for independent AllReduces or single calls
+            assert llar.llar_select_protocol_iters(n, "bf16", count, 200, False, True) != "ll128_direct"
+            assert llar.llar_select_protocol_iters(n, "bf16", count, 1, True, True) != "ll128_direct"
+    with pytest.raises(llar.LlarError):
+        llar.llar_set_auto_nondeterministic(True)  # needs a context
 
 
 def test_segment_protocol_selection():

@@ -212,3 +212,24 @@ def test_persistent_auto_follows_its_rule(n, kib, chain):
             want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype)
         assert llar.llar_last_launch()[0] == llar.llar_select_protocol_iters(n, dtype, count, iters, chain)
         assert np.array_equal(got, want)
+
+
+def test_nondeterministic_auto_takes_ll128_direct_in_long_chains():
+    # after llar_set_auto_nondeterministic(1), AUTO runs an 8-rank chain of
+    # 256 KiB per rank with the LL128 direct form; integers in [-2, 2] with
+    # scale 1/N keep every partial sum exact, so the chain is the oracle's
+    n, dtype, iters = 8, "bf16", 6
+    count = 256 * 512
+    x = inputs.integers(n, count, dtype, seed=9, lo=-2, hi=2)
+    want = orc.allreduce_iters(inputs.bits_of(x), iters, dtype, chain_scale=1.0 / n)
+    with context(n, dtype, 1 << 20):
+        got = allreduce_iters(x, dtype, "auto", iters, chain_scale=1.0 / n)
+        assert llar.llar_last_launch()[0] == "ll"  # deterministic by default
+        assert np.array_equal(got, want)
+        llar.llar_set_auto_nondeterministic(True)
+        got = allreduce_iters(x, dtype, "auto", iters, chain_scale=1.0 / n)
+        assert llar.llar_last_launch()[0] == "ll128_direct"
+        assert np.array_equal(got, want)
+    with context(n, dtype, 1 << 20):  # a new context starts deterministic again
+        allreduce_iters(x, dtype, "auto", iters, chain_scale=1.0 / n)
+        assert llar.llar_last_launch()[0] == "ll"

@@ -67,6 +67,7 @@ struct Ctx {
   std::map<long long, int> capacity;
   // LL launches of many AllReduces in clusters of N blocks (chosen by
   // calibrate_ll on this GPU)
+  int auto_atomic = 0;      // AUTO may take the (nondeterministic) LL128 direct form
   int ll_cluster = 0;       // LL launches of many AllReduces up to ll_cal_bytes run in clusters
   size_t ll_cal_bytes = 0;  // bytes per rank the placement was timed at
 };
@@ -169,9 +170,18 @@ int select_protocol(int n, int dtype, size_t count) {
 //   LL stays ahead up to 64 KiB with 6-8 ranks (8 x 64 KiB: 1.22 against
 //   1.67).
 // LL only up to the context's LL capacity (ll_cap).
-int select_protocol_iters(int n, int dtype, size_t count, int iters, bool chain, size_t ll_cap) {
+// With `atomic` (llar_set_auto_nondeterministic), chains also take the LL128
+// direct form where it measured fastest of all (bf16 and fp32): 5-8 ranks
+// at 512 KiB, 8 ranks from 256 KiB, 5-6 ranks above 512 KiB (5 x 1 MiB
+// bf16: 9.6 against LL 12.5); 7-8 ranks above 512 KiB keep the two-shot.
+int select_protocol_iters(int n, int dtype, size_t count, int iters, bool chain, size_t ll_cap,
+                          bool atomic = false, size_t ll128_cap = kDefaultLL128Cap) {
   if (const int f = forced_protocol()) return f;
   const size_t bytes = count * elem_bytes(dtype);
+  constexpr size_t K = 1024;
+  if (atomic && iters > 1 && chain && n >= 5 && bytes <= ll128_cap &&
+      (bytes >= 512 * K || (n == 8 && bytes >= 256 * K)) && (n <= 6 || bytes <= 512 * K))
+    return LLAR_PROTO_LL128_DIRECT;
   if (iters > 1 && chain && bytes <= ll_cap && (n <= 6 || bytes <= (512u << 10))) return LLAR_PROTO_LL;
   if (iters > 1 && chain) return LLAR_PROTO_FIXED_TWOSHOT;
   if (iters > 1 && n >= 6 && bytes <= std::min<size_t>(ll_cap, 64u << 10)) return LLAR_PROTO_LL;
@@ -522,7 +532,8 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   const size_t bytes = count * e;
   const size_t in_span = (size_t)(iters - 1) * in_stride * e + bytes;
   const size_t out_span = (size_t)(iters - 1) * out_stride * e + bytes;
-  if (proto == LLAR_PROTO_AUTO) proto = select_protocol_iters(c.n, c.dtype, count, iters, chain, c.ll_cap);
+  if (proto == LLAR_PROTO_AUTO)
+    proto = select_protocol_iters(c.n, c.dtype, count, iters, chain, c.ll_cap, c.auto_atomic != 0, c.ll128_cap);
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
   if (is_ll128(proto) && bytes > c.ll128_cap) return LLAR_ERR_TOO_LARGE;
@@ -1131,9 +1142,17 @@ int llar_select_protocol(int nranks, int dtype, size_t count) {
   return select_protocol(nranks, dtype, count);
 }
 
-int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained) {
+int llar_select_protocol_iters(int nranks, int dtype, size_t count, int iters, int chained, int nondeterministic) {
   if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks || iters < 1) return LLAR_PROTO_AUTO;
-  return select_protocol_iters(nranks, dtype, count, iters, chained != 0, kDefaultLLCap);
+  return select_protocol_iters(nranks, dtype, count, iters, chained != 0, kDefaultLLCap, nondeterministic != 0);
+}
+
+int llar_set_auto_nondeterministic(int allow) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g) return LLAR_ERR_NOT_INIT;
+  if (allow != 0 && allow != 1) return LLAR_ERR_INVALID;
+  g->auto_atomic = allow;
+  return LLAR_OK;
 }
 
 int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count) {

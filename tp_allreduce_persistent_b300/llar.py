@@ -89,7 +89,8 @@ def lib():
         "llar_select_protocol": (c_int, [c_int, c_int, c_size]),
         "llar_select_protocol_host": (c_int, [c_int, c_int, c_size]),
         "llar_select_protocol_segment": (c_int, [c_int, c_int, c_int, c_size]),
-        "llar_select_protocol_iters": (c_int, [c_int, c_int, c_size, c_int, c_int]),
+        "llar_select_protocol_iters": (c_int, [c_int, c_int, c_size, c_int, c_int, c_int]),
+        "llar_set_auto_nondeterministic": (c_int, [c_int]),
         "llar_epoch": (c_ull, []),
         "llar_sol_bound_us": (ctypes.c_double, [ctypes.c_double, ctypes.c_double]),
         "llar_sol_probe_placed": (c_int, [ctypes.POINTER(ctypes.c_double)] * 3 + [ctypes.POINTER(c_int)]),
@@ -343,10 +344,16 @@ def llar_select_protocol(nranks, dtype, count):
     return PROTOCOL_NAMES[lib().llar_select_protocol(int(nranks), _enum(DTYPES, dtype), int(count))]
 
 
-def llar_select_protocol_iters(nranks, dtype, count, iters, chained=False):
+def llar_select_protocol_iters(nranks, dtype, count, iters, chained=False, nondeterministic=False):
     """AUTO's choice for llar_allreduce_iters (default LL capacity)."""
     return PROTOCOL_NAMES[lib().llar_select_protocol_iters(int(nranks), _enum(DTYPES, dtype), int(count),
-                                                           int(iters), int(bool(chained)))]
+                                                           int(iters), int(bool(chained)),
+                                                           int(bool(nondeterministic)))]
+
+
+def llar_set_auto_nondeterministic(allow):
+    """Let AUTO pick the LL128 direct protocol where it measured fastest."""
+    _check(lib().llar_set_auto_nondeterministic(int(bool(allow))), "llar_set_auto_nondeterministic")
 
 
 def llar_select_protocol_segment(reduce_scatter, nranks, dtype, count):
