@@ -12,7 +12,8 @@ between them (the 16 KiB, 8-rank decode-step shape). L2 is flushed between
 steps by writing a 256 MiB buffer outside the timed events.
 Bandwidth leg: one step = BW_REPS AllReduces of 64 MiB per rank over 8
 ranks with the fixed-order two-shot path; its 1 GiB of inputs and outputs
-per AllReduce is larger than L2. Each launch is timed with CUDA events on
+per AllReduce is larger than L2. Each step (the latency leg's launch, the
+bandwidth leg's BW_REPS back-to-back launches) is timed with CUDA events on
 the launching stream.
 
 With --gpus N > 1 (torchrun, one process per GPU) every rank runs an
@@ -282,16 +283,21 @@ def bandwidth_leg(args, llar, torch, dev, stream, pg, local):
         llar.llar_allreduce(bw_ins, bw_outs, count, "fixed_twoshot")
     torch.cuda.synchronize()
     shape = llar.llar_last_launch()
-    bev = _events(args.steps * BW_REPS)
+    # one event pair per step around its BW_REPS launches, back to back as a
+    # stream of AllReduces runs (an event pair around every launch would add
+    # its own gap to each); 1 GiB of inputs and outputs per launch is more
+    # than L2 holds, so no launch finds the previous one's data there
+    bev = _events(args.steps)
     barrier(pg, local)
     torch.cuda.synchronize()
-    for i in range(args.steps * BW_REPS):
+    for i in range(args.steps):
         bev[i][0].record(stream)
-        llar.llar_allreduce(bw_ins, bw_outs, count, "fixed_twoshot")
+        for _ in range(BW_REPS):
+            llar.llar_allreduce(bw_ins, bw_outs, count, "fixed_twoshot")
         bev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(pg, local)
-    launch_s = statistics.mean(a.elapsed_time(b) for a, b in bev) * 1e-3
+    launch_s = statistics.mean(a.elapsed_time(b) for a, b in bev) * 1e-3 / BW_REPS
     alg_bytes = 2 * NRANKS * count * 2
     return {"gbs": alg_bytes / launch_s / 1e9, "launch_s": launch_s, "alg_bytes": alg_bytes,
             "count": count, "G": shape[1], "T": shape[2]}
