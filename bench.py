@@ -1047,7 +1047,7 @@ def main():
         return
     res = run_ours(args, world, rank, local, pg)
     if rank == 0 and res is not None:  # the llbuffer and config legs print their own line
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:  # the CPU baseline is a single-GPU figure
             us, n = time_oracle(10.0)
             us_all, n_all, cores, _, _ = time_oracle_all_cores(5.0)
             res["cpu_baseline"] = {"value": round(us, 3), "unit": "us", "cores": 1, "kind": "oracle",
