@@ -374,6 +374,8 @@ CONFIG_CASES = {
     "headline_dependent_ll": (8, "bf16", 8192, "ll", 10000, 1.0 / 8, None),
     "C3_ll128_direct_16KiB": (8, "bf16", 16 * 512, "ll128_direct", 1000, 0.0, None),
     "C2_ll": (4, "bf16", 8192, "ll", 10000, 0.0, None),
+    "C2_sentinel": (4, "bf16", 8192, "sentinel", 10000, 0.0, 16384),
+    "C5_sentinel_chain_N8": (8, "bf16", 65536, "sentinel", 160, 0.5, None),
     "C5_ll_chain_N4": (4, "bf16", 65536, "ll", 160, 0.5, None),
 }
 # fused decode layers for `--leg config --case NAME`: (ranks, tokens m, K, H), bf16
