@@ -426,7 +426,7 @@ def configs_leg(llar, torch, dev, stream):
                                          for kb in (4, 16, 64, 256, 1024)},
         C4_KEY: timed(8, "fp16", 32768, "sentinel", 1000, chunk=8192),
         "C5_chain_160_layers_128KiB_bf16_us": {
-            f"N{n}": {p: timed(n, "bf16", 65536, p, 160, chain=0.5, chunk=16384)
+            f"N{n}": {p: timed(n, "bf16", 65536, p, 160, chain=0.5)  # the library's sentinel chunk
                       for p in ("ll", "sentinel", "ll128", "ll128_direct", "fixed_oneshot", "fixed_twoshot")}
             for n in (4, 8)},
     }
