@@ -665,12 +665,15 @@ static void calibrate_ll(Ctx& c) {
   c.ll_cal_bytes = bytes;
   char* buf = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaStream_t st = nullptr;  // a stream of its own: no implicit wait on the caller's other streams
   if (cudaMalloc(&buf, 2 * (size_t)c.n * bytes) != cudaSuccess || cudaMemset(buf, 0, 2 * (size_t)c.n * bytes) != cudaSuccess ||
-      cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+      cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
     cudaGetLastError();
     if (buf) cudaFree(buf);
     if (e0) cudaEventDestroy(e0);
     if (e1) cudaEventDestroy(e1);
+    if (st) cudaStreamDestroy(st);
     return;
   }
   const void* in[llar::kMaxRanks];
@@ -684,9 +687,9 @@ static void calibrate_ll(Ctx& c) {
   for (int rep = 0; rep < 3 && ok; ++rep) {
     for (int pref = 0; pref < 2 && ok; ++pref) {
       c.ll_cluster = pref;
-      ok = cudaEventRecord(e0, 0) == cudaSuccess &&
-           run(in, out, count, LLAR_PROTO_LL, 300, 0, 0, 0.0f, 0) == LLAR_OK &&
-           cudaEventRecord(e1, 0) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
+      ok = cudaEventRecord(e0, st) == cudaSuccess &&
+           run(in, out, count, LLAR_PROTO_LL, 300, 0, 0, 0.0f, st) == LLAR_OK &&
+           cudaEventRecord(e1, st) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
       float ms = 0.f;
       if (ok && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) best[pref] = std::min(best[pref], ms);
     }
@@ -698,6 +701,7 @@ static void calibrate_ll(Ctx& c) {
                  c.ll_cluster ? "clustered" : "unclustered", best[0], best[1]);
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  cudaStreamDestroy(st);
   cudaFree(buf);
   if (c.status_host->code != 0) fill_staging(c, 0);  // a wait ran out: start the context clean
 }
