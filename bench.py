@@ -377,6 +377,7 @@ CONFIG_CASES = {
     "C2_sentinel": (4, "bf16", 8192, "sentinel", 10000, 0.0, 16384),
     "C5_sentinel_chain_N8": (8, "bf16", 65536, "sentinel", 160, 0.5, None),
     "C5_ll_chain_N4": (4, "bf16", 65536, "ll", 160, 0.5, None),
+    "C5_ll_chain_N8": (8, "bf16", 65536, "ll", 160, 0.5, None),
 }
 # fused decode layers for `--leg config --case NAME`: (ranks, tokens m, K, H), bf16
 FUSED_CASES = {
