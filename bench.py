@@ -936,19 +936,45 @@ def run_ours(args, world, rank, local, pg):
 
 
 # ------------------------------------------------------- CPU oracle timing
-def time_oracle(seconds, count=COUNT, nranks=NRANKS):
-    """Oracle AllReduces of the latency workload for ~`seconds` on one core."""
+def time_oracle(seconds, count=COUNT, nranks=NRANKS, dtype=DTYPE):
+    """Oracle AllReduces of one workload for ~`seconds` (at least one) on one core."""
     from oracle import allreduce as orc
     from tp_allreduce_persistent_b300 import inputs
-    xb = inputs.bits_of(inputs.normal(nranks, count, DTYPE, seed=1, scale=0.02))
+    xb = inputs.bits_of(inputs.normal(nranks, count, dtype, seed=1, scale=0.02))
     n = 0
     t0 = time.perf_counter()
     while True:
-        orc.allreduce(xb, DTYPE)
+        orc.allreduce(xb, dtype)
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             return el * 1e6 / n, n
+
+
+# the configurations' shapes for the CPU baseline: (ranks, dtype, elements per rank)
+ORACLE_CONFIGS = {
+    "C1_2ranks_128B_fp32": (2, "fp32", 32),
+    "C2_4ranks_16KiB_bf16": (4, "bf16", 8192),
+    "C3_8ranks_16KiB_bf16": (8, "bf16", 8192),
+    "C3_8ranks_1MiB_bf16": (8, "bf16", 1 << 19),
+    "C4_8ranks_64KiB_fp16": (8, "fp16", 32768),
+    "C5_8ranks_128KiB_bf16": (8, "bf16", 65536),
+    "bandwidth_8ranks_64MiB_bf16": (8, "bf16", 32 << 20),
+}
+
+
+def time_oracle_configs(seconds=0.5):
+    """The single-core oracle on every configuration's shape (one AllReduce;
+    a chain's steps are such AllReduces): us per AllReduce, and GB/s of
+    algorithmic bytes (2 N S) for the bandwidth shape."""
+    out = {}
+    for name, (n, dtype, count) in ORACLE_CONFIGS.items():
+        us, reps = time_oracle(seconds, count, n, dtype)
+        row = {"us": round(us, 2), "allreduces": reps}
+        if name.startswith("bandwidth"):
+            row["GB/s"] = round(2 * n * count * 2 / (us * 1e-6) / 1e9, 3)
+        out[name] = row
+    return out
 
 
 def host_cores():
@@ -1061,7 +1087,8 @@ def main():
                                                  "sample": f"{n_all} oracle AllReduces of the latency "
                                                            f"workload in ~5 s, elements split over "
                                                            f"{cores} worker processes running at "
-                                                           "once (same bits)"}}
+                                                           "once (same bits)"},
+                                   "per_config": time_oracle_configs()}
         print(json.dumps(res), flush=True)
     if pg is not None:
         pg.destroy_process_group()

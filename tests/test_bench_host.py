@@ -110,3 +110,19 @@ def test_chunked_floor_reduces_to_the_speed_of_light():
     assert abs(out["C4_chunked_floor"]["frac"] - floor / 8.0) < 1e-4
     assert out[bench.C4_KEY] == round(0.6 / 8.0, 4)
     assert "C4_chunked_floor" not in bench.per_config_roofline(per, 0.6, 6000.0)
+
+
+def test_oracle_config_timings_cover_every_shape():
+    # every configuration shape gets a single-core oracle timing (tiny sample here)
+    saved = dict(bench.ORACLE_CONFIGS)
+    try:
+        bench.ORACLE_CONFIGS.clear()
+        bench.ORACLE_CONFIGS.update({"C1_2ranks_128B_fp32": (2, "fp32", 32),
+                                     "bandwidth_8ranks_small_bf16": (8, "bf16", 4096)})
+        out = bench.time_oracle_configs(0.01)
+        assert set(out) == set(bench.ORACLE_CONFIGS)
+        assert all(v["us"] > 0 and v["allreduces"] >= 1 for v in out.values())
+        assert out["bandwidth_8ranks_small_bf16"]["GB/s"] > 0
+    finally:
+        bench.ORACLE_CONFIGS.clear()
+        bench.ORACLE_CONFIGS.update(saved)
