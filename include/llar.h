@@ -176,8 +176,11 @@ int llar_all_gather(const void* const* in, void* const* out, size_t count,
  * slot two transfers later (a one-way flow has no returning data to act
  * as the credit). protocol: LLAR_PROTO_LL (count * elem <= the LL
  * capacity, 1 MiB by default), LLAR_PROTO_SENTINEL (chunked; data must not
- * contain the all-ones element pattern) or LLAR_PROTO_AUTO (LL up to its
- * capacity, measured faster at every size there). Pointers of ranks that neither send (send) nor receive (recv)
+ * contain the all-ones element pattern), LLAR_PROTO_FIXED_ONESHOT (direct
+ * reads: the receiver's CTAs copy the sender's buffer, made ready by
+ * stream order; nothing is signalled) or LLAR_PROTO_AUTO (the direct
+ * copy: measured faster than LL and the sentinel at every size from 512 B
+ * to 8 MiB, 2 to 8 ranks, one GPU). Pointers of ranks that neither send (send) nor receive (recv)
  * may be NULL; the others are device pointers, 16-byte aligned, and no
  * receive span overlaps a send span or another receive span. The result
  * is a bit copy. Asynchronous; status codes as llar_allreduce. */

@@ -152,7 +152,7 @@ def test_random_segments_and_p2p(case):
             dst = [int(perm[(perm.index(r) + 1) % n]) for r in range(n)]  # a ring in random order
             if rng.integers(0, 2):
                 dst[int(rng.integers(0, n))] = -1
-            p = "sentinel" if proto == "sentinel" else "ll"
+            p = {"sentinel": "sentinel", "ll": "ll", "auto": "auto"}.get(proto, "fixed_oneshot")
             if p == "ll" and count * e > (1 << 20):
                 return
             recvs = filled_outputs(n, count, dtype)

@@ -53,7 +53,7 @@ MAPS = {
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
-@pytest.mark.parametrize("proto", ["ll", "sentinel"])
+@pytest.mark.parametrize("proto", ["ll", "sentinel", "fixed_oneshot"])
 @pytest.mark.parametrize("name", sorted(MAPS))
 def test_sendrecv_matches_oracle(name, proto, dtype):
     n, dst = MAPS[name]
@@ -154,23 +154,14 @@ def test_receiver_that_never_acknowledges_times_out(proto):
         assert np.array_equal(run(x, dtype, dst, proto, iters=6), expected(x, dtype, dst))
 
 
-@pytest.mark.parametrize("name", ["ring8", "pairs4"])
-def test_auto_takes_ll_up_to_its_capacity(name):
-    # AUTO: LL wherever the message fits the LL capacity (measured faster at
-    # every size there), the sentinel beyond it
+@pytest.mark.parametrize("name", ["ring8", "pairs4", "pipeline5"])
+def test_auto_takes_the_direct_copy(name):
+    # AUTO: the receiver's CTAs copy the sender's buffer (measured fastest at
+    # every size on one GPU); a bit copy at every size, ragged and empty-tail included
     n, dst = MAPS[name]
     dtype = "bf16"
-    with context(n, dtype, 1 << 20):
-        for count in (8, 32768 + 8, 131072, 1 << 19):  # up to 1 MiB per rank, the LL capacity
+    with context(n, dtype, 2 << 20):
+        for count in (1, 7, 8, 32768 + 3, 131072, (1 << 19) + 5):  # up to 1 MiB + 10 B per rank
             x = inputs.normal(1, n * count, dtype, seed=count + n).view(1, n, count)
             assert np.array_equal(run(x, dtype, dst, "auto"), expected(x, dtype, dst)), count
-            assert llar.llar_last_launch()[0] == "ll"
-
-
-def test_auto_takes_the_sentinel_beyond_the_ll_capacity():
-    n, dst, dtype = 2, [1, 0], "bf16"
-    with context(n, dtype, 2 << 20):
-        count = (1 << 19) + 8  # 1 MiB + 16 B per rank: over the 1 MiB LL capacity
-        x = inputs.normal(1, n * count, dtype, seed=5, exclude_sentinel=True).view(1, n, count)
-        assert np.array_equal(run(x, dtype, dst, "auto"), expected(x, dtype, dst))
-        assert llar.llar_last_launch()[0] == "sentinel"
+            assert llar.llar_last_launch()[0] == "fixed_oneshot"

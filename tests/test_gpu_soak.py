@@ -149,7 +149,7 @@ def test_one_context_serves_a_random_sequence(n, dtype, seed):
                 rs = op == 3
                 proto = SEG_PROTOS["rs" if rs else "ag"][int(rng.integers(0, len(SEG_PROTOS["rs" if rs else "ag"])))]
             elif op == 5:
-                proto = ["auto", "ll", "sentinel"][int(rng.integers(0, 3))]
+                proto = ["auto", "ll", "sentinel", "fixed_oneshot"][int(rng.integers(0, 4))]
             else:
                 proto = AR_PROTOS[int(rng.integers(0, len(AR_PROTOS)))]
             try:

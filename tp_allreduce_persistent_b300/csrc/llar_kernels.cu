@@ -2007,6 +2007,31 @@ __device__ __forceinline__ void post_ack(const Params& p, int me, int c, u64 val
 // LL: rank r publishes its words in its own staging (slot E & 1) as in the
 // one-shot; the receiver polls the sender's lines. Slot E & 1 held epoch
 // E - 2, so the sender first waits for the receiver's acknowledgement of it.
+// Point to point by direct reads (the fixed-order protocols' way): the
+// receiver's CTAs copy the sender's buffer, which stream order has made
+// ready, 16 bytes a thread; transfers of one launch are independent, so
+// nothing is signalled. Block b copies its share of rank b % N's transfer.
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads) k_p2p_copy(const Params p) {
+  const u64 E0 = launch_epoch(p);
+  const int r = rank_of_block(p), c = cta_of_block(p);
+  const int q = p.peer_dst[r];
+  if (q >= 0) {
+    constexpr int EB = Fmt<DT>::kBytes;
+    const size_t nbytes = p.count * EB;
+    const size_t NV = nbytes / 16;                    // whole vectors
+    const size_t total = (size_t)p.G * blockDim.x;    // this rank's threads
+    const size_t t0 = (size_t)c * blockDim.x + threadIdx.x;
+    for (int e = 0; e < p.iters; ++e) {
+      const char* src = p.in[r] + (size_t)e * p.in_stride * EB;
+      char* dst = p.out[q] + (size_t)e * p.out_stride * EB;
+      for (size_t v = t0; v < NV; v += total) st_v4(dst + v * 16, ld_stream_v4(src + v * 16));
+      for (size_t i = NV * 16 / EB + t0; i < p.count; i += total) Fmt<DT>::store(dst, i, Fmt<DT>::load(src, i));
+    }
+  }
+  finish_launch(p, E0);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kMaxThreads) k_p2p_ll(const Params p) {
   const u64 E0 = launch_epoch(p);
@@ -2288,13 +2313,16 @@ size_t bulk_smem_bytes(int nranks) { return (size_t)kBulkStages * nranks * kBulk
 size_t bulk_tile_vectors() { return kBulkTileBytes / 16; }
 
 static const void* p2p_kernel(int proto, int dtype) {
+  if (proto == 4)
+    return dtype == 0 ? (const void*)k_p2p_copy<0> : dtype == 1 ? (const void*)k_p2p_copy<1> : (const void*)k_p2p_copy<2>;
   if (proto == 1)
     return dtype == 0 ? (const void*)k_p2p_ll<0> : dtype == 1 ? (const void*)k_p2p_ll<1> : (const void*)k_p2p_ll<2>;
   return dtype == 0 ? (const void*)k_p2p_sentinel<0>
                     : dtype == 1 ? (const void*)k_p2p_sentinel<1> : (const void*)k_p2p_sentinel<2>;
 }
 cudaError_t launch_p2p(int proto, int dtype, const Params& p, int threads, cudaStream_t s) {
-  return launch_kernel(p2p_kernel(proto, dtype), p, threads, s, true);
+  // the direct copy waits on nothing: no co-residency needed
+  return launch_kernel(p2p_kernel(proto, dtype), p, threads, s, proto != 4);
 }
 int max_resident_p2p_ctas(int proto, int dtype, int threads) {
   int per = 0, sms = 0, dev = 0;

@@ -442,12 +442,15 @@ int run_p2p(const void* const* send, void* const* recv, const int* dst, size_t c
       src[d] = r;
     }
   }
-  // AUTO: LL wherever it fits. Measured on a B300 (bf16 ring, one call per
-  // launch replayed from a graph / 100 per launch): LL is ahead at every
-  // size up to its capacity, by 0.1-0.7 us up to 64 KiB and by far above
-  // (2 ranks x 1 MiB: 4.2 against 29.7 us; 8 x 256 KiB: 4.5 against 9.2)
-  if (proto == LLAR_PROTO_AUTO) proto = bytes <= c.ll_cap ? LLAR_PROTO_LL : LLAR_PROTO_SENTINEL;
-  if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_SENTINEL) return LLAR_ERR_UNSUPPORTED;
+  // AUTO: the direct copy. Measured on a B300 (bf16, a pair and an 8-rank
+  // ring, 512 B .. 8 MiB, one call per launch replayed from a graph / 50 per
+  // launch): it is ahead of LL and the sentinel at every size (512 B: 1.46
+  // against LL 2.20 us a call; 1 MiB: 2.0 against 4.2; 8 MiB: 5.2 against the
+  // sentinel's 231), since stream order already makes the sender's buffer
+  // ready and nothing has to be signalled between the virtual ranks
+  if (proto == LLAR_PROTO_AUTO) proto = LLAR_PROTO_FIXED_ONESHOT;
+  if (proto != LLAR_PROTO_LL && proto != LLAR_PROTO_SENTINEL && proto != LLAR_PROTO_FIXED_ONESHOT)
+    return LLAR_ERR_UNSUPPORTED;
   if (bytes > c.max_bytes) return LLAR_ERR_TOO_LARGE;
   if (proto == LLAR_PROTO_LL && bytes > c.ll_cap) return LLAR_ERR_TOO_LARGE;
   // participating buffers: 16-byte aligned, no receive span overlapping a
@@ -489,23 +492,34 @@ int run_p2p(const void* const* send, void* const* recv, const int* dst, size_t c
   p.iters = iters;
   p.in_stride = send_stride;
   p.out_stride = recv_stride;
-  // units of CTA work: LL 8-byte words; sentinel 16-byte vectors of a chunk
+  // units of CTA work: LL 8-byte words; sentinel 16-byte vectors of a chunk;
+  // the direct copy 16-byte vectors, two a thread, up to four CTAs an SM
   int T;
   size_t units;
   if (proto == LLAR_PROTO_LL) {
     T = 128;
     units = (bytes + 7) / 8;
+  } else if (proto == LLAR_PROTO_FIXED_ONESHOT) {
+    T = 256;
+    units = (bytes + 15) / 16;
   } else {
     T = 64;
     units = std::min(c.chunk_bytes, round_up(bytes, 16)) / 16;
   }
   int G = (int)std::max<size_t>(1, (units + T - 1) / T);
-  const int cap = llar::max_resident_p2p_ctas(proto, c.dtype, T);
-  if (cap <= 0) return LLAR_ERR_CUDA;
-  G = std::min(G, std::max(1, cap / c.n));
-  if (g_force_G > 0) G = g_force_G;
-  if (g_force_T > 0) T = g_force_T;
-  if (G * c.n > cap) return LLAR_ERR_OCCUPANCY;
+  if (proto == LLAR_PROTO_FIXED_ONESHOT)
+    G = (int)std::min<size_t>(std::max<size_t>(1, (units + 2 * T - 1) / (2 * T)), std::max(1, 4 * c.sms / c.n));
+  if (proto != LLAR_PROTO_FIXED_ONESHOT) {  // CTAs that wait on one another must all be resident
+    const int cap = llar::max_resident_p2p_ctas(proto, c.dtype, T);
+    if (cap <= 0) return LLAR_ERR_CUDA;
+    G = std::min(G, std::max(1, cap / c.n));
+    if (g_force_G > 0) G = g_force_G;
+    if (g_force_T > 0) T = g_force_T;
+    if (G * c.n > cap) return LLAR_ERR_OCCUPANCY;
+  } else {
+    if (g_force_G > 0) G = g_force_G;
+    if (g_force_T > 0) T = g_force_T;
+  }
   G = std::min(G, kFlagsGmax);
   p.G = G;
   const cudaError_t err = llar::launch_p2p(proto, c.dtype, p, T, stream);
