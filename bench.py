@@ -502,7 +502,7 @@ def configs_leg(llar, torch, dev, stream):
         finally:
             llar.llar_destroy()
 
-    out["p2p_ring_8ranks_16KiB_bf16_us"] = {p: p2p_us(p, 10000) for p in ("ll", "sentinel")}
+    out["p2p_ring_8ranks_16KiB_bf16_us"] = {p: p2p_us(p, 10000) for p in ("ll", "sentinel", "fixed_oneshot")}
     out.update(llbuffer_rows(llar, torch, dev, stream))
     sweep = {}
     for mib in (1, 4, 16, 64, 256):
