@@ -300,13 +300,16 @@ int llar_layout(int protocol, int dtype, int nranks, size_t count,
                 size_t* line_bytes, size_t* payload_elems_per_line,
                 size_t* staging_bytes_per_rank);
 
-/* The protocol LLAR_PROTO_AUTO picks for this rank count and size
- * (host-only). Measured per rank count on a B300 (one call per launch):
- * LL up to 256 KiB (2 ranks), 128 KiB (3-4), 64 KiB (5), 32 KiB (6-8);
- * then the direct-read one-shot up to 1 MiB (2-3), 512 KiB (4), 256 KiB
- * (5); then the direct-read two-shot, which streams through shared memory
- * with TMA bulk copies from 1 MiB (3-4), 512 KiB (5) or 32 KiB (6-8), and
- * never for 2 ranks. LLAR_PROTO (environment) forces a protocol. */
+/* The protocol LLAR_PROTO_AUTO picks for one AllReduce (llar_allreduce) of
+ * this rank count and size (host-only). Measured per rank count on a B300
+ * (graph-replayed single calls): a single call pays LL's cooperative
+ * launch and epoch exchange, which the direct-read one-shot does not, so
+ * the one-shot takes small messages with 2, 3, 5 and 6 ranks, LL those up
+ * to 64 KiB per rank with 4 ranks and up to 32 KiB with 7-8; the one-shot
+ * then runs up to 1 MiB (2-3 ranks), 256 KiB (4), 128 KiB (5), 64 KiB (6),
+ * and the direct-read two-shot above, streamed through shared memory with
+ * TMA bulk copies from 1 MiB (3-4 ranks), 512 KiB (5) or 32 KiB (6-8),
+ * never for 2. LLAR_PROTO (environment) forces a protocol. */
 int llar_select_protocol(int nranks, int dtype, size_t count);
 
 /* The protocol LLAR_PROTO_AUTO picks for llar_allreduce_iters (host-only;
@@ -314,8 +317,10 @@ int llar_select_protocol(int nranks, int dtype, size_t count);
  * iters == 1, llar_select_protocol. A chain (`chained` != 0) takes LL up to
  * the LL capacity, with 7-8 ranks up to 512 KiB per rank, and the
  * direct-read two-shot beyond (8 x 64 KiB bf16 chained: LL 1.41 us per
- * AllReduce against 11.7 for the two-shot); independent AllReduces take
- * llar_select_protocol's choice, except LL up to 64 KiB with 6-8 ranks.
+ * AllReduce against 11.7 for the two-shot); independent AllReduces back
+ * to back take LL up to 256 KiB per rank (2 ranks), 128 KiB (3-4), 64 KiB
+ * (5-8), the one-shot up to 1 MiB (2-3), 512 KiB (4), 256 KiB (5), and the
+ * two-shot above.
  * Deterministic protocols only, unless `nondeterministic` != 0 (what
  * llar_set_auto_nondeterministic(1) gives a context): then chains take the
  * LL128 direct form where it measured fastest, 5-8 ranks at 512 KiB per
@@ -368,8 +373,11 @@ int llar_last_launch(int* protocol, int* ctas_per_rank, int* threads, int* iters
  * page describes it: it exposes the launch-shape rule to tests). The shape
  * (CTAs per rank, threads per CTA) the runtime picks for a call of `count`
  * elements per rank with `nranks` ranks (2..8), element type `dtype` and
- * `protocol` (LLAR_PROTO_LL .. LLAR_PROTO_FIXED_TWOSHOT, not AUTO),
- * chained (`chained` != 0: llar_allreduce_iters with a chain scale) or not,
+ * `protocol` (LLAR_PROTO_LL .. LLAR_PROTO_LL128_DIRECT, not AUTO), for
+ * `chained` = 0: several AllReduces in one launch without a chain, 1: a
+ * chain (llar_allreduce_iters with a chain scale), 2: one AllReduce per
+ * launch (llar_allreduce; the fixed-order paths take a shape of their own
+ * there),
  * on a GPU with `sms` SMs and sentinel chunks of `chunk_bytes` (16 ..
  * 65536, a multiple of 16). It is the shape before a launch applies the
  * GPU's residency limit (fewer CTAs per rank when not all can be resident)

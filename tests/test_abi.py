@@ -58,20 +58,24 @@ def test_layout_constants(dtype):
 
 @pytest.mark.parametrize("n", range(2, 9))
 def test_protocol_selection_per_rank_count(n):
+    # one AllReduce per launch: LL / direct one-shot / direct two-shot
+    # thresholds in KiB per rank (ll_max 0: LL never)
     kib = 512  # bf16 elements per KiB
-    want = {2: (256, 1024), 3: (128, 1024), 4: (128, 512), 5: (64, 256), 6: (32, 32), 7: (32, 32), 8: (32, 32)}[n]
-    ll_max, one_max = want
+    ll_max, one_max = {2: (0, 1024), 3: (0, 1024), 4: (64, 256), 5: (0, 128), 6: (0, 64),
+                       7: (32, 32), 8: (32, 32)}[n]
     order = ["ll", "fixed_oneshot", "fixed_twoshot"]
     last = 0
     for k in (2, 4, 8, 16, 32, 33, 64, 65, 128, 129, 256, 257, 512, 513, 1024, 1025, 4096):
         p = llar.llar_select_protocol(n, "bf16", k * kib)
-        expect = "ll" if k <= ll_max else ("fixed_oneshot" if one_max is None or k <= one_max else "fixed_twoshot")
+        expect = "ll" if k <= ll_max else ("fixed_oneshot" if k <= one_max else "fixed_twoshot")
         assert p == expect, (n, k, p)
         assert order.index(p) >= last
         last = order.index(p)
     # the rule is in bytes: fp32 reaches each threshold at half the elements
-    assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4) == "ll"
-    assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4 + 1) != "ll"
+    if ll_max:
+        assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4) == "ll"
+        assert llar.llar_select_protocol(n, "fp32", (ll_max * 1024) // 4 + 1) != "ll"
+    assert llar.llar_select_protocol(n, "fp32", (one_max * 1024) // 4 + 1) == "fixed_twoshot"
 
 
 def test_protocol_selection_is_monotone_in_size():
@@ -111,15 +115,14 @@ def test_persistent_protocol_selection():
             ll = kib <= 1024 and (n <= 6 or kib <= 512)
             want = "ll" if ll else "fixed_twoshot"
             assert llar.llar_select_protocol_iters(n, "bf16", count, 160, True) == want, (n, kib)
-    # independent back to back: LL up to 64 KiB with 6-8 ranks, else the single-call rule
+    # independent back to back: LL up to 256 KiB (2 ranks), 128 KiB (3-4), 64 KiB (5-8),
+    # the one-shot up to 1 MiB (2-3), 512 KiB (4), 256 KiB (5), then the two-shot
+    loop = {2: (256, 1024), 3: (128, 1024), 4: (128, 512), 5: (64, 256), 6: (64, 64), 7: (64, 64), 8: (64, 64)}
     for n in range(2, 9):
-        for kib in (16, 33, 64, 65, 256):
-            count = kib * 512
-            got = llar.llar_select_protocol_iters(n, "bf16", count, 200, False)
-            if n >= 6 and kib <= 64:
-                assert got == "ll", (n, kib)
-            else:
-                assert got == llar.llar_select_protocol(n, "bf16", count), (n, kib)
+        for kib in (16, 33, 64, 65, 128, 129, 256, 257, 512, 513, 1024, 1025):
+            ll_max, one_max = loop[n]
+            want = "ll" if kib <= ll_max else ("fixed_oneshot" if kib <= one_max else "fixed_twoshot")
+            assert llar.llar_select_protocol_iters(n, "bf16", kib * 512, 200, False) == want, (n, kib)
     assert llar.llar_select_protocol_iters(8, "bf16", 8192, 0) == "auto"
     # with nondeterministic protocols allowed, chains take LL128 direct where measured fastest
     for n in range(2, 9):

@@ -99,3 +99,20 @@ def test_ll128_direct_takes_the_ll128_shapes():
         count = rng.choice([1, 63, 500, rng.randint(1, 1 << 20)])
         chained = rng.random() < 0.3
         assert shape(n, dtype, count, "ll128_direct", chained) == shape(n, dtype, count, "ll128", chained)
+
+
+def test_single_calls_of_the_fixed_paths_take_one_vector_a_thread():
+    # one AllReduce per launch: CTAs of 128 threads, one 16-byte vector a
+    # thread, while the one-shot's N reads (or a two-shot segment) stay small
+    for n, count, proto in ((4, 32768, "fixed_oneshot"), (8, 8192, "fixed_oneshot"),
+                            (4, 131072, "fixed_twoshot"), (2, 8192, "fixed_twoshot")):
+        vecs = count * 2 // 16
+        per_rank = vecs if proto == "fixed_oneshot" else -(-vecs // n)
+        g, t = shape(n, "bf16", count, proto, 2)
+        assert t == 128 and g == min(-(-per_rank // 128), SMS * 8 // n), (n, count, proto, g, t)
+        assert shape(n, "bf16", count, proto, 0)[1] == 256  # a persistent loop keeps 256-thread CTAs
+    # large one-shot messages keep the loop's shape
+    assert shape(8, "bf16", 131072, "fixed_oneshot", 2) == shape(8, "bf16", 131072, "fixed_oneshot", 0)
+    # the other protocols do not depend on it
+    for proto in ("ll", "sentinel", "ll128", "ll128_direct"):
+        assert shape(8, "bf16", 8192, proto, 2) == shape(8, "bf16", 8192, proto, 0)

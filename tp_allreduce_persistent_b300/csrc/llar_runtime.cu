@@ -116,12 +116,12 @@ bool valid_proto(int p) { return p >= LLAR_PROTO_AUTO && p <= LLAR_PROTO_LL128_D
 // the two-shot LL128 atomic protocols: the pages' LL AllGather, or reads from the owners' lines
 bool is_ll128(int p) { return p == LLAR_PROTO_LL128_ATOMIC || p == LLAR_PROTO_LL128_DIRECT; }
 
-// AUTO, per rank count. Measured on a B300 (bf16, one call per launch,
-// replayed from a CUDA graph, 2 KiB .. 4 MiB per rank): LL is fastest up
-// to ll_max, the direct-read one-shot up to oneshot_max, the direct-read
+// AUTO for AllReduces back to back in one launch, per rank count.
+// Measured on a B300 (bf16, 2 KiB .. 4 MiB per rank): LL is fastest up to
+// ll_max, the direct-read one-shot up to oneshot_max, the direct-read
 // two-shot above, streamed through shared memory with TMA bulk copies
 // from bulk_min (with 6 or more ranks already from 32 KiB: 3.3 us against
-// 3.5-6.2 us for the other paths at 64 KiB).
+// 3.5-6.2 us for the other paths at 64 KiB). bulk_min holds for every call.
 struct AutoRule {
   size_t ll_max, oneshot_max, bulk_min;
 };
@@ -133,6 +133,29 @@ AutoRule auto_rule(int n) {
     case 4: return {128 * K, 512 * K, 1 * M};
     case 5: return {64 * K, 256 * K, 512 * K};
     default: return {32 * K, 32 * K, 32 * K};
+  }
+}
+// AUTO for one AllReduce per launch (llar_allreduce), per rank count.
+// Measured on a B300 (bf16, graph-replayed single calls, 8 KiB .. 2 MiB
+// per rank), with the fixed-order paths' single-call shape (one vector a
+// thread): a single call pays the cooperative launch and the epoch
+// exchange of LL, which the direct-read one-shot (no co-residency, nothing
+// signalled) does not, so the one-shot wins small messages with 2, 3, 5
+// and 6 ranks (2 x 16 KiB: 2.22 against 2.47 us; 6 x 16 KiB: 2.71 against
+// 2.91), while LL keeps them with 4 ranks (up to 64 KiB, by ~0.1 us) and
+// 7-8 ranks (8 x 16 KiB: 2.59 against 2.96, up to 32 KiB); the two-shot
+// takes over from 512 KiB (4 ranks), 256 KiB (5), 128 KiB (6), 64 KiB
+// (7-8) and above 1 MiB (2-3).
+AutoRule auto_rule_single(int n) {
+  constexpr size_t K = 1024, M = 1024 * 1024;
+  const size_t bulk = auto_rule(n).bulk_min;
+  switch (n) {
+    case 2: return {0, 1 * M, bulk};
+    case 3: return {0, 1 * M, bulk};
+    case 4: return {64 * K, 256 * K, bulk};
+    case 5: return {0, 128 * K, bulk};
+    case 6: return {0, 64 * K, bulk};
+    default: return {32 * K, 32 * K, bulk};
   }
 }
 size_t bulk_min_bytes(int n) {
@@ -148,13 +171,15 @@ int forced_protocol() {
   return LLAR_PROTO_AUTO;
 }
 
-int select_protocol(int n, int dtype, size_t count) {
-  if (const int f = forced_protocol()) return f;
-  const size_t bytes = count * elem_bytes(dtype);
-  const AutoRule rule = auto_rule(n);
+int select_by(const AutoRule& rule, size_t bytes) {
   if (bytes <= rule.ll_max) return LLAR_PROTO_LL;
   if (bytes <= rule.oneshot_max) return LLAR_PROTO_FIXED_ONESHOT;
   return LLAR_PROTO_FIXED_TWOSHOT;
+}
+// one AllReduce per launch
+int select_protocol(int n, int dtype, size_t count) {
+  if (const int f = forced_protocol()) return f;
+  return select_by(auto_rule_single(n), count * elem_bytes(dtype));
 }
 
 // AUTO for a persistent launch of `iters` > 1 AllReduces. Measured on a
@@ -166,9 +191,8 @@ int select_protocol(int n, int dtype, size_t count) {
 //   19.9). The LL128 direct form is faster still at 8 ranks from 256 KiB
 //   (4.2 against 5.6) but its atomic sums are not bit-reproducible, so
 //   AUTO leaves it to the caller;
-// * independent AllReduces back to back: the single-call rule, except that
-//   LL stays ahead up to 64 KiB with 6-8 ranks (8 x 64 KiB: 1.22 against
-//   1.67).
+// * independent AllReduces back to back: auto_rule, except that LL stays
+//   ahead up to 64 KiB with 6-8 ranks (8 x 64 KiB: 1.22 against 1.67).
 // LL only up to the context's LL capacity (ll_cap).
 // With `atomic` (llar_set_auto_nondeterministic), chains also take the LL128
 // direct form where it measured fastest of all (bf16 and fp32): 5-8 ranks
@@ -185,6 +209,7 @@ int select_protocol_iters(int n, int dtype, size_t count, int iters, bool chain,
   if (iters > 1 && chain && bytes <= ll_cap && (n <= 6 || bytes <= (512u << 10))) return LLAR_PROTO_LL;
   if (iters > 1 && chain) return LLAR_PROTO_FIXED_TWOSHOT;
   if (iters > 1 && n >= 6 && bytes <= std::min<size_t>(ll_cap, 64u << 10)) return LLAR_PROTO_LL;
+  if (iters > 1) return select_by(auto_rule(n), bytes);
   return select_protocol(n, dtype, count);
 }
 
@@ -207,7 +232,8 @@ int select_protocol_host(int n, int dtype, size_t count) {
 }
 
 // CTAs per rank and threads per CTA for one launch.
-void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int* T) {
+// `single`: one AllReduce per launch (llar_allreduce), not a persistent loop.
+void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int* T, bool single = false) {
   const int n = c.n;
   const size_t e = c.esize;
   const int one_per_sm = std::max(1, c.sms / n);
@@ -223,10 +249,23 @@ void choose_shape(const Ctx& c, int proto, size_t count, int chain, int* G, int*
   int g = 1;
   if (proto == LLAR_PROTO_FIXED_TWOSHOT || proto == LLAR_PROTO_FIXED_ONESHOT) {
     t = 256;
-    const size_t per_rank = proto == LLAR_PROTO_FIXED_TWOSHOT ? (units + n - 1) / n : units;
-    const size_t want = (per_rank + 2 * t - 1) / (2 * t);
-    const int cap = chain ? one_per_sm : std::max(1, (c.sms * 4) / n);
-    g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)cap);
+    const bool two = proto == LLAR_PROTO_FIXED_TWOSHOT;
+    const size_t per_rank = two ? (units + n - 1) / n : units;
+    // A single call is latency-bound up to mid sizes: one vector a thread
+    // in CTAs of 128 threads. Measured, one call per launch (graph replay,
+    // bf16): one-shot 4 x 64 KiB 3.07 -> 2.55 us, 8 x 16 KiB 4.14 -> 3.03;
+    // two-shot (without TMA) 4 x 256 KiB 3.93 -> 3.05. Not where the
+    // one-shot's N reads of the message grow large (8 x 256 KiB: 4.71 ->
+    // 6.06, slower) or a two-shot segment passes 512 KiB (not measured).
+    if (single && !chain && (two ? per_rank <= 32768 : per_rank * (size_t)n <= 65536)) {
+      t = 128;
+      g = (int)std::min<size_t>(std::max<size_t>((per_rank + t - 1) / t, 1),
+                                (size_t)std::max(1, (c.sms * 8) / n));
+    } else {
+      const size_t want = (per_rank + 2 * t - 1) / (2 * t);
+      const int cap = chain ? one_per_sm : std::max(1, (c.sms * 4) / n);
+      g = (int)std::min<size_t>(std::max<size_t>(want, 1), (size_t)cap);
+    }
   } else if (proto == LLAR_PROTO_SENTINEL) {
     // every vector costs N-1 pushes, polls and resets plus a fence per
     // chunk: spread the chunk thinly over as many SMs as possible (measured,
@@ -565,7 +604,7 @@ int run(const void* const* in, void* const* out, size_t count, int proto, int it
   p.out_stride = out_stride;
 
   int G = 1, T = 128;
-  choose_shape(c, proto, count, chain, &G, &T);
+  choose_shape(c, proto, count, chain, &G, &T, iters == 1);
   const bool coop = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_SENTINEL ||
                     is_ll128(proto) || chain;
   // Thread-block clusters put the N CTAs that serve one range on one GPC.
@@ -1217,7 +1256,7 @@ int llar_debug_launch_shape(int nranks, int dtype, size_t count, int protocol, i
   int G = 1, T = 128;
   {
     std::lock_guard<std::mutex> lk(g_mu);  // a shape forced by llar_set_launch is read under the lock
-    choose_shape(c, protocol, count, chained ? 1 : 0, &G, &T);
+    choose_shape(c, protocol, count, chained == 1 ? 1 : 0, &G, &T, chained == 2);
   }
   if (ctas_per_rank) *ctas_per_rank = G;
   if (threads) *threads = T;

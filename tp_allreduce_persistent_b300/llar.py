@@ -379,10 +379,11 @@ def llar_last_launch():
 
 
 def llar_debug_launch_shape(nranks, dtype, count, protocol, chained=False, sms=148, chunk_bytes=64 << 10):
-    """(CTAs per rank, threads per CTA) the launch-shape rule picks; host arithmetic only."""
+    """(CTAs per rank, threads per CTA) the launch-shape rule picks; host arithmetic only.
+    chained: 0/False a loop of AllReduces, 1/True a chain, 2 one AllReduce per launch."""
     g, t = ctypes.c_int(), ctypes.c_int()
     _check(lib().llar_debug_launch_shape(int(nranks), _enum(DTYPES, dtype), int(count), _enum(PROTOCOLS, protocol),
-                                         int(bool(chained)), int(sms), int(chunk_bytes), ctypes.byref(g),
+                                         int(chained), int(sms), int(chunk_bytes), ctypes.byref(g),
                                          ctypes.byref(t)), "llar_debug_launch_shape")
     return g.value, t.value
 
