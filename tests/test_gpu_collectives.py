@@ -101,6 +101,41 @@ def test_all_gather(proto, dtype, n):
             assert np.array_equal(got, want), count
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_direct_read_segments_of_whole_vectors(dtype, n):
+    # segments a whole number of 16-byte vectors long take the vector path:
+    # one vector per thread in 128-thread CTAs while the grid holds them,
+    # 512-thread CTAs beyond; the last segment is ragged when count < n * per
+    e = inputs.ELEM_BYTES[dtype]
+    with context(n, dtype, 4 << 20):
+        seen = set()
+        for per in (16 // e, 1024, 40960):
+            for k in (0, 1, n - 1):
+                count = n * per - k
+                if count * e > 4 << 20:
+                    continue
+                x = inputs.normal(n, count, dtype, seed=count + 7 * n, scale=0.02, exclude_sentinel=True)
+                ins = device_inputs(x)
+                mid = filled_outputs(n, per, dtype)
+                outs = filled_outputs(n, count, dtype)
+                llar.llar_reduce_scatter(ins, mid, count, "fixed_oneshot")
+                seen.add(("rs", llar.llar_last_launch()[2]))
+                llar.llar_all_gather(mid, outs, count, "fixed_oneshot")
+                seen.add(("ag", llar.llar_last_launch()[2]))
+                torch.cuda.synchronize()
+                assert llar.llar_get_status()[0] == llar.OK
+                xb = inputs.bits_of(x)
+                want = orc.reduce_scatter(xb, dtype)
+                for s in range(n):
+                    assert np.array_equal(inputs.bits_of(mid[s])[: len(want[s])], want[s]), (count, s)
+                got = np.stack([inputs.bits_of(o) for o in outs])
+                assert np.array_equal(got, orc.allreduce(xb, dtype)), count
+        assert {("rs", 128), ("ag", 128)} <= seen, seen
+        if n == 8:
+            assert ("ag", 512) in seen, seen
+
+
 @pytest.mark.parametrize("n", [2, 7, 8])
 def test_auto_follows_the_segment_rule(n):
     # AUTO takes llar_select_protocol_segment's choice (direct reads for the

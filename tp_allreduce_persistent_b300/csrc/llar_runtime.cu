@@ -379,14 +379,16 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
 }
 
 // AUTO for the standalone halves. Measured on a B300 (bf16, one call per
-// launch replayed from a graph, 2..8 ranks, 1 KiB .. 1 MiB per rank):
-// the direct-read ReduceScatter is the fastest at every point (8 x 16 KiB:
-// 2.3 us against 4.1 for LL and 3.8 for LL128); for AllGather LL is faster
-// up to 64 KiB with 7 or 8 ranks (8 x 16 KiB: 2.8 against 3.4 us), the
-// direct reads everywhere else (4 x 16 KiB: 2.2 against 2.8).
-int select_segment_protocol(bool rs, int n, size_t bytes) {
+// launch replayed from a graph, 2..8 ranks, 1 KiB .. 64 MiB per rank): the
+// direct-read ReduceScatter is the fastest at every point (8 x 16 KiB:
+// 1.9 us against 4.0 for LL and 3.8 for LL128). The direct-read AllGather
+// is too when segments are whole 16-byte vectors (8 x 16 KiB: 1.6 against
+// 2.7 us for LL); with ragged segments it copies element by element, and LL
+// is ahead up to 64 KiB with 7 or 8 ranks (7 x 16 KiB: 2.75 against 3.0).
+int select_segment_protocol(bool rs, int n, size_t count, size_t e) {
   if (const int f = forced_protocol()) return f;
-  if (!rs && n >= 7 && bytes <= (64u << 10)) return LLAR_PROTO_LL;
+  const bool whole_vectors = (count + n - 1) / n * e % 16 == 0;
+  if (!rs && n >= 7 && count * e <= (64u << 10) && !whole_vectors) return LLAR_PROTO_LL;
   return LLAR_PROTO_FIXED_ONESHOT;
 }
 
@@ -397,7 +399,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   const size_t e = c.esize;
   const size_t bytes = count * e;
   const size_t seg_bytes = (count + c.n - 1) / c.n * e;
-  if (proto == LLAR_PROTO_AUTO) proto = select_segment_protocol(rs, c.n, bytes);
+  if (proto == LLAR_PROTO_AUTO) proto = select_segment_protocol(rs, c.n, count, e);
   // AllGather adds nothing, so the atomic LL128 protocol has no AllGather
   // of its own (its second half is LL)
   const bool ok_proto = proto == LLAR_PROTO_LL || proto == LLAR_PROTO_FIXED_ONESHOT ||
@@ -429,6 +431,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
     default: which = rs ? 2 : 3; break;
   }
   int T = proto == LLAR_PROTO_LL ? 128 : 256;
+  bool two_per_sm = false;
   size_t units;
   if (proto == LLAR_PROTO_LL) {
     const size_t words = (bytes + 7) / 8, seg_words = (seg_bytes + 7) / 8;
@@ -438,13 +441,27 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   } else if (proto == LLAR_PROTO_SENTINEL) {
     units = round_up(seg_bytes, 16) / 16;  // one thread per vector of a segment, thin CTAs
     T = units <= 512 ? 32 : 64;
+  } else if (seg_bytes % 16 == 0) {
+    // segments of whole 16-byte vectors: one vector per thread in 128-thread
+    // CTAs while the grid holds them (the single-call shape of the fixed
+    // AllReduce); beyond that 512-thread CTAs that loop. Measured on a B300
+    // (bf16, 2..8 ranks, 256 KiB .. 64 MiB per rank, CTAs of 32..512
+    // threads, 1..4 vectors a thread): two CTAs per SM over all ranks were
+    // the fastest for the ReduceScatter at every size (8 x 4 MiB: 4.8 us
+    // against 6.0 with four) and for the AllGather up to 8 MiB per rank
+    // (8 x 1 MiB: 4.0 against 5.0); larger AllGathers, which write N times
+    // what they read, kept four (8 x 16 MiB: 36 against 51 us with two)
+    units = (rs ? seg_bytes : seg_bytes * c.n) / 16;
+    T = units <= (size_t)128 * (4 * c.sms / c.n) ? 128 : 512;
+    two_per_sm = T == 512 && (rs || bytes <= (8u << 20));
   } else {
     units = rs ? seg_bytes / e : count;
   }
   int G = (int)std::max<size_t>(1, (units + T - 1) / T);
   if (proto == LLAR_PROTO_SENTINEL) G = std::max(G, 16);
   const bool waits = proto != LLAR_PROTO_FIXED_ONESHOT;
-  const int cap = waits ? llar::max_resident_segment_ctas(which, c.dtype, c.n, T) : 4 * c.sms;
+  int cap = waits || two_per_sm ? llar::max_resident_segment_ctas(which, c.dtype, c.n, T) : 4 * c.sms;
+  if (two_per_sm) cap = std::min(cap, 2 * c.sms);
   if (cap <= 0) return LLAR_ERR_CUDA;
   G = std::min(G, std::max(1, cap / c.n));
   if (g_force_G > 0) G = g_force_G;
@@ -1214,7 +1231,7 @@ int llar_set_auto_nondeterministic(int allow) {
 
 int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count) {
   if (!valid_dtype(dtype) || nranks < 2 || nranks > llar::kMaxRanks) return LLAR_PROTO_AUTO;
-  return select_segment_protocol(reduce_scatter != 0, nranks, count * elem_bytes(dtype));
+  return select_segment_protocol(reduce_scatter != 0, nranks, count, elem_bytes(dtype));
 }
 
 int llar_select_protocol_host(int nranks, int dtype, size_t count) {
