@@ -159,7 +159,10 @@ int llar_reduce_scatter(const void* const* in, void* const* out, size_t count,
  * r of a count-element vector (segments as for llar_reduce_scatter);
  * out[r]: all count elements, segment q at offset q*S. Protocols as for
  * llar_reduce_scatter except LLAR_PROTO_LL128_ATOMIC (nothing is added in
- * an AllGather: LLAR_ERR_UNSUPPORTED). */
+ * an AllGather: LLAR_ERR_UNSUPPORTED). With LLAR_PROTO_FIXED_ONESHOT and
+ * segments of whole 16-byte vectors (S * element size a multiple of 16),
+ * rank r's CTAs copy segment r into every output; otherwise rank r's CTAs
+ * copy every segment into out[r]. Either way out[r] ends up the same. */
 int llar_all_gather(const void* const* in, void* const* out, size_t count,
                     int protocol, void* stream);
 

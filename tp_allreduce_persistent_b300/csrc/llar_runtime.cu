@@ -441,19 +441,27 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   } else if (proto == LLAR_PROTO_SENTINEL) {
     units = round_up(seg_bytes, 16) / 16;  // one thread per vector of a segment, thin CTAs
     T = units <= 512 ? 32 : 64;
-  } else if (seg_bytes % 16 == 0) {
+  } else if (seg_bytes % 16 == 0 && rs) {
     // segments of whole 16-byte vectors: one vector per thread in 128-thread
     // CTAs while the grid holds them (the single-call shape of the fixed
-    // AllReduce); beyond that 512-thread CTAs that loop. Measured on a B300
-    // (bf16, 2..8 ranks, 256 KiB .. 64 MiB per rank, CTAs of 32..512
-    // threads, 1..4 vectors a thread): two CTAs per SM over all ranks were
-    // the fastest for the ReduceScatter at every size (8 x 4 MiB: 4.8 us
-    // against 6.0 with four) and for the AllGather up to 8 MiB per rank
-    // (8 x 1 MiB: 4.0 against 5.0); larger AllGathers, which write N times
-    // what they read, kept four (8 x 16 MiB: 36 against 51 us with two)
-    units = (rs ? seg_bytes : seg_bytes * c.n) / 16;
+    // AllReduce); beyond that 512-thread CTAs that loop, two per SM over all
+    // ranks. Measured on a B300 (bf16, 2..8 ranks, 256 KiB .. 64 MiB per
+    // rank, CTAs of 32..512 threads, 1..4 vectors a thread): 8 x 4 MiB took
+    // 4.8 us against 6.0 with four CTAs per SM
+    units = seg_bytes / 16;
     T = units <= (size_t)128 * (4 * c.sms / c.n) ? 128 : 512;
-    two_per_sm = T == 512 && (rs || bytes <= (8u << 20));
+    two_per_sm = T == 512;
+  } else if (seg_bytes % 16 == 0) {
+    // the AllGather's owners store every vector N times: threads over all
+    // ranks up to 512 per SM (up to 8 MiB per rank) or 512 x 8 / N per SM
+    // (larger), in 128-thread CTAs up to 8192 a rank, 256-thread ones
+    // beyond. Measured on a B300 (bf16, 2..8 ranks, 1 KiB .. 64 MiB per
+    // rank, 1..592 CTAs of 128..512 threads): the fastest shapes at each
+    // point had about these thread counts (8 x 64 MiB: 102 us with 64 x 128
+    // threads a rank, 109 with 74 x 512)
+    const size_t per_sm = bytes <= (8u << 20) ? 512 : 4096 / c.n;
+    units = std::min<size_t>(seg_bytes / 16, std::max<size_t>(1, per_sm * c.sms / c.n));
+    T = units <= 8192 ? 128 : 256;
   } else {
     units = rs ? seg_bytes / e : count;
   }
