@@ -59,9 +59,11 @@ def parse(argv=None):
     ap.add_argument("--protocol", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration table")
-    ap.add_argument("--leg", default="all", choices=["all", "latency", "bandwidth", "llbuffer", "config", "polls"],
+    ap.add_argument("--leg", default="all",
+                    choices=["all", "latency", "bandwidth", "llbuffer", "config", "polls", "segments"],
                     help="run one leg only (small profiling cases); llbuffer: the LL buffer rows alone; "
-                         "config: one row of the per-configuration table (--case)")
+                         "config: one row of the per-configuration table (--case); segments: the "
+                         "ReduceScatter / AllGather bandwidth row at --bw-mib MiB per rank")
     ap.add_argument("--case", default="C4_sentinel", choices=sorted(CONFIG_CASES) + sorted(FUSED_CASES),
                     help="row for --leg config")
     ap.add_argument("--iters", type=int, default=ITERS, help="AllReduces per latency launch")
@@ -511,7 +513,51 @@ def configs_leg(llar, torch, dev, stream):
         us = timed(8, "bf16", count, "fixed_twoshot", iters, max_bytes=mib << 20)
         sweep[f"{mib}MiB"] = {"us": us, "GB/s": round(2 * 8 * count * 2 / (us * 1e-6) / 1e9, 1)}
     out["C5_sweep_8ranks_bf16_fixed_twoshot"] = sweep
+    out[SEG_KEY] = segments_rows(llar, torch, dev, stream)
     return out
+
+
+SEG_KEY = "segments_8ranks_64MiB_bf16_fixed"
+
+
+def segments_rows(llar, torch, dev, stream, mib=64, n=8, reps=10, warmup=3):
+    """The standalone halves at bandwidth size: ReduceScatter and AllGather
+    of n ranks x `mib` MiB bf16 by direct copies (AUTO's choice there), `reps`
+    launches back to back between one event pair. Algorithmic bytes per
+    launch: ReduceScatter reads n x S and writes S, AllGather reads S and
+    writes n x S (S = mib MiB); both more than L2 holds."""
+    count = (mib << 20) // 2
+    seg = count // n
+    llar.llar_init(n, "bf16", mib << 20)
+    try:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(11)
+        full_in = [torch.randn(count, device=dev, generator=gen).to(torch.bfloat16) for _ in range(n)]
+        seg_buf = [torch.empty(seg, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        full_out = [torch.empty(count, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+        alg = (n + 1) * count * 2
+        rows = {}
+        for kind, call in (("reduce_scatter", lambda: llar.llar_reduce_scatter(full_in, seg_buf, count, "auto")),
+                           ("all_gather", lambda: llar.llar_all_gather(seg_buf, full_out, count, "auto"))):
+            for _ in range(warmup):
+                call()
+            torch.cuda.synchronize()
+            shape = llar.llar_last_launch()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            rows[kind] = {"us": round(us, 2), "GB/s": round(alg / (us * 1e-6) / 1e9, 1),
+                          "algorithmic_bytes": alg, "protocol": shape[0], "ctas_per_rank": shape[1],
+                          "threads_per_cta": shape[2]}
+        if llar.llar_get_status()[0] != llar.OK:
+            raise RuntimeError("device status not ok")
+        return rows
+    finally:
+        llar.llar_destroy()
 
 
 def mode_b_us(llar, torch, dev, stream, proto, n=4, count=8192, launches=10000):
@@ -785,7 +831,7 @@ def per_config_roofline(per_config, sol_us, hbm_gbs, l2_us=None, write_us=None):
     for key, val in per_config.items():
         if key.endswith("_us"):
             out[key] = lat(val)
-        elif key == "C5_sweep_8ranks_bf16_fixed_twoshot":
+        elif key in ("C5_sweep_8ranks_bf16_fixed_twoshot", SEG_KEY):
             out[key] = {k: round(v["GB/s"] / hbm_gbs, 4) for k, v in val.items()}
         elif key.startswith("fused_linear"):
             out[key] = {k: v["fused_frac_of_measured_hbm"] for k, v in val.items()}
@@ -819,6 +865,11 @@ def run_ours(args, world, rank, local, pg):
     if args.leg == "llbuffer":
         if rank == 0:
             print(json.dumps({"leg": "llbuffer", **llbuffer_rows(llar, torch, dev, stream)}))
+        return
+    if args.leg == "segments":
+        if rank == 0:
+            print(json.dumps({"leg": "segments", SEG_KEY: segments_rows(llar, torch, dev, stream,
+                                                                         mib=args.bw_mib)}))
         return
     if args.leg == "polls":
         if rank == 0:

@@ -112,6 +112,15 @@ def test_chunked_floor_reduces_to_the_speed_of_light():
     assert "C4_chunked_floor" not in bench.per_config_roofline(per, 0.6, 6000.0)
 
 
+def test_segment_bandwidth_rows_go_against_hbm():
+    # the ReduceScatter / AllGather bandwidth row is a bandwidth row: GB/s
+    # over the measured copy bandwidth, not the latency floor
+    per = {bench.SEG_KEY: {"reduce_scatter": {"us": 94.0, "GB/s": 6000.0},
+                           "all_gather": {"us": 103.0, "GB/s": 5400.0}}}
+    out = bench.per_config_roofline(per, 0.6, 6000.0)
+    assert out[bench.SEG_KEY] == {"reduce_scatter": 1.0, "all_gather": 0.9}
+
+
 def test_oracle_config_timings_cover_every_shape():
     # every configuration shape gets a single-core oracle timing (tiny sample here)
     saved = dict(bench.ORACLE_CONFIGS)
