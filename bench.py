@@ -868,8 +868,8 @@ def run_ours(args, world, rank, local, pg):
         return
     if args.leg == "segments":
         if rank == 0:
-            print(json.dumps({"leg": "segments", SEG_KEY: segments_rows(llar, torch, dev, stream,
-                                                                         mib=args.bw_mib)}))
+            print(json.dumps({"leg": "segments", f"segments_8ranks_{args.bw_mib}MiB_bf16_fixed":
+                              segments_rows(llar, torch, dev, stream, mib=args.bw_mib)}))
         return
     if args.leg == "polls":
         if rank == 0:
