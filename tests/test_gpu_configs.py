@@ -14,7 +14,8 @@ C5  decode chain: N=4 and 8, bf16, 65536 elements, 160 dependent
     1 .. 256 MiB per rank at N=8 with the fixed-order two-shot path, every
     element up to 64 MiB, sampled elements above.
 Also the exact launches bench.py times: 8 ranks x 16 KiB bf16, 10000
-back-to-back AllReduces of the same buffers, and 8 ranks x 64 MiB bf16
+back-to-back AllReduces of the same buffers, 8 ranks x 64 MiB bf16 (every
+element), and the ReduceScatter and AllGather of 8 ranks x 64 MiB bf16
 (every element).
 """
 
@@ -186,6 +187,34 @@ def test_bench_bandwidth_launch_exactly_every_element():
         torch.cuda.synchronize()
         assert llar.llar_get_status()[0] == llar.OK
         _full_check(ins, outs)
+
+
+def test_bench_segment_launches_exactly_every_element():
+    # the launches of bench.py's segment row: 8 ranks x 64 MiB bf16,
+    # ReduceScatter then AllGather by AUTO (direct copies, vector paths)
+    n, count = 8, 32 << 20
+    seg = count // n
+    with context(n, "bf16", 64 << 20):
+        ins = _bw_inputs(n, count)
+        mid = [torch.empty(seg, dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+        llar.llar_reduce_scatter(ins, mid, count, "auto")
+        rs_launch = llar.llar_last_launch()
+        outs = [torch.empty_like(t) for t in ins]
+        llar.llar_all_gather(mid, outs, count, "auto")
+        ag_launch = llar.llar_last_launch()
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.OK
+        assert rs_launch[0] == ag_launch[0] == "fixed_oneshot"
+        assert rs_launch[2] == 512 and ag_launch[2] == 256, (rs_launch, ag_launch)
+        xb = np.stack([inputs.bits_of(t) for t in ins])
+        want = orc.allreduce(xb, "bf16")[0]
+        del xb
+        for s in range(n):
+            bad = np.flatnonzero(inputs.bits_of(mid[s]) != want[s * seg:(s + 1) * seg])
+            assert bad.size == 0, ("reduce_scatter", s, bad[:8].tolist())
+        for r, t in enumerate(outs):
+            bad = np.flatnonzero(inputs.bits_of(t) != want)
+            assert bad.size == 0, ("all_gather", r, bad[:8].tolist())
 
 
 @pytest.mark.parametrize("n,count,chain", [(8, 65536, 0.5), (4, 65536, 0.5), (8, 32768, 0.0), (8, 8192, 0.0),
