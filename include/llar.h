@@ -347,10 +347,11 @@ int llar_set_auto_nondeterministic(int allow);
  * (reduce_scatter != 0) or llar_all_gather of `count` elements (host-only).
  * Measured per rank count on a B300 (one call per launch): the direct-read
  * ReduceScatter at every size (8 x 16 KiB bf16: 1.9 us against 4.0 for
- * LL); for AllGather the direct reads, except LL up to 64 KiB per rank
- * with 7-8 ranks when segments are not a whole number of 16-byte vectors
- * (ceil(count/N) * element size not a multiple of 16: the direct reads then
- * copy element by element). LLAR_PROTO (environment) forces a protocol.
+ * LL); for AllGather the direct copies (LLAR_PROTO_FIXED_ONESHOT),
+ * except LL up to 64 KiB per rank with 7-8 ranks when segments are not a
+ * whole number of 16-byte vectors (ceil(count/N) * element size not a
+ * multiple of 16: the direct copies then go element by element).
+ * LLAR_PROTO (environment) forces a protocol.
  * LLAR_PROTO_AUTO for an invalid rank count or dtype. */
 int llar_select_protocol_segment(int reduce_scatter, int nranks, int dtype, size_t count);
 
