@@ -138,8 +138,21 @@ def _ptr(x):
     return x.data_ptr() if hasattr(x, "data_ptr") else int(x)
 
 
+_PTR_ARRAY_TYPES = {}
+
+
 def _ptr_array(xs):
-    return (ctypes.c_void_p * len(xs))(*[x.data_ptr() if hasattr(x, "data_ptr") else int(x) for x in xs])
+    """Host array of the N pointers (tensors or integers). Marshalling only:
+    a call from Python pays this per pointer array, so the array type is
+    kept per length and tensors take the direct path."""
+    n = len(xs)
+    t = _PTR_ARRAY_TYPES.get(n)
+    if t is None:
+        t = _PTR_ARRAY_TYPES[n] = ctypes.c_void_p * n
+    try:
+        return t(*[x.data_ptr() for x in xs])
+    except AttributeError:
+        return t(*[_ptr(x) for x in xs])
 
 
 _raw_stream = None
@@ -149,12 +162,14 @@ def _stream(stream):
     """cudaStream_t of `stream`; None means torch's current stream."""
     global _raw_stream
     if stream is None:
-        import torch
-        if not torch.cuda.is_available():
-            return 0
         if _raw_stream is None:
+            import torch
+            if not torch.cuda.is_available():
+                return 0
             getter = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-            _raw_stream = (lambda: getter(torch.cuda.current_device())) if getter else \
+            device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+            torch.cuda.init()
+            _raw_stream = (lambda: getter(device())) if getter else \
                 (lambda: torch.cuda.current_stream().cuda_stream)
         return _raw_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
