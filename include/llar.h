@@ -104,11 +104,18 @@ typedef enum {
  * all-ones -NaN pattern, LL128 lines zeroed), the epoch counter and the
  * status word, and chooses the LL placement (llar_ll_placement). Tuning
  * variables of the environment (LLAR_CTAS_PER_RANK, LLAR_THREADS,
- * LLAR_CLUSTER, LLAR_BULK, LLAR_BULK_MIN_BYTES, LLAR_PDL, LLAR_SPREAD_SMEM,
- * LLAR_CHUNK_BYTES, LLAR_LL_MAX_BYTES, LLAR_LL128_MAX_BYTES, LLAR_LOG,
- * LLAR_TUNE) are read
+ * LLAR_CLUSTER, LLAR_BULK, LLAR_BULK_MIN_BYTES, LLAR_PDL, LLAR_COOP,
+ * LLAR_SPREAD_SMEM, LLAR_CHUNK_BYTES, LLAR_LL_MAX_BYTES,
+ * LLAR_LL128_MAX_BYTES, LLAR_LOG, LLAR_TUNE) are read
  * here: each context sees the environment as it is at its init, an unset
- * variable meaning the built-in default. Returns LLAR_ERR_INVALID for a
+ * variable meaning the built-in default. LLAR_COOP=0 launches the kernels
+ * whose CTAs wait on each other without the cooperative attribute: cheaper
+ * per call outside CUDA graphs (8 x 16 KiB bf16 LL queued from C: 5.0 ->
+ * 3.1 us of GPU time a call; in a graph no gain), the grid still sized to
+ * fit the GPU at once;
+ * but the launch is then not held back while other kernels occupy SMs, so
+ * its waits can run out (LLAR_ERR_TIMEOUT) if the library's launches
+ * overlap other kernels. Default 1 (cooperative). Returns LLAR_ERR_INVALID for a
  * second init without llar_destroy, LLAR_ERR_CUDA if no device or memory
  * is available. */
 int llar_init(int nranks, int dtype, size_t max_bytes);

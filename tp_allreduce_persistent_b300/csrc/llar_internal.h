@@ -81,6 +81,8 @@ struct Params {
   int clustered;              // launch in clusters of nranks blocks (one CTA per rank, same range)
   int spread_smem;            // dynamic shared memory reserved only to keep one CTA per SM
   int pdl;                    // launch as a programmatic dependent of the previous kernel
+  int no_coop;                // 1: waiting kernels launch without the cooperative attribute
+                              // (the grid is still sized to fit the GPU at once)
   int iters;
   int chain;                  // 1: next input = RNE(chain_scale * output)
   float chain_scale;

@@ -2217,9 +2217,9 @@ __global__ void __launch_bounds__(kMaxThreads) k_p2p_sentinel(const Params p) {
 
 // ============================================================ launchers
 // Launch N x G blocks: cooperative when CTAs wait on each other (the
-// runtime refuses a grid that cannot be fully resident), in clusters of N
-// blocks (one CTA of every rank for the same range, on one GPC) when
-// p.clustered is set.
+// runtime refuses a grid that cannot be fully resident and starts it only
+// when it is), unless p.no_coop; in clusters of N blocks (one CTA of every
+// rank for the same range, on one GPC) when p.clustered is set.
 static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream_t s, bool coop,
                                         cudaLaunchAttribute* at) {
   cudaLaunchConfig_t cfg = {};
@@ -2228,7 +2228,7 @@ static cudaLaunchConfig_t launch_config(const Params& p, int threads, cudaStream
   cfg.dynamicSmemBytes = p.spread_smem;
   cfg.stream = s;
   int na = 0;
-  if (coop) {
+  if (coop && !p.no_coop) {
     at[na].id = cudaLaunchAttributeCooperative;
     at[na].val.cooperative = 1;
     ++na;

@@ -77,6 +77,17 @@ Ctx* g = nullptr;
 unsigned long long g_timeout_ns = 1000000000ull;
 int g_force_G = 0, g_force_T = 0;
 int g_cluster = 1, g_log = 0, g_bulk = 1, g_spread = 0, g_pdl = 1;  // LLAR_PDL=0: plain stream order
+// LLAR_COOP=0: waiting kernels launch without the cooperative attribute.
+// Measured on a B300 (8 x 16 KiB bf16 LL, one AllReduce per call, calls
+// queued back to back from C): 4.0 -> 2.5 us of host time and 5.0 -> 3.1 us
+// of GPU time per call; from Python 8.5 -> 7.7 us (host-bound); replayed
+// from a CUDA graph no gain (2.50 -> 2.65 us), so the cooperative launch
+// stays the default. The grid is still sized by the same residency check
+// (it fits the GPU at once), but nothing holds the launch back while other
+// kernels occupy SMs: rank CTAs that start then wait for the rest, and a
+// wait that outlasts the timeout fails with LLAR_ERR_TIMEOUT. For callers
+// whose library launches overlap no other kernels.
+int g_no_coop = 0;
 size_t g_bulk_min_bytes = 0;  // LLAR_BULK_MIN_BYTES: TMA two-shot threshold for every N (0: per N)
 int g_inject_rank = -1, g_inject_mode = 0;
 int g_last_proto = 0, g_last_G = 0, g_last_T = 0, g_last_iters = 0;
@@ -376,6 +387,7 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
   p.abort_flag = reinterpret_cast<unsigned*>(c.base + c.abort_off);
   p.status = c.status_dev;
   p.pdl = g_pdl;
+  p.no_coop = g_no_coop;
 }
 
 // AUTO for the standalone halves. Measured on a B300 (bf16, one call per
@@ -823,6 +835,7 @@ int llar_init(int nranks, int dtype, size_t max_bytes) {
   g_log = (int)env_size("LLAR_LOG", 0);
   g_bulk = (int)env_size("LLAR_BULK", 1);
   g_pdl = (int)env_size("LLAR_PDL", 1);
+  g_no_coop = env_size("LLAR_COOP", 1) == 0 ? 1 : 0;
   g_bulk_min_bytes = env_size("LLAR_BULK_MIN_BYTES", 0);
   g_spread = (int)env_size("LLAR_SPREAD_SMEM", 0);
 
