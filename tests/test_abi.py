@@ -140,21 +140,14 @@ def test_persistent_protocol_selection():
 
 
 def test_segment_protocol_selection():
-    # ReduceScatter: direct reads at every size; AllGather: LL up to 64 KiB
-    # per rank with 7-8 ranks when segments are not whole 16-byte vectors,
-    # direct reads otherwise
+    # the direct copies for both halves at every size and rank count, whole
+    # 16-byte vector segments or ragged ones
     for n in range(2, 9):
         for kib in (1, 16, 64, 65, 1024):
             for dtype, e in (("bf16", 2), ("fp32", 4)):
-                for count in (kib * 1024 // e, kib * 1024 // e - 1):
+                for count in (kib * 1024 // e, kib * 1024 // e - 1, kib * 1024 // e - 8 * n + 3):
                     assert llar.llar_select_protocol_segment(True, n, dtype, count) == "fixed_oneshot"
-                    whole = -(-count // n) * e % 16 == 0
-                    want = "ll" if n >= 7 and count * e <= 65536 and not whole else "fixed_oneshot"
-                    assert llar.llar_select_protocol_segment(False, n, dtype, count) == want, (n, count, dtype)
-    assert llar.llar_select_protocol_segment(False, 8, "bf16", 8192) == "fixed_oneshot"
-    assert llar.llar_select_protocol_segment(False, 8, "bf16", 8191) == "fixed_oneshot"  # segments of 1024
-    assert llar.llar_select_protocol_segment(False, 8, "bf16", 8150) == "ll"
-    assert llar.llar_select_protocol_segment(False, 7, "bf16", 8192) == "ll"
+                    assert llar.llar_select_protocol_segment(False, n, dtype, count) == "fixed_oneshot", (n, count)
     assert llar.llar_select_protocol_segment(True, 9, "bf16", 8) == "auto"
 
 

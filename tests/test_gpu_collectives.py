@@ -141,11 +141,11 @@ def test_direct_read_segments_of_whole_vectors(dtype, n):
 
 @pytest.mark.parametrize("n", [2, 7, 8])
 def test_auto_follows_the_segment_rule(n):
-    # AUTO takes llar_select_protocol_segment's choice (direct reads for the
-    # ReduceScatter; LL for small AllGathers of 7-8 ranks) and the oracle's bits
+    # AUTO takes llar_select_protocol_segment's choice (the direct copies)
+    # and the oracle's bits, for segments of whole vectors and ragged ones
     dtype = "bf16"
     with context(n, dtype, 1 << 20):
-        for count in (512, 32768, 32768 + 8 * 7):  # 1 KiB, 64 KiB, just above 64 KiB per rank
+        for count in (512, 509, 32768, 32768 + 8 * 7 + 3):
             x = inputs.normal(n, count, dtype, seed=count + n, scale=0.02)
             ins = device_inputs(x)
             mid = filled_outputs(n, _seg_len(count, n), dtype)

@@ -1723,14 +1723,13 @@ __device__ __forceinline__ void body_rs_fixed(const Params& p, const u64 E) {
   }
 }
 
-// Fixed AllGather by direct copies. When segments are a whole number of
-// 16-byte vectors long, rank r's CTAs read segment r once and store each
-// vector to every rank's output (as the two-shot's owner does), so each
-// input byte is read once; measured on a B300 (bf16, 2..8 ranks, 16 KiB ..
-// 64 MiB per rank) this beat every rank reading all N segments into its
-// own output at all but the smallest size (8 x 1 MiB: 2.75 against 3.95
-// us; 8 x 64 MiB: 107 against 134). Otherwise rank r copies segment by
-// segment, element by element, into out[r].
+// Fixed AllGather by direct copies: rank r's CTAs read segment r once and
+// store it to every rank's output (as the two-shot's owner does), so each
+// input byte is read once; in 16-byte vectors when segments are a whole
+// number of them long, element by element otherwise. Measured on a B300
+// (bf16, 2..8 ranks, 16 KiB .. 64 MiB per rank) this beat every rank
+// reading all N segments into its own output at all but the smallest size
+// (8 x 1 MiB: 2.75 against 3.95 us; 8 x 64 MiB: 107 against 134).
 template <int DT>
 __device__ __forceinline__ void body_ag_fixed(const Params& p, const u64 E) {
   (void)E;
@@ -1740,9 +1739,9 @@ __device__ __forceinline__ void body_ag_fixed(const Params& p, const u64 E) {
   const int c = cta_of_block(p);
   const size_t stride = (size_t)p.G * blockDim.x;
   const size_t per = (p.count + N - 1) / N;
+  size_t lo, hi;
+  segment_of(p.count, N, r, lo, hi);
   if ((per * EB) % 16 == 0) {
-    size_t lo, hi;
-    segment_of(p.count, N, r, lo, hi);
     const size_t len = hi - lo, nv = (len + PER16 - 1) / PER16;
     for (size_t j = (size_t)c * blockDim.x + threadIdx.x; j < nv; j += stride) {
       const uint4 v = load_vec16<DT>(p.in[r], j, len, true);
@@ -1752,12 +1751,11 @@ __device__ __forceinline__ void body_ag_fixed(const Params& p, const u64 E) {
     }
     return;
   }
-  char* dst = p.out[r];
-  for (int q = 0; q < N; ++q) {
-    size_t lo, hi;
-    segment_of(p.count, N, q, lo, hi);
-    for (size_t g = lo + (size_t)c * blockDim.x + threadIdx.x; g < hi; g += stride)
-      Fmt<DT>::store(dst, g, Fmt<DT>::load(p.in[q], g - lo));
+  for (size_t g = lo + (size_t)c * blockDim.x + threadIdx.x; g < hi; g += stride) {
+    const unsigned v = Fmt<DT>::load(p.in[r], g - lo);
+#pragma unroll
+    for (int q = 0; q < kMaxRanks; ++q)
+      if (q < N) Fmt<DT>::store(p.out[q], g, v);
   }
 }
 

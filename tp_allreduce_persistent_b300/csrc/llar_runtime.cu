@@ -391,16 +391,17 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
 }
 
 // AUTO for the standalone halves. Measured on a B300 (bf16, one call per
-// launch replayed from a graph, 2..8 ranks, 1 KiB .. 64 MiB per rank): the
-// direct-read ReduceScatter is the fastest at every point (8 x 16 KiB:
-// 1.9 us against 4.0 for LL and 3.8 for LL128). The direct-read AllGather
-// is too when segments are whole 16-byte vectors (8 x 16 KiB: 1.6 against
-// 2.7 us for LL); with ragged segments it copies element by element, and LL
-// is ahead up to 64 KiB with 7 or 8 ranks (7 x 16 KiB: 2.75 against 3.0).
+// launch replayed from a graph, 2..8 ranks, 1 KiB .. 64 MiB per rank,
+// segments of whole 16-byte vectors and ragged ones): the direct copies are
+// the fastest at every point, ReduceScatter (8 x 16 KiB: 1.9 us against
+// 4.0 for LL and 3.8 for LL128) and AllGather (8 x 16 KiB: 1.6 against 2.7
+// for LL; ragged segments, 7 ranks x 16 KiB: 1.5 against 2.8).
 int select_segment_protocol(bool rs, int n, size_t count, size_t e) {
+  (void)rs;
+  (void)n;
+  (void)count;
+  (void)e;
   if (const int f = forced_protocol()) return f;
-  const bool whole_vectors = (count + n - 1) / n * e % 16 == 0;
-  if (!rs && n >= 7 && count * e <= (64u << 10) && !whole_vectors) return LLAR_PROTO_LL;
   return LLAR_PROTO_FIXED_ONESHOT;
 }
 
@@ -475,7 +476,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
     units = std::min<size_t>(seg_bytes / 16, std::max<size_t>(1, per_sm * c.sms / c.n));
     T = units <= 8192 ? 128 : 256;
   } else {
-    units = rs ? seg_bytes / e : count;
+    units = seg_bytes / e;  // one element per thread (the AllGather's owner stores it N times)
   }
   int G = (int)std::max<size_t>(1, (units + T - 1) / T);
   if (proto == LLAR_PROTO_SENTINEL) G = std::max(G, 16);
