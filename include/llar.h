@@ -353,7 +353,7 @@ int llar_set_auto_nondeterministic(int allow);
  * (reduce_scatter != 0) or llar_all_gather of `count` elements (host-only).
  * Measured per rank count on a B300 (one call per launch, 2..8 ranks,
  * 1 KiB .. 64 MiB): the direct copies (LLAR_PROTO_FIXED_ONESHOT) at every
- * size for both (8 x 16 KiB bf16: ReduceScatter 1.9 us against 4.0 for
+ * size for both (8 x 16 KiB bf16: ReduceScatter 1.7 us against 4.0 for
  * LL, AllGather 1.6 against 2.7). LLAR_PROTO (environment) forces a
  * protocol.
  * LLAR_PROTO_AUTO for an invalid rank count or dtype. */

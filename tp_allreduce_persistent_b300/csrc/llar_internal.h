@@ -13,6 +13,8 @@ namespace llar {
 
 constexpr int kMaxRanks = 8;
 constexpr int kMaxThreads = 512;   // threads per CTA, upper bound of every kernel
+constexpr size_t kRsVectorMinBytes = 64u << 10;  // fixed ReduceScatter: 16-byte vectors above this
+                                                 // many bytes per rank, one element a thread up to it
 constexpr int kLL128Line = 128;    // bytes per LL128 line
 constexpr int kLL128Lanes = 8;     // 16-byte lanes (threads) per line
 constexpr int kLLLine = 16;        // bytes per LL line: 8 data + 8 flag

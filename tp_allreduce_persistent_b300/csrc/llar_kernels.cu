@@ -1694,12 +1694,16 @@ __device__ __forceinline__ void body_rs_fixed(const Params& p, const u64 E) {
   segment_of(p.count, N, r, lo, hi);
   const size_t stride = (size_t)p.G * blockDim.x;
   char* dst = p.out[r];
-  if ((((p.count + N - 1) / N) * EB) % 16 == 0) {
+  if ((((p.count + N - 1) / N) * EB) % 16 == 0 && p.count * EB > kRsVectorMinBytes) {
     // every segment starts on a 16-byte boundary: one vector per item, the N
     // loads of an item in flight together. The test is the same for all
     // ranks: with segments of ragged length, a vector path for the ranks
     // whose segment happens to start aligned made the launch slower (bf16,
-    // 5 and 7 ranks x 1 .. 256 KiB: 2.9-3.9 against 1.5-2.6 us)
+    // 5 and 7 ranks x 1 .. 256 KiB: 2.9-3.9 against 1.5-2.6 us). Up to
+    // kRsVectorMinBytes per rank one element per thread is faster (more
+    // threads share the work: 8 x 16 KiB bf16 1.70 against 1.80 us, 8 x
+    // 1 KiB 1.57 against 1.84; from 256 KiB the vectors win, 8 x 1 MiB
+    // 2.56 against 3.85)
     const size_t len = hi - lo, nv = (len + PER16 - 1) / PER16;
     for (size_t j = (size_t)c * blockDim.x + threadIdx.x; j < nv; j += stride) {
       uint4 x[kMaxRanks];

@@ -393,7 +393,7 @@ void fill_params(Ctx& c, Params& p, const void* const* in, void* const* out, siz
 // AUTO for the standalone halves. Measured on a B300 (bf16, one call per
 // launch replayed from a graph, 2..8 ranks, 1 KiB .. 64 MiB per rank,
 // segments of whole 16-byte vectors and ragged ones): the direct copies are
-// the fastest at every point, ReduceScatter (8 x 16 KiB: 1.9 us against
+// the fastest at every point, ReduceScatter (8 x 16 KiB: 1.7 us against
 // 4.0 for LL and 3.8 for LL128) and AllGather (8 x 16 KiB: 1.6 against 2.7
 // for LL; ragged segments, 7 ranks x 16 KiB: 1.5 against 2.8).
 int select_segment_protocol(bool rs, int n, size_t count, size_t e) {
@@ -454,7 +454,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
   } else if (proto == LLAR_PROTO_SENTINEL) {
     units = round_up(seg_bytes, 16) / 16;  // one thread per vector of a segment, thin CTAs
     T = units <= 512 ? 32 : 64;
-  } else if (seg_bytes % 16 == 0 && rs) {
+  } else if (seg_bytes % 16 == 0 && rs && bytes > llar::kRsVectorMinBytes) {
     // segments of whole 16-byte vectors: one vector per thread in 128-thread
     // CTAs while the grid holds them (the single-call shape of the fixed
     // AllReduce); beyond that 512-thread CTAs that loop, two per SM over all
@@ -464,7 +464,7 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
     units = seg_bytes / 16;
     T = units <= (size_t)128 * (4 * c.sms / c.n) ? 128 : 512;
     two_per_sm = T == 512;
-  } else if (seg_bytes % 16 == 0) {
+  } else if (seg_bytes % 16 == 0 && !rs) {
     // the AllGather's owners store every vector N times: threads over all
     // ranks up to 512 per SM (up to 8 MiB per rank) or 512 x 8 / N per SM
     // (larger), in 128-thread CTAs up to 8192 a rank, 256-thread ones
@@ -476,7 +476,9 @@ int run_segment(bool rs, const void* const* in, void* const* out, size_t count, 
     units = std::min<size_t>(seg_bytes / 16, std::max<size_t>(1, per_sm * c.sms / c.n));
     T = units <= 8192 ? 128 : 256;
   } else {
-    units = seg_bytes / e;  // one element per thread (the AllGather's owner stores it N times)
+    // one element per thread (ReduceScatter: small or ragged segments;
+    // AllGather: ragged ones, each element stored N times by its owner)
+    units = seg_bytes / e;
   }
   int G = (int)std::max<size_t>(1, (units + T - 1) / T);
   if (proto == LLAR_PROTO_SENTINEL) G = std::max(G, 16);
