@@ -528,6 +528,8 @@ def segments_rows(llar, torch, dev, stream, mib=64, n=8, reps=10, warmup=3):
     writes n x S (S = mib MiB); both more than L2 holds."""
     count = (mib << 20) // 2
     seg = count // n
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # fresh allocations, not blocks cached by earlier rows
     llar.llar_init(n, "bf16", mib << 20)
     try:
         gen = torch.Generator(device=dev)
