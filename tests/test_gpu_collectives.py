@@ -141,6 +141,35 @@ def test_direct_read_segments_of_whole_vectors(dtype, n):
             assert ("ag", 256) in seen, seen
 
 
+@pytest.mark.parametrize("n,dtype,per,k", [(8, "bf16", 560000, 3), (5, "fp32", 2000000, 2), (2, "fp16", 4194304, 0),
+                                           (3, "bf16", 1400008, 1)])
+def test_large_all_gather_every_element(n, dtype, per, k):
+    # the owner push of whole-vector segments above 8 MiB per rank (the
+    # larger thread shape), the last segment k elements short of a whole
+    # vector
+    e = inputs.ELEM_BYTES[dtype]
+    count = n * per - k
+    assert per * e % 16 == 0 and count * e > 8 << 20
+    with context(n, dtype, count * e):
+        full = inputs.normal(1, count, dtype, seed=per + n, exclude_sentinel=True)[0]
+        bounds = [orc.shard_bounds(count, n, s) for s in range(n)]
+        ins = []
+        for lo, hi in bounds:
+            t = torch.empty(max(hi - lo, 1), dtype=full.dtype, device="cuda")
+            t[: hi - lo] = full[lo:hi].cuda()
+            ins.append(t)
+        outs = filled_outputs(n, count, dtype)
+        llar.llar_all_gather(ins, outs, count, "auto")
+        launch = llar.llar_last_launch()
+        torch.cuda.synchronize()
+        assert llar.llar_get_status()[0] == llar.OK
+        assert launch[0] == "fixed_oneshot", launch
+        want = inputs.bits_of(full)
+        for r, o in enumerate(outs):
+            bad = np.flatnonzero(inputs.bits_of(o) != want)
+            assert bad.size == 0, (r, bad[:8].tolist())
+
+
 @pytest.mark.parametrize("n", [2, 7, 8])
 def test_auto_follows_the_segment_rule(n):
     # AUTO takes llar_select_protocol_segment's choice (the direct copies)
